@@ -1,0 +1,199 @@
+/*
+ * moe.h -- C ABI of the B300 (sm_103a) top-k Mixture-of-Experts FFN forward.
+ *
+ * The layer computes, for T tokens x[t] of width d, E experts of hidden width
+ * h and k experts per token:
+ *
+ *   logits = x . W_g (+ logit_bias)                      router contraction
+ *   G(x)   = softmax(TopK(logits))                       gate, two equal forms
+ *   y[t]   = sum_{kept slots j} G_j(x_t) * E_{e_j}(x_t)   combine, slot order
+ *   E_e(x) = W2[e] . SiLU(W1[e] . x + b1[e]) + b2[e]      expert FFN
+ *   loss   = E * sum_e f_e * P_e                         load-balancing statistic
+ *
+ * as written on the page "MoE mixture-of-experts routing mechanism: principles
+ * and sparse activation" (yunthe.com): the gating formula and output sum of
+ * section "MoE architecture and gated routing principle", the TopKRouter /
+ * Expert / MoELayer listing and load_balancing_loss of section "Top-K gated
+ * routing PyTorch implementation", and the capacity rule of section "Expert
+ * Choice routing and capacity-factor tuning".  The router / executor split
+ * (indices and weights handed from the gate to an expert executor that groups
+ * tokens by expert) follows "Breaking the MoE trilemma" (0539edu.com), 3.2-3.3.
+ *
+ * Conventions for every entry point:
+ *  - Pointers are DEVICE pointers owned by the caller (CUDA allocations on the
+ *    current device), contiguous and row-major.  Activations, weights, expert
+ *    biases, row buffers and the workspace are 16-byte aligned; int32 and fp32
+ *    arrays 4-byte aligned; misalignment is MOE_ERR_INVALID_ARGUMENT.  With an
+ *    empty batch (T = 0) the token-indexed buffers may be NULL.  The library
+ *    allocates no memory, keeps no per-call state and may be called from
+ *    several host threads on different streams with different workspaces.
+ *  - Calls enqueue work on `stream` and return after host-side validation; no
+ *    call waits for the GPU except moe_device_error.  The number of kept rows M
+ *    never travels to the host: row buffers are sized for the worst case T*k.
+ *  - Host-detectable problems return an error before anything is enqueued.
+ *    Problems only the GPU can see (an expert index out of range, a row index
+ *    out of range, a non-finite logit, a pipeline wait that gave up) set bits
+ *    in a flag word at the start of the workspace; moe_device_error reads it.
+ *    Kernels never trap.  Each entry point clears the flag word first.
+ *  - Supported range: 1 <= k <= 8, k <= E <= 256, d and h multiples of 8 (and
+ *    at least 8), 0 <= T and T*k < 2^31.  Outside it: MOE_ERR_UNSUPPORTED.
+ *  - Weights use the nn.Linear orientation [out_features, in_features] stacked
+ *    with the expert index first: W_g [E,d], W1 [E,h,d], b1 [E,h], W2 [E,d,h],
+ *    b2 [E,d].  x, weights, expert biases and all row buffers share `dtype`;
+ *    logits, gate weights, the logit bias and the loss are fp32.
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st* moe_stream_t;
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARGUMENT = 1, /* NULL required pointer, misaligned pointer, bad enum */
+  MOE_ERR_UNSUPPORTED = 2,      /* sizes outside the supported range */
+  MOE_ERR_WORKSPACE = 3,        /* ws NULL or ws_bytes below the required size */
+  MOE_ERR_CUDA = 4,             /* a CUDA runtime/driver call or launch failed */
+  MOE_ERR_DEVICE = 5            /* moe_device_error: the GPU raised a flag */
+} moe_status;
+
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
+
+typedef enum {
+  /* G(x) = softmax(TopK(x . W_g)): non-kept logits at -inf, softmax over the kept
+     (gating formula, "MoE architecture and gated routing principle"). */
+  MOE_GATE_TOPK_SOFTMAX = 0,
+  /* p = softmax(x . W_g); keep the top-k of p; divide them by their sum
+     (TopKRouter.forward in the listing).  Same function as mode 0 up to rounding. */
+  MOE_GATE_SOFTMAX_TOPK_RENORM = 1
+} moe_gate;
+
+/* Bits of the device flag word (moe_device_error). */
+enum {
+  MOE_DEVERR_BAD_INDEX = 1, /* an expert index outside [0,E) reached dispatch; that slot was dropped */
+  MOE_DEVERR_BAD_ROW = 2,   /* a slot_row outside [-1, T*k) reached combine; that slot was skipped */
+  MOE_DEVERR_NONFINITE = 4, /* a router logit was NaN or infinite */
+  MOE_DEVERR_TIMEOUT = 8    /* a bounded pipeline wait inside a GEMM gave up; outputs are invalid */
+};
+
+typedef struct moe_config {
+  int64_t T;              /* tokens */
+  int32_t d;              /* model width */
+  int32_t h;              /* expert hidden width */
+  int32_t E;              /* experts */
+  int32_t k;              /* experts per token */
+  int32_t dtype;          /* moe_dtype */
+  int32_t gate;           /* moe_gate */
+  double capacity_factor; /* > 0: capacity C = ceil(T * capacity_factor / E) kept assignments
+                             per expert, later ones dropped; <= 0: no limit */
+} moe_config;
+
+/* Inputs and outputs of moe_forward.  Outputs marked "or NULL" are optional;
+   when NULL the library keeps them inside the workspace. */
+typedef struct moe_forward_args {
+  const void* x;            /* [T,d] dtype */
+  const void* w_gate;       /* [E,d] dtype */
+  const float* logit_bias;  /* [E] fp32 added to every token's logits, or NULL */
+  const void* w1;           /* [E,h,d] dtype */
+  const void* b1;           /* [E,h] dtype, or NULL for zero */
+  const void* w2;           /* [E,d,h] dtype */
+  const void* b2;           /* [E,d] dtype, or NULL for zero */
+  void* y;                  /* [T,d] dtype, required */
+  float* logits;            /* [T,E] fp32, or NULL */
+  int32_t* topk_idx;        /* [T,k], or NULL */
+  float* topk_w;            /* [T,k] fp32, or NULL */
+  int32_t* counts;          /* [E] pre-drop assignments per expert, or NULL */
+  float* aux_loss;          /* [1] fp32, or NULL */
+  int32_t* offsets;         /* [E+1], or NULL */
+  int32_t* kept_counts;     /* [E], or NULL */
+  int32_t* slot_row;        /* [T,k], or NULL */
+  int32_t* row_token;       /* [T*k], or NULL */
+  int32_t* dropped;         /* [1], or NULL */
+} moe_forward_args;
+
+/* Human-readable name of a status code.  Never NULL. */
+const char* moe_status_str(moe_status s);
+
+/* Capacity of the configuration: ceil(T * capacity_factor / E) computed in double
+   ("capacity = tokens_per_batch / num_experts * capacity_factor", rounded up to a
+   whole token), or -1 when capacity_factor <= 0.  Host only. */
+moe_status moe_capacity(const moe_config* cfg, int64_t* capacity);
+
+/* Workspace bytes moe_forward needs (includes the permuted row buffers
+   [T*k,d] + [T*k,h] + [T*k,d]).  Host only. */
+moe_status moe_workspace_size(const moe_config* cfg, size_t* bytes);
+
+/* Workspace bytes the stage calls (moe_route, moe_dispatch, moe_expert_ffn,
+   moe_combine) need: the flag word, per-chunk histograms and partial sums,
+   and the [T,E] logits when moe_route is not given a logits buffer.  Host only. */
+moe_status moe_stage_workspace_size(const moe_config* cfg, size_t* bytes);
+
+/* Router (gating formula and TopKRouter.forward):
+   logits[t,e] = sum_i x[t,i] W_g[e,i] + logit_bias[e]   (fp32 accumulation)
+   topk_idx[t,j]: the j-th largest logit of token t (ties -> lower expert index)
+   topk_w[t,j]  : gate weight of that expert by cfg->gate
+   counts[e]    : number of (t,j) with topk_idx[t,j] == e (before any capacity drop)
+   aux_loss[0]  : E * sum_e f_e P_e, f_e = mean_t softmax(logits)[t,e], P_e = counts[e]/T
+   logits may be NULL (kept in the workspace).  Selection and weights are
+   computed from exactly the fp32 logits written.  Results are deterministic. */
+moe_status moe_route(const moe_config* cfg, const void* x, const void* w_gate,
+                     const float* logit_bias, float* logits, int32_t* topk_idx, float* topk_w,
+                     int32_t* counts, float* aux_loss, void* ws, size_t ws_bytes,
+                     moe_stream_t stream);
+
+/* Dispatch (capacity section; grouping by expert id of "Breaking the MoE
+   trilemma" 3.3).  Visiting assignments token by token, slot by slot, expert e
+   hands out positions 0,1,2,...; an assignment is kept iff capacity is off or
+   its position < C.  offsets = exclusive prefix sum of kept_counts (offsets[E]
+   = M kept rows).  Kept (t,j) of expert e goes to row offsets[e] + position:
+   slot_row[t,j] = that row (-1 when dropped), row_token[row] = t (rows >= M are
+   -1), x_perm[row,:] = x[t,:].  dropped[0] = T*k - M (may be NULL).  An index
+   outside [0,E) is treated as dropped and raises MOE_DEVERR_BAD_INDEX. */
+moe_status moe_dispatch(const moe_config* cfg, const void* x, const int32_t* topk_idx,
+                        int32_t* offsets, int32_t* kept_counts, int32_t* slot_row,
+                        int32_t* row_token, int32_t* dropped, void* x_perm, void* ws,
+                        size_t ws_bytes, moe_stream_t stream);
+
+/* Expert FFN (Expert.forward) on the expert-contiguous rows:
+   for every expert e and row r in [offsets[e], offsets[e+1]):
+     h_buf[r,:]  = SiLU(x_perm[r,:] . W1[e]^T + b1[e])      (rounded to dtype)
+     y_perm[r,:] = h_buf[r,:] . W2[e]^T + b2[e]             (rounded to dtype)
+   with fp32 accumulation.  x_perm, h_buf and y_perm have T*k rows; rows >=
+   offsets[E] are neither read for results nor written.  offsets must be
+   non-decreasing with offsets[0] = 0 and offsets[E] <= T*k. */
+moe_status moe_expert_ffn(const moe_config* cfg, const void* x_perm, const int32_t* offsets,
+                          const void* w1, const void* b1, const void* w2, const void* b2,
+                          void* h_buf, void* y_perm, void* ws, size_t ws_bytes,
+                          moe_stream_t stream);
+
+/* Combine (output sum; the listing adds each slot's expert output in slot order):
+   y[t,:] = sum over j = 0..k-1 with slot_row[t,j] >= 0 of topk_w[t,j] * y_perm[slot_row[t,j],:]
+   accumulated in fp32 in slot order and rounded once; a token with every slot
+   dropped gets exactly 0.  No atomics: results are deterministic. */
+moe_status moe_combine(const moe_config* cfg, const void* y_perm, const int32_t* slot_row,
+                       const float* topk_w, void* y, void* ws, size_t ws_bytes,
+                       moe_stream_t stream);
+
+/* The whole layer: route, dispatch, expert FFN and combine on one stream, with
+   every intermediate kept in `ws` (size from moe_workspace_size).  Equivalent to
+   the four stage calls in order. */
+moe_status moe_forward(const moe_config* cfg, const moe_forward_args* args, void* ws,
+                       size_t ws_bytes, moe_stream_t stream);
+
+/* Waits for `stream`, then reads the device flag word at the start of `ws` into
+   *flags (may be NULL).  Returns MOE_ERR_DEVICE when any bit is set, MOE_OK
+   otherwise, MOE_ERR_CUDA if the wait or the read failed. */
+moe_status moe_device_error(const void* ws, moe_stream_t stream, int32_t* flags);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H */

@@ -1,0 +1,199 @@
+"""Python binding of ``libmoe.so``, the sm_103a top-k Mixture-of-Experts FFN forward.
+
+Argument marshalling only: every function here takes torch CUDA tensors (or None
+for optional arguments), passes their device pointers and the current CUDA stream
+to the C entry point of the same name declared in ``include/moe.h``, and raises
+``MoeError`` on a non-OK status.  No step of the layer runs in Python, and there is
+no fallback: if ``libmoe.so`` is missing the import of the library fails loudly.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+PKG_DIR = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG_DIR, "libmoe.so")
+
+MOE_OK = 0
+MOE_ERR_INVALID_ARGUMENT = 1
+MOE_ERR_UNSUPPORTED = 2
+MOE_ERR_WORKSPACE = 3
+MOE_ERR_CUDA = 4
+MOE_ERR_DEVICE = 5
+
+MOE_F32 = 0
+MOE_BF16 = 1
+MOE_GATE_TOPK_SOFTMAX = 0
+MOE_GATE_SOFTMAX_TOPK_RENORM = 1
+
+MOE_DEVERR_BAD_INDEX = 1
+MOE_DEVERR_BAD_ROW = 2
+MOE_DEVERR_NONFINITE = 4
+MOE_DEVERR_TIMEOUT = 8
+
+# Every C symbol include/moe.h declares.
+EXPORTED = ("moe_status_str", "moe_capacity", "moe_workspace_size", "moe_stage_workspace_size",
+            "moe_route", "moe_dispatch", "moe_expert_ffn", "moe_combine", "moe_forward",
+            "moe_device_error")
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_str(status)}")
+
+
+class MoeConfig(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int64), ("d", ctypes.c_int32), ("h", ctypes.c_int32),
+                ("E", ctypes.c_int32), ("k", ctypes.c_int32), ("dtype", ctypes.c_int32),
+                ("gate", ctypes.c_int32), ("capacity_factor", ctypes.c_double)]
+
+
+class MoeForwardArgs(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in (
+        "x", "w_gate", "logit_bias", "w1", "b1", "w2", "b2", "y", "logits", "topk_idx", "topk_w",
+        "counts", "aux_loss", "offsets", "kept_counts", "slot_row", "row_token", "dropped")]
+
+
+_lib = None
+
+
+def lib():
+    """The loaded ``libmoe.so``; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -m sparse_mixture_experts_61_b300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        P, S = ctypes.c_void_p, ctypes.c_size_t
+        cfg = ctypes.POINTER(MoeConfig)
+        L.moe_status_str.argtypes = [ctypes.c_int]
+        L.moe_status_str.restype = ctypes.c_char_p
+        L.moe_capacity.argtypes = [cfg, ctypes.POINTER(ctypes.c_int64)]
+        L.moe_workspace_size.argtypes = [cfg, ctypes.POINTER(S)]
+        L.moe_stage_workspace_size.argtypes = [cfg, ctypes.POINTER(S)]
+        L.moe_route.argtypes = [cfg, P, P, P, P, P, P, P, P, P, S, P]
+        L.moe_dispatch.argtypes = [cfg, P, P, P, P, P, P, P, P, P, S, P]
+        L.moe_expert_ffn.argtypes = [cfg, P, P, P, P, P, P, P, P, P, S, P]
+        L.moe_combine.argtypes = [cfg, P, P, P, P, P, S, P]
+        L.moe_forward.argtypes = [cfg, ctypes.POINTER(MoeForwardArgs), P, S, P]
+        L.moe_device_error.argtypes = [P, P, ctypes.POINTER(ctypes.c_int32)]
+        for name in EXPORTED:
+            if name != "moe_status_str":
+                getattr(L, name).restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def status_str(status: int) -> str:
+    return lib().moe_status_str(int(status)).decode()
+
+
+def config(T, d, h, E, k, dtype="bf16", gate=0, capacity_factor=0.0) -> MoeConfig:
+    dt = {"f32": MOE_F32, "bf16": MOE_BF16}[dtype] if isinstance(dtype, str) else int(dtype)
+    return MoeConfig(int(T), int(d), int(h), int(E), int(k), dt, int(gate),
+                     float(capacity_factor or 0.0))
+
+
+def config_from_workload(w) -> MoeConfig:
+    """Config for an object with T, d, h, E, k, dtype, gate, capacity_factor attributes."""
+    return config(w.T, w.d, w.h, w.E, w.k, w.dtype, w.gate, w.capacity_factor)
+
+
+def _p(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check(status: int, where: str) -> None:
+    if status != MOE_OK:
+        raise MoeError(status, where)
+
+
+def moe_capacity(cfg: MoeConfig) -> int:
+    v = ctypes.c_int64()
+    _check(lib().moe_capacity(ctypes.byref(cfg), ctypes.byref(v)), "moe_capacity")
+    return v.value
+
+
+def moe_workspace_size(cfg: MoeConfig) -> int:
+    v = ctypes.c_size_t()
+    _check(lib().moe_workspace_size(ctypes.byref(cfg), ctypes.byref(v)), "moe_workspace_size")
+    return v.value
+
+
+def moe_stage_workspace_size(cfg: MoeConfig) -> int:
+    v = ctypes.c_size_t()
+    _check(lib().moe_stage_workspace_size(ctypes.byref(cfg), ctypes.byref(v)),
+           "moe_stage_workspace_size")
+    return v.value
+
+
+def moe_route(cfg, x, w_gate, logit_bias, logits, topk_idx, topk_w, counts, aux_loss, ws,
+              stream=None):
+    _check(lib().moe_route(ctypes.byref(cfg), _p(x), _p(w_gate), _p(logit_bias), _p(logits),
+                           _p(topk_idx), _p(topk_w), _p(counts), _p(aux_loss), _p(ws),
+                           ws.numel() * ws.element_size(), _stream(stream)), "moe_route")
+
+
+def moe_dispatch(cfg, x, topk_idx, offsets, kept_counts, slot_row, row_token, dropped, x_perm, ws,
+                 stream=None):
+    _check(lib().moe_dispatch(ctypes.byref(cfg), _p(x), _p(topk_idx), _p(offsets),
+                              _p(kept_counts), _p(slot_row), _p(row_token), _p(dropped),
+                              _p(x_perm), _p(ws), ws.numel() * ws.element_size(),
+                              _stream(stream)), "moe_dispatch")
+
+
+def moe_expert_ffn(cfg, x_perm, offsets, w1, b1, w2, b2, h_buf, y_perm, ws, stream=None):
+    _check(lib().moe_expert_ffn(ctypes.byref(cfg), _p(x_perm), _p(offsets), _p(w1), _p(b1),
+                                _p(w2), _p(b2), _p(h_buf), _p(y_perm), _p(ws),
+                                ws.numel() * ws.element_size(), _stream(stream)),
+           "moe_expert_ffn")
+
+
+def moe_combine(cfg, y_perm, slot_row, topk_w, y, ws, stream=None):
+    _check(lib().moe_combine(ctypes.byref(cfg), _p(y_perm), _p(slot_row), _p(topk_w), _p(y),
+                             _p(ws), ws.numel() * ws.element_size(), _stream(stream)),
+           "moe_combine")
+
+
+FORWARD_INPUTS = ("x", "w_gate", "logit_bias", "w1", "b1", "w2", "b2")
+FORWARD_OUTPUTS = ("y", "logits", "topk_idx", "topk_w", "counts", "aux_loss", "offsets",
+                   "kept_counts", "slot_row", "row_token", "dropped")
+
+
+def forward_args(inputs: dict, outputs: dict) -> MoeForwardArgs:
+    """Build the moe_forward_args struct from dicts of tensors (missing keys -> NULL)."""
+    a = MoeForwardArgs()
+    for n in FORWARD_INPUTS:
+        setattr(a, n, _p(inputs.get(n)))
+    for n in FORWARD_OUTPUTS:
+        setattr(a, n, _p(outputs.get(n)))
+    return a
+
+
+def moe_forward(cfg, inputs: dict, outputs: dict, ws, stream=None, args: MoeForwardArgs = None):
+    """One call of the whole layer.  ``inputs`` holds x, w_gate, w1, w2 and optionally
+    logit_bias, b1, b2; ``outputs`` holds y and any optional outputs to expose."""
+    if args is None:
+        args = forward_args(inputs, outputs)
+    _check(lib().moe_forward(ctypes.byref(cfg), ctypes.byref(args), _p(ws),
+                             ws.numel() * ws.element_size(), _stream(stream)), "moe_forward")
+
+
+def moe_device_error(ws, stream=None) -> int:
+    """Waits for the stream and returns the device flag word (0 = clean)."""
+    v = ctypes.c_int32()
+    s = lib().moe_device_error(_p(ws), _stream(stream), ctypes.byref(v))
+    if s not in (MOE_OK, MOE_ERR_DEVICE):
+        raise MoeError(s, "moe_device_error")
+    return v.value

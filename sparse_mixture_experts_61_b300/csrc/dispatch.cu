@@ -1,0 +1,127 @@
+// Dispatch: capacity drop and expert-contiguous placement of the token rows.
+//
+// Assignments (t, j) are visited token by token, slot by slot; expert e hands out
+// positions 0, 1, 2, ... in that order and an assignment is kept iff capacity is
+// off or its position is below C ("Expert Choice routing and capacity-factor
+// tuning": capacity = tokens / experts * capacity_factor, overflow tokens are
+// rejected and pass through the residual).  Kept rows of expert e occupy
+// [offsets[e], offsets[e+1]) in token order, the grouping by expert id that
+// "Breaking the MoE trilemma" 3.3 describes.
+//
+// Parallel form of that sequential walk: tokens are cut into chunks of kChunk;
+// a per-chunk expert histogram is scanned over chunks (route.cu, finalize) to
+// give each chunk's first position per expert, and inside a chunk the position
+// of an assignment is that base plus the number of earlier assignments of the
+// chunk (in token-then-slot order) with the same expert.
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+namespace {
+
+constexpr int kThreads = 256;
+
+__global__ void __launch_bounds__(kThreads)
+    dispatch_hist_kernel(const int32_t* __restrict__ topk_idx, int64_t T, int E, int k,
+                         int32_t* __restrict__ hist, int* flags) {
+  __shared__ int s_hist[kMaxExperts];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) s_hist[e] = 0;
+  __syncthreads();
+  const int64_t base = static_cast<int64_t>(blockIdx.x) * kChunk * k;
+  const int64_t total = T * k;
+  for (int a = threadIdx.x; a < kChunk * k; a += blockDim.x) {
+    if (base + a >= total) break;
+    const int e = topk_idx[base + a];
+    if (e < 0 || e >= E)
+      raise_flag(flags, MOE_DEVERR_BAD_INDEX);
+    else
+      atomicAdd(&s_hist[e], 1);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    hist[static_cast<int64_t>(blockIdx.x) * E + e] = s_hist[e];
+}
+
+template <typename Tin>
+__global__ void __launch_bounds__(kThreads)
+    dispatch_place_kernel(const int32_t* __restrict__ topk_idx, int64_t T, int E, int k, int64_t C,
+                          const int32_t* __restrict__ chunk_base,
+                          const int32_t* __restrict__ offsets, int32_t* __restrict__ slot_row,
+                          int32_t* __restrict__ row_token, const Tin* __restrict__ x,
+                          Tin* __restrict__ x_perm, int d, int* flags) {
+  __shared__ int s_idx[kChunk * kMaxK];
+  __shared__ int s_row[kChunk * kMaxK];
+  const int c = blockIdx.x;
+  const int64_t t0 = static_cast<int64_t>(c) * kChunk;
+  const int ntok = static_cast<int>(T - t0 < kChunk ? T - t0 : kChunk);
+  const int npairs = ntok * k;
+  const int64_t base = t0 * k;
+  for (int a = threadIdx.x; a < npairs; a += blockDim.x) s_idx[a] = topk_idx[base + a];
+  __syncthreads();
+
+  for (int a = threadIdx.x; a < npairs; a += blockDim.x) {
+    const int e = s_idx[a];
+    int row = -1;
+    if (e >= 0 && e < E) {
+      int rank = 0;
+      for (int b = 0; b < a; ++b) rank += (s_idx[b] == e);
+      const int64_t pos = static_cast<int64_t>(chunk_base[static_cast<int64_t>(c) * E + e]) + rank;
+      if (C < 0 || pos < C) row = offsets[e] + static_cast<int>(pos);
+    } else {
+      raise_flag(flags, MOE_DEVERR_BAD_INDEX);
+    }
+    s_row[a] = row;
+    slot_row[base + a] = row;
+    if (row >= 0) row_token[row] = static_cast<int32_t>(t0 + a / k);
+  }
+  __syncthreads();
+
+  // Row gather, one warp per kept assignment, 16-byte vectors.
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nvec = d * static_cast<int>(sizeof(Tin)) / 16;
+  for (int a = warp; a < npairs; a += kThreads / 32) {
+    const int row = s_row[a];
+    if (row < 0) continue;
+    const uint4* src = reinterpret_cast<const uint4*>(x + (t0 + a / k) * d);
+    uint4* dst = reinterpret_cast<uint4*>(x_perm + static_cast<int64_t>(row) * d);
+    for (int v = lane; v < nvec; v += 32) dst[v] = __ldg(src + v);
+  }
+
+  // Rows past the kept total carry no token.
+  const int64_t M = offsets[E];
+  for (int64_t r = M + static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; r < T * k;
+       r += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    row_token[r] = -1;
+}
+
+}  // namespace
+
+cudaError_t launch_dispatch_hist(const int32_t* topk_idx, int64_t T, int E, int k, int32_t* hist,
+                                 int* flags, cudaStream_t stream) {
+  const int64_t nchunks = (T + kChunk - 1) / kChunk;
+  if (nchunks == 0) return cudaSuccess;
+  dispatch_hist_kernel<<<static_cast<unsigned>(nchunks), kThreads, 0, stream>>>(topk_idx, T, E, k,
+                                                                               hist, flags);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dispatch_place(int dtype, const int32_t* topk_idx, int64_t T, int E, int k,
+                                  int64_t C, const int32_t* chunk_base, const int32_t* offsets,
+                                  int32_t* slot_row, int32_t* row_token, const void* x,
+                                  void* x_perm, int d, int* flags, cudaStream_t stream) {
+  const int64_t nchunks = (T + kChunk - 1) / kChunk;
+  if (nchunks == 0) return cudaSuccess;
+  const unsigned grid = static_cast<unsigned>(nchunks);
+  if (dtype == MOE_F32)
+    dispatch_place_kernel<float><<<grid, kThreads, 0, stream>>>(
+        topk_idx, T, E, k, C, chunk_base, offsets, slot_row, row_token,
+        static_cast<const float*>(x), static_cast<float*>(x_perm), d, flags);
+  else
+    dispatch_place_kernel<__nv_bfloat16><<<grid, kThreads, 0, stream>>>(
+        topk_idx, T, E, k, C, chunk_base, offsets, slot_row, row_token,
+        static_cast<const __nv_bfloat16*>(x), static_cast<__nv_bfloat16*>(x_perm), d, flags);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,63 @@
+// Host-side launchers of the MoE kernels (one per kernel family).  Each returns
+// the launch status; none allocates or synchronises.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+// R2 + R3: softmax, top-k, gate weights, per-chunk expert histogram and per-chunk
+// softmax column sums over fp32 logits [T,E].
+cudaError_t launch_route_topk(const float* logits, int64_t T, int E, int k, int gate,
+                              int32_t* topk_idx, float* topk_w, int32_t* hist, float* psum,
+                              int* flags, cudaStream_t stream);
+
+// R4 + D1: reduces the per-chunk histograms (and, when psum != nullptr, the softmax
+// sums into the balance loss), then applies the capacity and scans the offsets.
+// Any of counts/aux/chunk_base/kept/offsets/dropped may be nullptr.
+cudaError_t launch_route_finalize(const int32_t* hist, const float* psum, int nchunks, int E,
+                                  int64_t T, int64_t C, int32_t* counts, float* aux,
+                                  int32_t* chunk_base, int32_t* kept, int32_t* offsets,
+                                  int32_t* dropped, cudaStream_t stream);
+
+// Per-chunk expert histogram of caller-provided indices (moe_dispatch on its own).
+cudaError_t launch_dispatch_hist(const int32_t* topk_idx, int64_t T, int E, int k, int32_t* hist,
+                                 int* flags, cudaStream_t stream);
+
+// D2 + D3: stable positions, capacity drop, slot_row / row_token and the row gather.
+cudaError_t launch_dispatch_place(int dtype, const int32_t* topk_idx, int64_t T, int E, int k,
+                                  int64_t C, const int32_t* chunk_base, const int32_t* offsets,
+                                  int32_t* slot_row, int32_t* row_token, const void* x,
+                                  void* x_perm, int d, int* flags, cudaStream_t stream);
+
+// C1: y[t] = sum_j w[t,j] * y_perm[slot_row[t,j]] in slot order.
+cudaError_t launch_combine(int dtype, const void* y_perm, const int32_t* slot_row,
+                           const float* topk_w, int64_t T, int d, int k, void* y, int* flags,
+                           cudaStream_t stream);
+
+// Grouped GEMM operands.  Rows of A for group g are [offsets[g], offsets[g+1]) (or
+// [0, m_rows) with one group when offsets == nullptr); B is [G][N][K] (K-major);
+// out[row, n] = act(sum_k A[row,k] * B[g][n][k] + bias[g][n]).
+struct GemmArgs {
+  const void* A;          // [rows_alloc, K]
+  int64_t rows_alloc;     // rows of the A / out buffers
+  const void* B;          // [G, N, K]
+  const void* bias;       // [G, N] in the operand dtype, or fp32 [N] (router), or nullptr
+  void* out;              // [rows_alloc, N]
+  const int32_t* offsets; // [G+1] device, or nullptr
+  int64_t m_rows;         // rows when offsets == nullptr
+  int G, N, K;
+  int* flags;
+};
+
+enum Epilogue { EPI_BIAS_SILU = 0, EPI_BIAS = 1, EPI_ROUTER_F32 = 2 };
+
+// fp32 SIMT grouped GEMM (fp32 operands, fp32 bias and output).
+cudaError_t launch_simt_gemm_f32(const GemmArgs& a, int epi, int sm_count, cudaStream_t stream);
+
+// bf16 tcgen05 grouped GEMM (bf16 operands).  EPI_BIAS_SILU / EPI_BIAS take a bf16
+// bias and write bf16; EPI_ROUTER_F32 takes an fp32 [N] bias and writes fp32.
+cudaError_t launch_tc_gemm_bf16(const GemmArgs& a, int epi, int sm_count, cudaStream_t stream);
+
+}  // namespace moe

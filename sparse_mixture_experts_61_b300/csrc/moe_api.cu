@@ -1,0 +1,383 @@
+// C ABI of the MoE FFN forward (include/moe.h): argument validation, workspace
+// carving and the launch sequence of every entry point.  Nothing here allocates
+// device memory, synchronises (except moe_device_error) or keeps per-call state.
+
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+
+#include "../../include/moe.h"
+#include "common.cuh"
+#include "kernels.h"
+
+#define MOE_EXPORT extern "C" __attribute__((visibility("default")))
+
+namespace moe {
+namespace {
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t v) { return (v + kAlign - 1) & ~(kAlign - 1); }
+
+// Workspace layout: [flags | per-chunk hist | chunk bases | per-chunk softmax sums |
+// logits] = the stage workspace, then the forward-only intermediates.
+struct Layout {
+  size_t flags, hist, chunk_base, psum, logits, stage_end;
+  size_t idx, w, counts, aux, offsets, kept, slot_row, row_token, dropped, x_perm, h_buf, y_perm;
+  size_t total;
+  int64_t nchunks;
+};
+
+Layout make_layout(const moe_config& c) {
+  Layout L{};
+  const int64_t T = c.T, E = c.E, k = c.k;
+  const size_t s = c.dtype == MOE_F32 ? 4 : 2;
+  L.nchunks = (T + kChunk - 1) / kChunk;
+  size_t o = 0;
+  L.flags = o; o += kAlign;
+  L.hist = o; o = align_up(o + L.nchunks * E * 4);
+  L.chunk_base = o; o = align_up(o + L.nchunks * E * 4);
+  L.psum = o; o = align_up(o + L.nchunks * E * 4);
+  L.logits = o; o = align_up(o + T * E * 4);
+  L.stage_end = o;
+  L.idx = o; o = align_up(o + T * k * 4);
+  L.w = o; o = align_up(o + T * k * 4);
+  L.counts = o; o = align_up(o + E * 4);
+  L.aux = o; o = align_up(o + 4);
+  L.offsets = o; o = align_up(o + (E + 1) * 4);
+  L.kept = o; o = align_up(o + E * 4);
+  L.slot_row = o; o = align_up(o + T * k * 4);
+  L.row_token = o; o = align_up(o + T * k * 4);
+  L.dropped = o; o = align_up(o + 4);
+  L.x_perm = o; o = align_up(o + T * k * c.d * s);
+  L.h_buf = o; o = align_up(o + T * k * c.h * s);
+  L.y_perm = o; o = align_up(o + T * k * c.d * s);
+  L.total = o;
+  return L;
+}
+
+moe_status check_config(const moe_config* c) {
+  if (!c) return MOE_ERR_INVALID_ARGUMENT;
+  if (c->dtype != MOE_F32 && c->dtype != MOE_BF16) return MOE_ERR_INVALID_ARGUMENT;
+  if (c->gate != MOE_GATE_TOPK_SOFTMAX && c->gate != MOE_GATE_SOFTMAX_TOPK_RENORM)
+    return MOE_ERR_INVALID_ARGUMENT;
+  if (!std::isfinite(c->capacity_factor)) return MOE_ERR_INVALID_ARGUMENT;
+  if (c->T < 0 || c->k < 1 || c->k > kMaxK || c->E < c->k || c->E > kMaxExperts)
+    return MOE_ERR_UNSUPPORTED;
+  if (c->d < 8 || c->d % 8 != 0 || c->h < 8 || c->h % 8 != 0) return MOE_ERR_UNSUPPORTED;
+  if (c->T * static_cast<int64_t>(c->k) >= (int64_t{1} << 31)) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+int64_t capacity_of(const moe_config& c) {
+  if (!(c.capacity_factor > 0.0)) return -1;
+  return static_cast<int64_t>(
+      std::ceil(static_cast<double>(c.T) * c.capacity_factor / static_cast<double>(c.E)));
+}
+
+bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool al4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+// Required 16-byte-aligned buffer.
+bool need16(const void* p) { return p != nullptr && al16(p); }
+// Required 4-byte-aligned array.
+bool need4(const void* p) { return p != nullptr && al4(p); }
+// Optional arrays: NULL or aligned.
+bool opt16(const void* p) { return p == nullptr || al16(p); }
+bool opt4(const void* p) { return p == nullptr || al4(p); }
+// Token-indexed buffers are required unless the batch is empty (T = 0), where they
+// hold no element and may be NULL.
+bool tok16(const moe_config& c, const void* p) { return c.T == 0 ? opt16(p) : need16(p); }
+bool tok4(const moe_config& c, const void* p) { return c.T == 0 ? opt4(p) : need4(p); }
+
+int sm_count() {
+  static std::atomic<int> cached[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev < 0 || dev >= 64) return 0;
+  int n = cached[dev].load(std::memory_order_relaxed);
+  if (n > 0) return n;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  cached[dev].store(n, std::memory_order_relaxed);
+  return n;
+}
+
+template <typename T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+#define MOE_CUDA(call)                            \
+  do {                                            \
+    if ((call) != cudaSuccess) return MOE_ERR_CUDA; \
+  } while (0)
+
+// R1: logits[T,E] (fp32) = x . W_g^T + logit_bias.
+moe_status run_router_logits(const moe_config& c, const void* x, const void* w_gate,
+                             const float* logit_bias, float* logits, int* flags, int sms,
+                             cudaStream_t st) {
+  GemmArgs g{};
+  g.A = x;
+  g.rows_alloc = c.T;
+  g.B = w_gate;
+  g.bias = logit_bias;
+  g.out = logits;
+  g.offsets = nullptr;
+  g.m_rows = c.T;
+  g.G = 1;
+  g.N = c.E;
+  g.K = c.d;
+  g.flags = flags;
+  MOE_CUDA(c.dtype == MOE_F32 ? launch_simt_gemm_f32(g, EPI_ROUTER_F32, sms, st)
+                              : launch_tc_gemm_bf16(g, EPI_ROUTER_F32, sms, st));
+  return MOE_OK;
+}
+
+// G1 + G2 over the expert-contiguous rows.
+moe_status run_expert_ffn(const moe_config& c, const void* x_perm, const int32_t* offsets,
+                          const void* w1, const void* b1, const void* w2, const void* b2,
+                          void* h_buf, void* y_perm, int* flags, int sms, cudaStream_t st) {
+  GemmArgs g1{};
+  g1.A = x_perm;
+  g1.rows_alloc = c.T * c.k;
+  g1.B = w1;
+  g1.bias = b1;
+  g1.out = h_buf;
+  g1.offsets = offsets;
+  g1.G = c.E;
+  g1.N = c.h;
+  g1.K = c.d;
+  g1.flags = flags;
+  GemmArgs g2 = g1;
+  g2.A = h_buf;
+  g2.B = w2;
+  g2.bias = b2;
+  g2.out = y_perm;
+  g2.N = c.d;
+  g2.K = c.h;
+  if (c.dtype == MOE_F32) {
+    MOE_CUDA(launch_simt_gemm_f32(g1, EPI_BIAS_SILU, sms, st));
+    MOE_CUDA(launch_simt_gemm_f32(g2, EPI_BIAS, sms, st));
+  } else {
+    MOE_CUDA(launch_tc_gemm_bf16(g1, EPI_BIAS_SILU, sms, st));
+    MOE_CUDA(launch_tc_gemm_bf16(g2, EPI_BIAS, sms, st));
+  }
+  return MOE_OK;
+}
+
+moe_status zero_async(void* p, size_t bytes, cudaStream_t st) {
+  if (p && bytes) MOE_CUDA(cudaMemsetAsync(p, 0, bytes, st));
+  return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+MOE_EXPORT const char* moe_status_str(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARGUMENT: return "MOE_ERR_INVALID_ARGUMENT";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+    case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+    case MOE_ERR_DEVICE: return "MOE_ERR_DEVICE";
+  }
+  return "MOE_ERR_UNKNOWN";
+}
+
+MOE_EXPORT moe_status moe_capacity(const moe_config* cfg, int64_t* capacity) {
+  moe_status s = check_config(cfg);
+  if (s != MOE_OK) return s;
+  if (!capacity) return MOE_ERR_INVALID_ARGUMENT;
+  *capacity = capacity_of(*cfg);
+  return MOE_OK;
+}
+
+MOE_EXPORT moe_status moe_workspace_size(const moe_config* cfg, size_t* bytes) {
+  moe_status s = check_config(cfg);
+  if (s != MOE_OK) return s;
+  if (!bytes) return MOE_ERR_INVALID_ARGUMENT;
+  *bytes = make_layout(*cfg).total;
+  return MOE_OK;
+}
+
+MOE_EXPORT moe_status moe_stage_workspace_size(const moe_config* cfg, size_t* bytes) {
+  moe_status s = check_config(cfg);
+  if (s != MOE_OK) return s;
+  if (!bytes) return MOE_ERR_INVALID_ARGUMENT;
+  *bytes = make_layout(*cfg).stage_end;
+  return MOE_OK;
+}
+
+MOE_EXPORT moe_status moe_route(const moe_config* cfg, const void* x, const void* w_gate,
+                                const float* logit_bias, float* logits, int32_t* topk_idx,
+                                float* topk_w, int32_t* counts, float* aux_loss, void* ws,
+                                size_t ws_bytes, moe_stream_t stream) {
+  moe_status s = check_config(cfg);
+  if (s != MOE_OK) return s;
+  const moe_config& c = *cfg;
+  if (!tok16(c, x) || !need16(w_gate) || !opt4(logit_bias) || !opt16(logits) ||
+      !tok4(c, topk_idx) || !tok4(c, topk_w) || !opt4(counts) || !opt4(aux_loss))
+    return MOE_ERR_INVALID_ARGUMENT;
+  const Layout L = make_layout(c);
+  if (!ws || !al16(ws) || ws_bytes < L.stage_end) return MOE_ERR_WORKSPACE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int* flags = at<int>(ws, L.flags);
+  MOE_CUDA(cudaMemsetAsync(flags, 0, sizeof(int), st));
+  if (c.T == 0) {
+    if ((s = zero_async(counts, sizeof(int32_t) * c.E, st)) != MOE_OK) return s;
+    return zero_async(aux_loss, sizeof(float), st);
+  }
+  const int sms = sm_count();
+  if (sms <= 0) return MOE_ERR_CUDA;
+  float* lg = logits ? logits : at<float>(ws, L.logits);
+  if ((s = run_router_logits(c, x, w_gate, logit_bias, lg, flags, sms, st)) != MOE_OK) return s;
+  MOE_CUDA(launch_route_topk(lg, c.T, c.E, c.k, c.gate, topk_idx, topk_w, at<int32_t>(ws, L.hist),
+                             at<float>(ws, L.psum), flags, st));
+  if (counts || aux_loss)
+    MOE_CUDA(launch_route_finalize(at<int32_t>(ws, L.hist), at<float>(ws, L.psum),
+                                   static_cast<int>(L.nchunks), c.E, c.T, -1, counts, aux_loss,
+                                   nullptr, nullptr, nullptr, nullptr, st));
+  return MOE_OK;
+}
+
+MOE_EXPORT moe_status moe_dispatch(const moe_config* cfg, const void* x, const int32_t* topk_idx,
+                                   int32_t* offsets, int32_t* kept_counts, int32_t* slot_row,
+                                   int32_t* row_token, int32_t* dropped, void* x_perm, void* ws,
+                                   size_t ws_bytes, moe_stream_t stream) {
+  moe_status s = check_config(cfg);
+  if (s != MOE_OK) return s;
+  const moe_config& c = *cfg;
+  if (!tok16(c, x) || !tok4(c, topk_idx) || !need4(offsets) || !opt4(kept_counts) ||
+      !tok4(c, slot_row) || !tok4(c, row_token) || !opt4(dropped) || !tok16(c, x_perm))
+    return MOE_ERR_INVALID_ARGUMENT;
+  const Layout L = make_layout(c);
+  if (!ws || !al16(ws) || ws_bytes < L.stage_end) return MOE_ERR_WORKSPACE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int* flags = at<int>(ws, L.flags);
+  MOE_CUDA(cudaMemsetAsync(flags, 0, sizeof(int), st));
+  if (c.T == 0) {
+    if ((s = zero_async(offsets, sizeof(int32_t) * (c.E + 1), st)) != MOE_OK) return s;
+    if ((s = zero_async(kept_counts, sizeof(int32_t) * c.E, st)) != MOE_OK) return s;
+    return zero_async(dropped, sizeof(int32_t), st);
+  }
+  int32_t* hist = at<int32_t>(ws, L.hist);
+  int32_t* chunk_base = at<int32_t>(ws, L.chunk_base);
+  MOE_CUDA(launch_dispatch_hist(topk_idx, c.T, c.E, c.k, hist, flags, st));
+  MOE_CUDA(launch_route_finalize(hist, nullptr, static_cast<int>(L.nchunks), c.E, c.T,
+                                 capacity_of(c), nullptr, nullptr, chunk_base, kept_counts, offsets,
+                                 dropped, st));
+  MOE_CUDA(launch_dispatch_place(c.dtype, topk_idx, c.T, c.E, c.k, capacity_of(c), chunk_base,
+                                 offsets, slot_row, row_token, x, x_perm, c.d, flags, st));
+  return MOE_OK;
+}
+
+MOE_EXPORT moe_status moe_expert_ffn(const moe_config* cfg, const void* x_perm,
+                                     const int32_t* offsets, const void* w1, const void* b1,
+                                     const void* w2, const void* b2, void* h_buf, void* y_perm,
+                                     void* ws, size_t ws_bytes, moe_stream_t stream) {
+  moe_status s = check_config(cfg);
+  if (s != MOE_OK) return s;
+  const moe_config& c = *cfg;
+  if (!tok16(c, x_perm) || !need4(offsets) || !need16(w1) || !opt16(b1) || !need16(w2) ||
+      !opt16(b2) || !tok16(c, h_buf) || !tok16(c, y_perm))
+    return MOE_ERR_INVALID_ARGUMENT;
+  const Layout L = make_layout(c);
+  if (!ws || !al16(ws) || ws_bytes < L.stage_end) return MOE_ERR_WORKSPACE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int* flags = at<int>(ws, L.flags);
+  MOE_CUDA(cudaMemsetAsync(flags, 0, sizeof(int), st));
+  if (c.T == 0) return MOE_OK;
+  const int sms = sm_count();
+  if (sms <= 0) return MOE_ERR_CUDA;
+  return run_expert_ffn(c, x_perm, offsets, w1, b1, w2, b2, h_buf, y_perm, flags, sms, st);
+}
+
+MOE_EXPORT moe_status moe_combine(const moe_config* cfg, const void* y_perm,
+                                  const int32_t* slot_row, const float* topk_w, void* y, void* ws,
+                                  size_t ws_bytes, moe_stream_t stream) {
+  moe_status s = check_config(cfg);
+  if (s != MOE_OK) return s;
+  const moe_config& c = *cfg;
+  if (!tok16(c, y_perm) || !tok4(c, slot_row) || !tok4(c, topk_w) || !tok16(c, y))
+    return MOE_ERR_INVALID_ARGUMENT;
+  const Layout L = make_layout(c);
+  if (!ws || !al16(ws) || ws_bytes < L.stage_end) return MOE_ERR_WORKSPACE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int* flags = at<int>(ws, L.flags);
+  MOE_CUDA(cudaMemsetAsync(flags, 0, sizeof(int), st));
+  if (c.T == 0) return MOE_OK;
+  MOE_CUDA(launch_combine(c.dtype, y_perm, slot_row, topk_w, c.T, c.d, c.k, y, flags, st));
+  return MOE_OK;
+}
+
+MOE_EXPORT moe_status moe_forward(const moe_config* cfg, const moe_forward_args* a, void* ws,
+                                  size_t ws_bytes, moe_stream_t stream) {
+  moe_status s = check_config(cfg);
+  if (s != MOE_OK) return s;
+  if (!a) return MOE_ERR_INVALID_ARGUMENT;
+  const moe_config& c = *cfg;
+  if (!tok16(c, a->x) || !need16(a->w_gate) || !opt4(a->logit_bias) || !need16(a->w1) ||
+      !opt16(a->b1) || !need16(a->w2) || !opt16(a->b2) || !tok16(c, a->y) || !opt16(a->logits) ||
+      !opt4(a->topk_idx) || !opt4(a->topk_w) || !opt4(a->counts) || !opt4(a->aux_loss) ||
+      !opt4(a->offsets) || !opt4(a->kept_counts) || !opt4(a->slot_row) || !opt4(a->row_token) ||
+      !opt4(a->dropped))
+    return MOE_ERR_INVALID_ARGUMENT;
+  const Layout L = make_layout(c);
+  if (!ws || !al16(ws) || ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int* flags = at<int>(ws, L.flags);
+  MOE_CUDA(cudaMemsetAsync(flags, 0, sizeof(int), st));
+  float* logits = a->logits ? a->logits : at<float>(ws, L.logits);
+  int32_t* idx = a->topk_idx ? a->topk_idx : at<int32_t>(ws, L.idx);
+  float* w = a->topk_w ? a->topk_w : at<float>(ws, L.w);
+  int32_t* counts = a->counts ? a->counts : at<int32_t>(ws, L.counts);
+  float* aux = a->aux_loss ? a->aux_loss : at<float>(ws, L.aux);
+  int32_t* offsets = a->offsets ? a->offsets : at<int32_t>(ws, L.offsets);
+  int32_t* kept = a->kept_counts ? a->kept_counts : at<int32_t>(ws, L.kept);
+  int32_t* slot_row = a->slot_row ? a->slot_row : at<int32_t>(ws, L.slot_row);
+  int32_t* row_token = a->row_token ? a->row_token : at<int32_t>(ws, L.row_token);
+  int32_t* dropped = a->dropped ? a->dropped : at<int32_t>(ws, L.dropped);
+  if (c.T == 0) {
+    if ((s = zero_async(counts, sizeof(int32_t) * c.E, st)) != MOE_OK) return s;
+    if ((s = zero_async(aux, sizeof(float), st)) != MOE_OK) return s;
+    if ((s = zero_async(offsets, sizeof(int32_t) * (c.E + 1), st)) != MOE_OK) return s;
+    if ((s = zero_async(kept, sizeof(int32_t) * c.E, st)) != MOE_OK) return s;
+    return zero_async(dropped, sizeof(int32_t), st);
+  }
+  const int sms = sm_count();
+  if (sms <= 0) return MOE_ERR_CUDA;
+  int32_t* hist = at<int32_t>(ws, L.hist);
+  int32_t* chunk_base = at<int32_t>(ws, L.chunk_base);
+  float* psum = at<float>(ws, L.psum);
+  void* x_perm = at<void>(ws, L.x_perm);
+  void* h_buf = at<void>(ws, L.h_buf);
+  void* y_perm = at<void>(ws, L.y_perm);
+  const int64_t C = capacity_of(c);
+
+  if ((s = run_router_logits(c, a->x, a->w_gate, a->logit_bias, logits, flags, sms, st)) != MOE_OK)
+    return s;
+  MOE_CUDA(launch_route_topk(logits, c.T, c.E, c.k, c.gate, idx, w, hist, psum, flags, st));
+  MOE_CUDA(launch_route_finalize(hist, psum, static_cast<int>(L.nchunks), c.E, c.T, C, counts, aux,
+                                 chunk_base, kept, offsets, dropped, st));
+  MOE_CUDA(launch_dispatch_place(c.dtype, idx, c.T, c.E, c.k, C, chunk_base, offsets, slot_row,
+                                 row_token, a->x, x_perm, c.d, flags, st));
+  if ((s = run_expert_ffn(c, x_perm, offsets, a->w1, a->b1, a->w2, a->b2, h_buf, y_perm, flags,
+                          sms, st)) != MOE_OK)
+    return s;
+  MOE_CUDA(launch_combine(c.dtype, y_perm, slot_row, w, c.T, c.d, c.k, a->y, flags, st));
+  return MOE_OK;
+}
+
+MOE_EXPORT moe_status moe_device_error(const void* ws, moe_stream_t stream, int32_t* flags) {
+  if (!ws) return MOE_ERR_WORKSPACE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  if (cudaMemcpyAsync(&v, ws, sizeof(v), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (flags) *flags = v;
+  return v ? MOE_ERR_DEVICE : MOE_OK;
+}

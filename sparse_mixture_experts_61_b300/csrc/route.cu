@@ -1,0 +1,237 @@
+// Router stages after the logits contraction:
+//   R2  softmax over the experts, top-k selection on the logits (value desc,
+//       lower expert index on equality) and the gate weights of the kept experts,
+//   R3  per-chunk expert histogram and per-chunk softmax column sums,
+//   R4  balance loss E * sum_e f_e P_e, and (shared with dispatch) D1: capacity,
+//       kept counts, exclusive-scan offsets and the per-chunk position bases.
+// Formulas: gating formula G(x)=softmax(TopK(x.W_g)) and TopKRouter.forward /
+// load_balancing_loss of "MoE mixture-of-experts routing mechanism: principles
+// and sparse activation"; capacity from its "Expert Choice routing and
+// capacity-factor tuning" section.
+//
+// Every reduction has a fixed order (butterfly shuffles, per-warp partials summed
+// in warp order, per-chunk partials summed in chunk order), so repeated runs give
+// bitwise-identical results.  Integer histograms use shared-memory atomics, whose
+// result does not depend on order.
+
+#include <math.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+namespace {
+
+constexpr int kRouteWarps = 8;
+constexpr int kTokensPerWarp = kChunk / kRouteWarps;
+
+// One CTA per chunk of kChunk tokens, one warp per token at a time.  Lane l holds
+// experts l, l+32, ... (EPL of them).
+template <int EPL>
+__global__ void __launch_bounds__(kRouteWarps * 32)
+    route_topk_kernel(const float* __restrict__ logits, int64_t T, int E, int k, int gate,
+                      int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
+                      int32_t* __restrict__ hist, float* __restrict__ psum, int* flags) {
+  __shared__ int s_hist[kMaxExperts];
+  __shared__ float s_ps[kRouteWarps][kMaxExperts];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) s_hist[e] = 0;
+  __syncthreads();
+
+  float ps[EPL];
+#pragma unroll
+  for (int q = 0; q < EPL; ++q) ps[q] = 0.f;
+
+  const int64_t t_first = static_cast<int64_t>(blockIdx.x) * kChunk + warp * kTokensPerWarp;
+  for (int i = 0; i < kTokensPerWarp; ++i) {
+    const int64_t t = t_first + i;
+    if (t >= T) break;  // warp-uniform
+    const float* lrow = logits + t * E;
+    float v[EPL];
+    bool bad = false;
+#pragma unroll
+    for (int q = 0; q < EPL; ++q) {
+      const int e = lane + 32 * q;
+      v[q] = e < E ? lrow[e] : -INFINITY;
+      if (e < E && !isfinite(v[q])) bad = true;
+    }
+    if (__any_sync(0xffffffffu, bad) && lane == 0) raise_flag(flags, MOE_DEVERR_NONFINITE);
+
+    // softmax: m = max, s = sum exp(l - m)
+    float m = -INFINITY;
+#pragma unroll
+    for (int q = 0; q < EPL; ++q)
+      if (lane + 32 * q < E) m = fmaxf(m, v[q]);
+    m = warp_max(m);
+    float ex[EPL];
+    float s = 0.f;
+#pragma unroll
+    for (int q = 0; q < EPL; ++q) {
+      ex[q] = (lane + 32 * q < E) ? expf(v[q] - m) : 0.f;
+      s += ex[q];
+    }
+    s = warp_sum(s);
+#pragma unroll
+    for (int q = 0; q < EPL; ++q) ps[q] += ex[q] / s;
+
+    // top-k: k rounds of a warp arg-max under (value desc, index asc).
+    uint32_t taken = 0;
+    int sel_e[kMaxK];
+    float sel_v[kMaxK];
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j) {
+      sel_e[j] = 0;
+      sel_v[j] = 0.f;
+      if (j < k) {
+        float bv = -INFINITY;
+        int be = E;  // sentinel: larger than any valid index
+#pragma unroll
+        for (int q = 0; q < EPL; ++q) {
+          const int e = lane + 32 * q;
+          if (e < E && !((taken >> q) & 1u) && (v[q] > bv || (v[q] == bv && e < be))) {
+            bv = v[q];
+            be = e;
+          }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+          const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+          if (ov > bv || (ov == bv && oe < be)) {
+            bv = ov;
+            be = oe;
+          }
+        }
+        if (be >= E) be = 0;  // only reachable with NaN logits, already flagged
+        if ((be & 31) == lane) taken |= 1u << (be >> 5);
+        sel_e[j] = be;
+        sel_v[j] = bv;
+      }
+    }
+
+    // gate weights of the kept experts
+    float w[kMaxK];
+    float den = 0.f;
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j) {
+      w[j] = 0.f;
+      if (j < k) {
+        // mode 0: softmax over the kept logits, shifted by the largest (slot 0);
+        // mode 1: the full-softmax probability p_j = exp(l_j - m) / s.
+        w[j] = (gate == 0) ? expf(sel_v[j] - sel_v[0]) : expf(sel_v[j] - m) / s;
+        den += w[j];
+      }
+    }
+    int my_e = 0;
+    float my_w = 0.f;
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j)
+      if (j == lane) {
+        my_e = sel_e[j];
+        my_w = w[j] / den;
+      }
+    if (lane < k) {
+      topk_idx[t * k + lane] = my_e;
+      topk_w[t * k + lane] = my_w;
+      atomicAdd(&s_hist[my_e], 1);
+    }
+  }
+
+#pragma unroll
+  for (int q = 0; q < EPL; ++q)
+    if (lane + 32 * q < E) s_ps[warp][lane + 32 * q] = ps[q];
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    float acc = 0.f;
+#pragma unroll
+    for (int w = 0; w < kRouteWarps; ++w) acc += s_ps[w][e];
+    psum[static_cast<int64_t>(blockIdx.x) * E + e] = acc;
+    hist[static_cast<int64_t>(blockIdx.x) * E + e] = s_hist[e];
+  }
+}
+
+// Single CTA of 256 threads; thread e owns expert e.
+__global__ void __launch_bounds__(kMaxExperts)
+    route_finalize_kernel(const int32_t* __restrict__ hist, const float* __restrict__ psum,
+                          int nchunks, int E, int64_t T, int64_t C, int32_t* counts, float* aux,
+                          int32_t* chunk_base, int32_t* kept, int32_t* offsets,
+                          int32_t* dropped) {
+  __shared__ double s_red[kMaxExperts];
+  __shared__ int s_scan[kMaxExperts];
+  __shared__ int s_drop;
+  const int e = threadIdx.x;
+  if (e == 0) s_drop = 0;
+  int cnt = 0;
+  double ps = 0.0;
+  if (e < E) {
+    for (int c = 0; c < nchunks; ++c) {
+      if (chunk_base) chunk_base[static_cast<int64_t>(c) * E + e] = cnt;
+      cnt += hist[static_cast<int64_t>(c) * E + e];
+      if (psum) ps += static_cast<double>(psum[static_cast<int64_t>(c) * E + e]);
+    }
+    if (counts) counts[e] = cnt;
+  }
+  // balance loss: E * sum_e (psum_e / T) * (count_e / T), fixed-order tree sum
+  s_red[e] = (e < E && T > 0) ? (ps / static_cast<double>(T)) *
+                                    (static_cast<double>(cnt) / static_cast<double>(T))
+                              : 0.0;
+  __syncthreads();
+  for (int o = kMaxExperts / 2; o > 0; o >>= 1) {
+    if (e < o) s_red[e] += s_red[e + o];
+    __syncthreads();
+  }
+  if (e == 0 && psum && aux) aux[0] = static_cast<float>(static_cast<double>(E) * s_red[0]);
+
+  // capacity, kept counts and the exclusive scan of the offsets
+  int kp = 0;
+  if (e < E) kp = (C < 0 || cnt < C) ? cnt : static_cast<int>(C);
+  if (kept && e < E) kept[e] = kp;
+  if (e < E && cnt > kp) atomicAdd(&s_drop, cnt - kp);
+  s_scan[e] = kp;
+  __syncthreads();
+  for (int o = 1; o < kMaxExperts; o <<= 1) {
+    const int add = (e >= o) ? s_scan[e - o] : 0;
+    __syncthreads();
+    s_scan[e] += add;
+    __syncthreads();
+  }
+  if (offsets) {
+    if (e < E) offsets[e] = s_scan[e] - kp;
+    if (e == E - 1) offsets[E] = s_scan[e];
+  }
+  if (e == 0 && dropped) dropped[0] = s_drop;
+}
+
+}  // namespace
+
+cudaError_t launch_route_topk(const float* logits, int64_t T, int E, int k, int gate,
+                              int32_t* topk_idx, float* topk_w, int32_t* hist, float* psum,
+                              int* flags, cudaStream_t stream) {
+  const int64_t nchunks = (T + kChunk - 1) / kChunk;
+  if (nchunks == 0) return cudaSuccess;
+  const dim3 grid(static_cast<unsigned>(nchunks)), block(kRouteWarps * 32);
+  if (E <= 32)
+    route_topk_kernel<1><<<grid, block, 0, stream>>>(logits, T, E, k, gate, topk_idx, topk_w, hist,
+                                                     psum, flags);
+  else if (E <= 64)
+    route_topk_kernel<2><<<grid, block, 0, stream>>>(logits, T, E, k, gate, topk_idx, topk_w, hist,
+                                                     psum, flags);
+  else if (E <= 128)
+    route_topk_kernel<4><<<grid, block, 0, stream>>>(logits, T, E, k, gate, topk_idx, topk_w, hist,
+                                                     psum, flags);
+  else
+    route_topk_kernel<8><<<grid, block, 0, stream>>>(logits, T, E, k, gate, topk_idx, topk_w, hist,
+                                                     psum, flags);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_route_finalize(const int32_t* hist, const float* psum, int nchunks, int E,
+                                  int64_t T, int64_t C, int32_t* counts, float* aux,
+                                  int32_t* chunk_base, int32_t* kept, int32_t* offsets,
+                                  int32_t* dropped, cudaStream_t stream) {
+  route_finalize_kernel<<<1, kMaxExperts, 0, stream>>>(hist, psum, nchunks, E, T, C, counts, aux,
+                                                       chunk_base, kept, offsets, dropped);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

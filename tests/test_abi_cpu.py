@@ -1,0 +1,149 @@
+"""Host-side checks of the C ABI (no GPU needed, no kernel launched).
+
+The library is built for sm_103a and loaded; every function include/moe.h declares
+must be exported; struct layouts must match the header; and every host-side
+validation path must return its documented status before touching the GPU (all
+pointers below are fake, 16-byte-aligned integers that are never dereferenced).
+"""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import oracle
+import sparse_mixture_experts_61_b300 as moe
+from sparse_mixture_experts_61_b300 import build as moe_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe.h")
+
+FAKE = 0x10000          # aligned fake device address, never dereferenced
+FAKE_ODD = 0x10004      # 4-byte aligned but not 16-byte aligned
+
+
+@pytest.fixture(scope="module")
+def L():
+    moe_build.build()
+    return moe.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:moe_status|const char\*)\s+(moe_\w+)\s*\(", text, re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("moe_route", "moe_dispatch", "moe_expert_ffn", "moe_combine", "moe_forward",
+              "moe_workspace_size", "moe_device_error", "moe_status_str"):
+        assert n in names
+    assert sorted(moe.EXPORTED) == names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for n in declared_functions():
+        assert hasattr(L, n), f"{n} not exported"
+    # only the C API is visible
+    out = os.popen(f"nm -D --defined-only {moe.LIB_PATH}").read()
+    exported = sorted(set(re.findall(r" T (moe_\w+)", out)))
+    assert exported == declared_functions()
+
+
+def test_struct_layouts_match_header():
+    assert ctypes.sizeof(moe.MoeConfig) == 40
+    assert moe.MoeConfig.capacity_factor.offset == 32
+    assert ctypes.sizeof(moe.MoeForwardArgs) == 18 * 8
+
+
+def test_status_strings(L):
+    for s, name in [(0, "MOE_OK"), (1, "MOE_ERR_INVALID_ARGUMENT"), (2, "MOE_ERR_UNSUPPORTED"),
+                    (3, "MOE_ERR_WORKSPACE"), (4, "MOE_ERR_CUDA"), (5, "MOE_ERR_DEVICE")]:
+        assert moe.status_str(s) == name
+    assert moe.status_str(99) == "MOE_ERR_UNKNOWN"
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(k=0), moe.MOE_ERR_UNSUPPORTED),
+    (dict(k=9, E=16), moe.MOE_ERR_UNSUPPORTED),
+    (dict(k=4, E=3), moe.MOE_ERR_UNSUPPORTED),
+    (dict(E=257), moe.MOE_ERR_UNSUPPORTED),
+    (dict(d=12), moe.MOE_ERR_UNSUPPORTED),
+    (dict(h=0), moe.MOE_ERR_UNSUPPORTED),
+    (dict(T=-1), moe.MOE_ERR_UNSUPPORTED),
+    (dict(T=2**30, k=2), moe.MOE_ERR_UNSUPPORTED),
+    (dict(dtype=7), moe.MOE_ERR_INVALID_ARGUMENT),
+    (dict(gate=2), moe.MOE_ERR_INVALID_ARGUMENT),
+    (dict(capacity_factor=float("nan")), moe.MOE_ERR_INVALID_ARGUMENT),
+])
+def test_config_validation(L, kw, status):
+    base = dict(T=64, d=64, h=128, E=8, k=2, dtype=1, gate=0, capacity_factor=0.0)
+    base.update(kw)
+    cfg = moe.MoeConfig(base["T"], base["d"], base["h"], base["E"], base["k"], base["dtype"],
+                        base["gate"], base["capacity_factor"])
+    n = ctypes.c_size_t()
+    assert L.moe_workspace_size(ctypes.byref(cfg), ctypes.byref(n)) == status
+    assert L.moe_route(ctypes.byref(cfg), FAKE, FAKE, None, None, FAKE, FAKE, None, None, FAKE,
+                       1 << 40, None) == status
+
+
+def test_null_config_and_outputs(L):
+    n = ctypes.c_size_t()
+    assert L.moe_workspace_size(None, ctypes.byref(n)) == moe.MOE_ERR_INVALID_ARGUMENT
+    cfg = moe.config(64, 64, 128, 8, 2)
+    assert L.moe_workspace_size(ctypes.byref(cfg), None) == moe.MOE_ERR_INVALID_ARGUMENT
+    assert L.moe_forward(ctypes.byref(cfg), None, FAKE, 1 << 40, None) == moe.MOE_ERR_INVALID_ARGUMENT
+
+
+def _ws(cfg):
+    return moe.moe_stage_workspace_size(cfg), moe.moe_workspace_size(cfg)
+
+
+def test_workspace_sizes_cover_buffers(L):
+    cfg = moe.config(4096, 4096, 14336, 8, 2, "bf16")
+    stage, full = _ws(cfg)
+    rows = 4096 * 2
+    assert full >= stage + rows * (4096 + 14336 + 4096) * 2
+    assert stage >= 4096 * 8 * 4       # logits
+    assert full % 256 == 0 and stage % 256 == 0
+    c32 = moe.config(4096, 4096, 14336, 8, 2, "f32")
+    assert moe.moe_workspace_size(c32) > full
+
+
+def test_required_pointers_and_alignment(L):
+    cfg = moe.config(64, 64, 128, 8, 2)
+    big = 1 << 40
+    INV = moe.MOE_ERR_INVALID_ARGUMENT
+    # moe_route: x, w_gate, topk_idx, topk_w required; x 16-byte aligned
+    assert L.moe_route(ctypes.byref(cfg), None, FAKE, None, None, FAKE, FAKE, None, None, FAKE, big, None) == INV
+    assert L.moe_route(ctypes.byref(cfg), FAKE_ODD, FAKE, None, None, FAKE, FAKE, None, None, FAKE, big, None) == INV
+    assert L.moe_route(ctypes.byref(cfg), FAKE, FAKE, None, None, None, FAKE, None, None, FAKE, big, None) == INV
+    # moe_dispatch: x_perm required
+    assert L.moe_dispatch(ctypes.byref(cfg), FAKE, FAKE, FAKE, None, FAKE, FAKE, None, None, FAKE, big, None) == INV
+    # moe_expert_ffn: w1 required, b1 optional but aligned
+    assert L.moe_expert_ffn(ctypes.byref(cfg), FAKE, FAKE, None, None, FAKE, None, FAKE, FAKE, FAKE, big, None) == INV
+    assert L.moe_expert_ffn(ctypes.byref(cfg), FAKE, FAKE, FAKE, FAKE_ODD, FAKE, None, FAKE, FAKE, FAKE, big, None) == INV
+    # moe_combine: y required
+    assert L.moe_combine(ctypes.byref(cfg), FAKE, FAKE, FAKE, None, FAKE, big, None) == INV
+
+
+def test_workspace_too_small_is_rejected_before_launch(L):
+    cfg = moe.config(64, 64, 128, 8, 2)
+    stage, full = _ws(cfg)
+    WS = moe.MOE_ERR_WORKSPACE
+    assert L.moe_route(ctypes.byref(cfg), FAKE, FAKE, None, None, FAKE, FAKE, None, None, FAKE, stage - 1, None) == WS
+    assert L.moe_route(ctypes.byref(cfg), FAKE, FAKE, None, None, FAKE, FAKE, None, None, None, stage, None) == WS
+    assert L.moe_dispatch(ctypes.byref(cfg), FAKE, FAKE, FAKE, None, FAKE, FAKE, None, FAKE, FAKE, stage - 1, None) == WS
+    assert L.moe_expert_ffn(ctypes.byref(cfg), FAKE, FAKE, FAKE, None, FAKE, None, FAKE, FAKE, FAKE, 16, None) == WS
+    assert L.moe_combine(ctypes.byref(cfg), FAKE, FAKE, FAKE, FAKE, FAKE, 0, None) == WS
+    args = moe.MoeForwardArgs(x=FAKE, w_gate=FAKE, w1=FAKE, w2=FAKE, y=FAKE)
+    assert L.moe_forward(ctypes.byref(cfg), ctypes.byref(args), FAKE, full - 1, None) == WS
+    assert L.moe_device_error(None, None, None) == WS
+
+
+@pytest.mark.parametrize("T,E,cf", [(8192, 128, 1.25), (1000, 16, 1.25), (3, 4, 1.0), (10, 3, 0.7),
+                                    (64, 64, 0.0), (5, 8, -1.0)])
+def test_capacity_matches_oracle(L, T, E, cf):
+    cfg = moe.config(T, 64, 64, E, 1, "bf16", 1, cf)
+    assert moe.moe_capacity(cfg) == oracle.capacity(T, E, cf if cf > 0 else None)
