@@ -1,0 +1,458 @@
+#!/usr/bin/env python3
+"""Benchmark of the top-k MoE FFN forward (moe_forward through the C ABI) on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step = one moe_forward (router, softmax/top-k, balance loss, dispatch, grouped
+expert GEMMs, combine) over one batch of seeded synthetic tokens already resident in
+HBM.  Default workload: the 8-expert top-2 prefill layer (T=4096, d=4096, h=14336,
+bf16).  L2 is flushed (a 256 MB write) before every timed step, outside the step's
+CUDA-event pair.  Under torchrun each rank runs an independent replica on its own
+batch (token-parallel, no data-path collective): value = tokens of all ranks / the
+slowest rank's time.  Rank 0 prints one JSON line.
+
+The line carries: the device-timed tokens/s (`value`), the end-to-end tokens/s with
+host-resident x and y copied in and out inside the timed region (`e2e`), the grouped
+expert GEMM pair timed alone against the measured roofline (`roofline`), the CPU
+oracle timed on a bounded sample of the same workload (`cpu_baseline`), SM clocks
+sampled during the timed region (`clocks`) and the number of our kernel launches in
+the timed region (`gpu_launches`).
+
+--impl reference times the CPU oracle itself (the plain fp64 implementation the
+parity tests use) on the host cores, each step a bounded sample of the workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from moe_workloads import WORKLOADS, capacity_factor_or_none, input_recipe, make_inputs  # noqa: E402
+
+METRIC = "MoE-layer fwd tokens/s at 1 B300; grouped-GEMM % BF16 peak; decode % HBM BW"
+UNIT = "tokens/s"
+DEFAULT_WORKLOAD = "mixtral_prefill"
+L2_FLUSH_BYTES = 256 << 20
+KERNELS_PER_FORWARD = 7   # router GEMM, softmax/top-k, finalize/scan, place/gather, GEMM1, GEMM2, combine
+
+# dram__bytes_read.sum + dram__bytes_write.sum per launch of the grouped GEMM pair, from
+# the ncu capture summarised in profiles/ (None until a capture of the current kernel).
+NCU_TRAFFIC_BYTES = {}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        p = json.load(open(path))
+        return dict(hbm_gbs=p["hbm_gbs"], bf16_tflops=p["bf16_tflops"],
+                    bf16_tflops_sustained=p.get("bf16_tflops_sustained"), source="measured")
+    return dict(hbm_gbs=6400.0, bf16_tflops=1800.0, bf16_tflops_sustained=1400.0, source="fallback")
+
+
+# ------------------------------------------------------------------ distributed
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def dist_init(world, local):
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def allreduce_max(v: float, world: int) -> float:
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi sampler of SM clocks and throttle reasons; keeps timestamped rows."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        rows = []
+        if self.path and os.path.exists(self.path):
+            for line in open(self.path):
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                    ts += float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                    rows.append((ts, float(parts[1]), float(parts[2]), parts[4:]))
+                except (ValueError, IndexError):
+                    continue
+            os.unlink(self.path)
+        if not rows:
+            return dict(sm_mhz=None, sm_max_mhz=None, reasons=[], samples=0)
+        inside = [r for r in rows if t0 - 0.05 <= r[0] <= t1 + 0.05] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in inside for i, v in enumerate(r[3][1:5])
+                          if v.strip().lower() == "active"})
+        return dict(sm_mhz=statistics.median(r[1] for r in inside),
+                    sm_max_mhz=max(r[2] for r in inside), reasons=reasons, samples=len(inside))
+
+
+# ------------------------------------------------------------------ oracle (CPU) timing
+def oracle_tokens_step(w, host, fetch, tokens):
+    """Runs the oracle's whole layer on the given tokens (a batch of its own).  Returns
+    the seconds spent inside oracle calls (host copies of weights are not timed)."""
+    import oracle
+
+    cf = capacity_factor_or_none(w)
+    xs = host["x"][torch.as_tensor(tokens)]
+    spent = 0.0
+    t = time.perf_counter()
+    lg = oracle.logits(xs, host["w_gate"], host["logit_bias"])
+    p = oracle.softmax(lg)
+    idx = oracle.topk(lg, w.k)
+    wts = oracle.gate_weights(lg, idx, w.gate)
+    oracle.aux_loss(p, idx)
+    disp = oracle.dispatch(idx, w.E, oracle.capacity(len(tokens), w.E, cf))
+    spent += time.perf_counter() - t
+    z = np.zeros((len(tokens), w.k, w.d))
+    by_e = {}
+    for a in range(len(tokens)):
+        for j in range(w.k):
+            if disp["slot_row"][a, j] >= 0:
+                by_e.setdefault(int(idx[a, j]), []).append((a, j))
+    for e, items in sorted(by_e.items()):
+        w1, b1, w2, b2 = fetch(e)
+        rows = xs[[a for a, _ in items]]
+        t = time.perf_counter()
+        ze = oracle.expert_rows(rows, w1, b1, w2, b2)
+        spent += time.perf_counter() - t
+        for q, (a, j) in enumerate(items):
+            z[a, j] = ze[q]
+    t = time.perf_counter()
+    oracle.combine(disp["slot_row"], wts, z)
+    spent += time.perf_counter() - t
+    return spent
+
+
+def host_view(inp):
+    host = {"x": inp["x"].cpu(), "w_gate": inp["w_gate"].cpu(),
+            "logit_bias": inp["logit_bias"].cpu() if inp["logit_bias"] is not None else None}
+    cache = {}
+
+    def fetch(e):
+        if e not in cache:
+            if len(cache) >= 16:
+                cache.pop(next(iter(cache)))
+            cache[e] = tuple(inp[n][e].cpu() for n in ("w1", "b1", "w2", "b2"))
+        return cache[e]
+
+    return host, fetch
+
+
+def cpu_baseline(w, inp, budget_s=12.0):
+    """Oracle throughput on a bounded sample: consecutive tokens from token 0, in growing
+    batches, until about budget_s seconds of oracle work."""
+    import oracle
+
+    host, fetch = host_view(inp)
+    done, spent, batch = 0, 0.0, 1
+    while spent < budget_s and done < w.T:
+        toks = list(range(done, min(w.T, done + batch)))
+        spent += oracle_tokens_step(w, host, fetch, toks)
+        done += len(toks)
+        batch = min(batch * 2, 256)
+    return dict(value=done / spent, unit=UNIT, cores=oracle.num_threads(), kind="oracle",
+                sample=f"first {done} of {w.T} tokens of the workload, whole layer in fp64 "
+                       f"({spent:.1f} s of oracle time)")
+
+
+# ------------------------------------------------------------------ roofline
+def ffn_algorithmic(w, M, nonempty):
+    s = 2 if w.dtype == "bf16" else 4
+    flops = 4.0 * M * w.d * w.h
+    byts = s * (2.0 * M * w.d + 2.0 * M * w.h + nonempty * (2.0 * w.d * w.h + w.h + w.d))
+    return flops, byts
+
+
+def roofline(w, M, nonempty, t_ffn_s, peaks):
+    flops, byts = ffn_algorithmic(w, M, nonempty)
+    t_tensor = flops / (peaks["bf16_tflops"] * 1e12)
+    t_hbm = byts / (peaks["hbm_gbs"] * 1e9)
+    traffic = NCU_TRAFFIC_BYTES.get(w.name)
+    if t_tensor >= t_hbm:
+        achieved = flops / t_ffn_s / 1e12
+        r = dict(bound="tensor", achieved=round(achieved, 1), peak=peaks["bf16_tflops"],
+                 unit="TFLOP/s", frac=round(achieved / peaks["bf16_tflops"], 4))
+        if peaks.get("bf16_tflops_sustained"):
+            r["frac_of_sustained"] = round(achieved / peaks["bf16_tflops_sustained"], 4)
+    else:
+        achieved = byts / t_ffn_s / 1e9
+        r = dict(bound="hbm", achieved=round(achieved, 1), peak=peaks["hbm_gbs"], unit="GB/s",
+                 frac=round(achieved / peaks["hbm_gbs"], 4))
+    r.update(traffic=traffic, kernel="grouped expert GEMM pair G1+G2 (moe_expert_ffn)",
+             algorithmic_flops=flops, algorithmic_bytes=byts, peak_source=peaks["source"],
+             ms=round(t_ffn_s * 1e3, 4))
+    return r
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args, world, rank, local):
+    import sparse_mixture_experts_61_b300 as moe
+
+    moe.lib()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = WORKLOADS[args.workload]
+    inp = make_inputs(w, seed=rank, device=str(dev))
+    cfg = moe.config_from_workload(w)
+    i32 = dict(dtype=torch.int32, device=dev)
+    outs = dict(y=torch.empty((w.T, w.d), dtype=w.torch_dtype, device=dev),
+                offsets=torch.empty((w.E + 1,), **i32), kept_counts=torch.empty((w.E,), **i32))
+    ws = torch.empty(moe.moe_workspace_size(cfg), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    fwd_args = moe.forward_args(inp, outs)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        moe.moe_forward(cfg, inp, outs, ws, stream, args=fwd_args)
+
+    for _ in range(args.warmup):
+        step()
+    assert moe.moe_device_error(ws) == 0
+    M = int(outs["offsets"][-1])
+    nonempty = int((outs["kept_counts"] > 0).sum())
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    clocks = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    if clocks:
+        clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    for i in range(args.steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    t1 = time.time()
+    if clocks:
+        clocks.stop()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    mean_ms = allreduce_max(statistics.fmean(step_ms), world)
+    assert moe.moe_device_error(ws) == 0
+
+    # The grouped expert GEMM pair alone (same rows, same stream), for the roofline.
+    sws = torch.empty(moe.moe_stage_workspace_size(cfg), dtype=torch.uint8, device=dev)
+    rows = w.T * w.k
+    x_perm = torch.empty((rows, w.d), dtype=w.torch_dtype, device=dev)
+    h_buf = torch.empty((rows, w.h), dtype=w.torch_dtype, device=dev)
+    y_perm = torch.empty((rows, w.d), dtype=w.torch_dtype, device=dev)
+    idx = torch.empty((w.T, w.k), **i32)
+    wts = torch.empty((w.T, w.k), dtype=torch.float32, device=dev)
+    slot_row = torch.empty((w.T, w.k), **i32)
+    row_token = torch.empty((rows,), **i32)
+    offsets = torch.empty((w.E + 1,), **i32)
+    moe.moe_route(cfg, inp["x"], inp["w_gate"], inp["logit_bias"], None, idx, wts, None, None, sws)
+    moe.moe_dispatch(cfg, inp["x"], idx, offsets, None, slot_row, row_token, None, x_perm, sws)
+    ffn_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+    for i in range(args.steps + args.warmup):
+        flush.zero_()
+        if i >= args.warmup:
+            ffn_ev[i - args.warmup][0].record(stream)
+        moe.moe_expert_ffn(cfg, x_perm, offsets, inp["w1"], inp["b1"], inp["w2"], inp["b2"],
+                           h_buf, y_perm, sws)
+        if i >= args.warmup:
+            ffn_ev[i - args.warmup][1].record(stream)
+    torch.cuda.synchronize()
+    assert moe.moe_device_error(sws) == 0
+    t_ffn = statistics.fmean(a.elapsed_time(b) for a, b in ffn_ev) / 1e3
+    del x_perm, h_buf, y_perm
+
+    # End to end through the same C call with host-resident x and y (pinned).
+    x_host = inp["x"].cpu().pin_memory()
+    y_host = torch.empty((w.T, w.d), dtype=w.torch_dtype).pin_memory()
+    x_dev = inp["x"]
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+    for i in range(args.steps + args.warmup):
+        flush.zero_()
+        if i >= args.warmup:
+            e2e_ev[i - args.warmup][0].record(stream)
+        x_dev.copy_(x_host, non_blocking=True)
+        step()
+        y_host.copy_(outs["y"], non_blocking=True)
+        if i >= args.warmup:
+            e2e_ev[i - args.warmup][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = allreduce_max(statistics.fmean(a.elapsed_time(b) for a, b in e2e_ev), world)
+
+    if rank != 0:
+        return None
+    peaks = load_peaks()
+    line = {
+        "metric": METRIC,
+        "value": round(world * w.T / (mean_ms / 1e3), 1),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(mean_ms, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": w.dtype,
+        "data": "synthetic",
+        "config": {"workload": w.name, "T": w.T, "d": w.d, "h": w.h, "E": w.E, "k": w.k,
+                   "gate": ["topk_softmax", "softmax_topk_renorm"][w.gate],
+                   "capacity_factor": w.capacity_factor, "kept_rows": M,
+                   "nonempty_experts": nonempty, "inputs": input_recipe(w),
+                   "l2": "flushed before every timed step (256 MB write outside the event pair)",
+                   "parallelism": f"replicas x{world} (token-parallel, no collective)"},
+        "roofline": roofline(w, M, nonempty, t_ffn, peaks),
+        "e2e": {"value": round(world * w.T / (e2e_ms / 1e3), 1), "unit": UNIT,
+                "h2d_bytes_per_step": x_host.numel() * x_host.element_size(),
+                "d2h_bytes_per_step": y_host.numel() * y_host.element_size()},
+        "gpu_launches": KERNELS_PER_FORWARD * args.steps,
+        "clocks": clocks.summary(t0, t1) if clocks else None,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, inp)
+    return line
+
+
+# ------------------------------------------------------------------ reference arm
+def run_reference(args, world, rank, local):
+    if rank != 0:
+        return None
+    import oracle
+
+    w = WORKLOADS[args.workload]
+    device = "cuda" if torch.cuda.is_available() else "cpu"
+    gen_dev = device if w.d * w.h * w.E > (1 << 27) else "cpu"
+    inp = make_inputs(w, seed=0, device=gen_dev)
+    host, fetch = host_view(inp)
+    # Size one step's sample from the cost of one token so the whole run stays short.
+    probe = oracle_tokens_step(w, host, fetch, [0])
+    per_token = max(probe, 1e-4)
+    total_steps = args.steps + args.warmup
+    target = max(0.05, min(5.0, 150.0 / max(total_steps, 1)))
+    S = int(max(1, min(w.T, target / per_token)))
+    times = []
+    for i in range(total_steps):
+        start = (i * S) % w.T
+        toks = [(start + q) % w.T for q in range(S)]
+        t = oracle_tokens_step(w, host, fetch, toks)
+        if i >= args.warmup:
+            times.append(t)
+    mean_s = statistics.fmean(times) if times else probe
+    value = S / mean_s
+    sample = f"{S} consecutive tokens per step of the {w.T}-token workload, whole layer in fp64"
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 3),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(mean_s * 1e3, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": w.name, "T": w.T, "d": w.d, "h": w.h, "E": w.E, "k": w.k,
+                   "gate": ["topk_softmax", "softmax_topk_renorm"][w.gate],
+                   "capacity_factor": w.capacity_factor, "inputs": input_recipe(w)},
+        "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true",
+                    help="skip the timed CPU-oracle sample (for quick runs)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        line = run_reference(args, world, rank, local)
+    else:
+        dist_init(world, local)
+        line = run_ours(args, world, rank, local)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()
