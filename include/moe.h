@@ -192,6 +192,32 @@ moe_status moe_forward(const moe_config* cfg, const moe_forward_args* args, void
    otherwise, MOE_ERR_CUDA if the wait or the read failed. */
 moe_status moe_device_error(const void* ws, moe_stream_t stream, int32_t* flags);
 
+/* Table cells (ceil(T/64) * E) that moe_dispatch_static's library-held scratch holds:
+   2 MiB of device memory in every GPU that loads the library. */
+#define MOE_DISPATCH_STATIC_MAX_CELLS 262144
+
+/* moe_dispatch without a workspace.  The pages have no counterpart to this entry
+   point: it exists for callers that cannot allocate device memory at the call site
+   -- code running under a host framework that owns all device memory and forbids
+   allocation once it is serving, or a plugin that is handed only its inputs and
+   outputs -- and so cannot pass the workspace moe_dispatch needs.  It computes
+   exactly what moe_dispatch computes (same arguments and outputs, same kernels)
+   and calls no allocator.  Its scratch (per-chunk tables and the flag word) is one
+   array owned by the library:
+    - sizes with ceil(T/64) * E > MOE_DISPATCH_STATIC_MAX_CELLS return
+      MOE_ERR_UNSUPPORTED (T <= 65536 tokens at E = 256);
+    - every call shares the array and it keeps the last call's contents; each call
+      rewrites what it reads and clears the flag word, but calls whose GPU work
+      overlaps (other streams, other host threads) race on it: serialise them;
+    - the array's device address is looked up on the first call made with a given
+      device current; make that first call before any stream capture begins.
+   device_flags: optional [1] int32 device buffer that receives the device flag word
+   (MOE_DEVERR_BAD_INDEX); NULL keeps it inside the library's array. */
+moe_status moe_dispatch_static(const moe_config* cfg, const void* x, const int32_t* topk_idx,
+                               int32_t* offsets, int32_t* kept_counts, int32_t* slot_row,
+                               int32_t* row_token, int32_t* dropped, void* x_perm,
+                               int32_t* device_flags, moe_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

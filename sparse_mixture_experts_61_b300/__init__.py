@@ -36,7 +36,10 @@ MOE_DEVERR_TIMEOUT = 8
 # Every C symbol include/moe.h declares.
 EXPORTED = ("moe_status_str", "moe_capacity", "moe_workspace_size", "moe_stage_workspace_size",
             "moe_route", "moe_dispatch", "moe_expert_ffn", "moe_combine", "moe_forward",
-            "moe_device_error")
+            "moe_device_error", "moe_dispatch_static")
+
+# Table cells of moe_dispatch_static's library-held scratch (include/moe.h).
+MOE_DISPATCH_STATIC_MAX_CELLS = 262144
 
 
 class MoeError(RuntimeError):
@@ -81,6 +84,7 @@ def lib():
         L.moe_combine.argtypes = [cfg, P, P, P, P, P, S, P]
         L.moe_forward.argtypes = [cfg, ctypes.POINTER(MoeForwardArgs), P, S, P]
         L.moe_device_error.argtypes = [P, P, ctypes.POINTER(ctypes.c_int32)]
+        L.moe_dispatch_static.argtypes = [cfg, P, P, P, P, P, P, P, P, P, P]
         for name in EXPORTED:
             if name != "moe_status_str":
                 getattr(L, name).restype = ctypes.c_int
@@ -197,3 +201,14 @@ def moe_device_error(ws, stream=None) -> int:
     if s not in (MOE_OK, MOE_ERR_DEVICE):
         raise MoeError(s, "moe_device_error")
     return v.value
+
+
+def moe_dispatch_static(cfg, x, topk_idx, offsets, kept_counts, slot_row, row_token, dropped,
+                        x_perm, device_flags=None, stream=None):
+    """moe_dispatch for callers that cannot allocate a workspace: the library keeps the
+    scratch in its own device array (see include/moe.h for the size limit and the rule
+    that overlapping calls must be serialised)."""
+    _check(lib().moe_dispatch_static(ctypes.byref(cfg), _p(x), _p(topk_idx), _p(offsets),
+                                     _p(kept_counts), _p(slot_row), _p(row_token), _p(dropped),
+                                     _p(x_perm), _p(device_flags), _stream(stream)),
+           "moe_dispatch_static")
