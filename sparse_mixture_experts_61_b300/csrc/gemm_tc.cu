@@ -1,33 +1,39 @@
-// Ragged grouped GEMM on the 5th-generation tensor cores (tcgen05, sm_103a).
+// GEMMs on the 5th-generation tensor cores (tcgen05, sm_103a): the two expert GEMMs
+// of the expert FFN and the router contraction.
 //
-//   out[r, n] = act( sum_c A[r, c] * B[g][n][c] + bias[g][n] ),  r in group g's rows
+//   expert FFN ("MoE mixture-of-experts routing mechanism: principles and sparse
+//   activation", Expert.forward = w2(silu(w1(x))) with nn.Linear biases), run as one
+//   ragged grouped GEMM per layer -- the job "Breaking the MoE trilemma" 3.3 gives
+//   _grouped_ffn, with every expert's token group handled by one kernel launch:
+//       out[r, n] = act( sum_c X[r, c] * W[g][n][c] + bias[g][n] ),  r in group g's rows
+//   router (gating formula, x . W_g):  logits[t, e] = sum_c x[t, c] * W_g[e, c] + b[e].
 //
-// It serves the two expert GEMMs of the expert FFN (Expert.forward =
-// w2(silu(w1(x))) with nn.Linear biases, "MoE mixture-of-experts routing
-// mechanism: principles and sparse activation") -- bias + SiLU fused into the
-// first GEMM's epilogue, bias into the second's -- and, with one group and an fp32
-// epilogue, the router contraction x . W_g of the gating formula.  Its job is the
-// one "Breaking the MoE trilemma" 3.3 gives _grouped_ffn: every expert's token
-// group multiplied in one kernel, with no per-expert launch.
-//
-// Design (one CTA per SM, persistent):
-//  * 128 x BN output tiles; a tile never straddles two groups.  Group g owns
-//    ceil(rows_g / 128) row tiles.  Tiles are ordered (group, column block, row
-//    block) so CTAs running side by side share the same weight tile through L2.
-//    The tile list is derived on the device from the group offsets: the number
-//    of kept rows never goes to the host.
-//  * warp 0: TMA producer.  A tile [128 x 64] from a 2-D tensor map over the row
-//    buffer; B tile [BN x 64] from a 3-D map [G, N, K] addressed by group, so
-//    no per-group descriptors.  Rows past the buffer are zero-filled by TMA; rows
-//    past the group's end are computed and discarded by the epilogue.
-//  * warp 1: allocates TMEM and issues tcgen05.mma (M=128, N=BN, K=16) from one
-//    thread into one of two TMEM accumulators, committing each smem stage back to
-//    the producer and each finished accumulator to the epilogue.
-//  * warps 2-5: epilogue.  tcgen05.ld drains the accumulator 32 columns at a time
-//    (thread = row), adds the bias, applies the activation, rounds and stores.
-//    Two accumulators let the epilogue of one tile overlap the next main loop.
+// Both kernels share one warp-specialised pipeline (one persistent CTA per SM):
+//  * warp 0: TMA producer.  128-byte-swizzled K-major tiles, 64 bf16 deep.
+//  * warp 1: allocates TMEM (two fp32 accumulators) and issues tcgen05.mma from one
+//    thread, committing each shared-memory stage back to the producer and each
+//    finished accumulator to the epilogue.
+//  * warps 2-5: epilogue, draining TMEM with tcgen05.ld while the next tile's main
+//    loop runs in the other accumulator.
 //  * Every wait is bounded (common.cuh); on a timeout the CTA records
-//    MOE_DEVERR_TIMEOUT, drains its own TMA copies and MMAs, frees TMEM, returns.
+//    MOE_DEVERR_TIMEOUT, lets its own TMA copies and MMAs land, frees TMEM, returns.
+//
+// Expert GEMMs use the "weights as M" orientation: the MMA's M = 128 side is a block
+// of 128 weight rows (output features), which always fills the tile, and its N side
+// is a block of one expert's token rows, set per tile in the instruction descriptor.
+// An expert's n rows are cut into nt = ceil(n / TB) equal blocks of ceil(n / nt)
+// rows rounded up to 16, so a ragged group costs at most 15 padded token columns per
+// block.  CTAs work in clusters of two: both take the same token block and
+// neighbouring weight blocks; each loads its own 128 weight rows and half of the
+// token rows, multicasting them into both CTAs' shared memory, so a 64-deep k-block
+// moves 16 KB of weights + TB*64 B of tokens per CTA instead of 16 KB + TB*128 B.
+// A stage is released when both CTAs' MMAs have read it (each MMA commit arrives on
+// both CTAs' "empty" barriers).  Tiles are ordered (group, weight-block pair, token
+// block) so clusters running side by side read the same weight tiles, which come
+// from HBM once.  The tile list is derived on the device from the group offsets:
+// the kept-row count never goes to the host.
+//
+// The router keeps tokens as M (128 rows per tile) and the E experts as N.
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -41,14 +47,14 @@
 namespace moe {
 namespace {
 
-constexpr int TC_BM = 128;
 constexpr int TC_BK = 64;  // 64 bf16 = 128 bytes = one swizzle row
 constexpr int TC_THREADS = 192;
+constexpr int TILE_M = 128;
 
-template <int BN, int STAGES>
-struct TcSmem {
-  uint8_t a[STAGES][TC_BM * TC_BK * 2];
-  uint8_t b[STAGES][BN * TC_BK * 2];
+template <int A_BYTES, int B_BYTES, int STAGES>
+struct PipeSmem {
+  uint8_t a[STAGES][A_BYTES];
+  uint8_t b[STAGES][B_BYTES];
   uint64_t full[STAGES];
   uint64_t empty[STAGES];
   uint64_t tfull[2];
@@ -56,7 +62,7 @@ struct TcSmem {
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
-  int mpref[kMaxExperts + 1];
+  int pref[kMaxExperts + 1];  // per-group prefix of tile units
 };
 
 // Wait used only while unwinding: bounded by time, ignores the abort flag.
@@ -66,111 +72,19 @@ __device__ __forceinline__ void mbar_wait_unwind(uint32_t bar, uint32_t parity) 
     if (global_ns() - t0 > kWaitLimitNs) return;
 }
 
-struct TileCoord {
-  int g;
-  int64_t row0, row_end;
-  int n0;
-};
-
-__device__ __forceinline__ TileCoord decode_tile(int tile, const int* mpref, int G, int NB,
-                                                 const GemmArgs& p, int bn) {
-  int lo = 0, hi = G;
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (mpref[mid] * NB <= tile) lo = mid; else hi = mid;
-  }
-  TileCoord c;
-  c.g = lo;
-  const int mt_g = mpref[lo + 1] - mpref[lo];
-  const int local = tile - mpref[lo] * NB;
-  const int nb = local / mt_g, mt = local % mt_g;
-  const int64_t base = p.offsets ? p.offsets[lo] : 0;
-  c.row0 = base + static_cast<int64_t>(mt) * TC_BM;
-  c.row_end = p.offsets ? p.offsets[lo + 1] : p.m_rows;
-  c.n0 = nb * bn;
-  return c;
-}
-
-template <int EPI, int CH>
-__device__ __forceinline__ void epilogue_store(const GemmArgs& p, int g, int64_t row, int n_start,
-                                               const float (&v)[CH]) {
-  if constexpr (EPI == EPI_ROUTER_F32) {
-    float* out = static_cast<float*>(p.out) + row * p.N;
-    const float* bias = static_cast<const float*>(p.bias);
-#pragma unroll
-    for (int i = 0; i < CH; ++i) {
-      const int n = n_start + i;
-      if (n < p.N) out[n] = v[i] + (bias ? bias[n] : 0.f);
-    }
-  } else {
-    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + row * p.N + n_start;
-    const __nv_bfloat16* bias =
-        p.bias ? static_cast<const __nv_bfloat16*>(p.bias) + static_cast<int64_t>(g) * p.N + n_start
-               : nullptr;
-    if (n_start + CH <= p.N) {
-#pragma unroll
-      for (int q = 0; q < CH / 8; ++q) {
-        float b[8];
-        if (bias) {
-          const uint4 bv = __ldg(reinterpret_cast<const uint4*>(bias + 8 * q));
-          const __nv_bfloat162* bh = reinterpret_cast<const __nv_bfloat162*>(&bv);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float2 f = __bfloat1622float2(bh[i]);
-            b[2 * i] = f.x;
-            b[2 * i + 1] = f.y;
-          }
-        } else {
-#pragma unroll
-          for (int i = 0; i < 8; ++i) b[i] = 0.f;
-        }
-        uint4 packed;
-        __nv_bfloat162* ph = reinterpret_cast<__nv_bfloat162*>(&packed);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          float x0 = v[8 * q + 2 * i] + b[2 * i];
-          float x1 = v[8 * q + 2 * i + 1] + b[2 * i + 1];
-          if (EPI == EPI_BIAS_SILU) {
-            x0 = x0 / (1.f + __expf(-x0));
-            x1 = x1 / (1.f + __expf(-x1));
-          }
-          ph[i] = __floats2bfloat162_rn(x0, x1);
-        }
-        *reinterpret_cast<uint4*>(out + 8 * q) = packed;
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < CH; ++i) {
-        if (n_start + i >= p.N) break;
-        float x = v[i] + (bias ? __bfloat162float(bias[i]) : 0.f);
-        if (EPI == EPI_BIAS_SILU) x = x / (1.f + __expf(-x));
-        out[i] = __float2bfloat16_rn(x);
-      }
-    }
-  }
-}
-
-template <int BN, int STAGES, int EPI>
-__global__ void __launch_bounds__(TC_THREADS, 1)
-    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const GemmArgs p) {
-  static_assert(BN >= 16 && BN <= 256 && (BN & (BN - 1)) == 0, "BN: power of two in [16, 256]");
-  constexpr uint32_t kTmemCols = (2 * BN < 32) ? 32 : 2 * BN;
-  constexpr uint32_t kIdesc = bf16_idesc(TC_BM, BN);
-  constexpr uint32_t kStageBytes = (TC_BM + BN) * TC_BK * 2;
-  constexpr int CH = BN < 32 ? BN : 32;
-  using Smem = TcSmem<BN, STAGES>;
-
-  extern __shared__ uint8_t smem_raw[];
-  Smem& S = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                     ~static_cast<uintptr_t>(1023));
+// Barrier set-up, TMEM allocation and the per-group prefix of ceil(rows_g / unit)
+// (rows_g from the offsets, or m_rows for a single dense group).  All threads call.
+// CTAS = CTAs per cluster whose MMAs read (and so must release) each stage.
+template <class Smem, int STAGES, int CTAS>
+__device__ __forceinline__ void pipe_prologue(Smem& S, uint32_t tmem_cols, const GemmArgs& p,
+                                              int G, int unit, const void* tmA,
+                                              const void* tmB) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
   if (threadIdx.x == 0) {
 #pragma unroll
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(smem_u32(&S.full[s]), 1);
-      mbar_init(smem_u32(&S.empty[s]), 1);
+      mbar_init(smem_u32(&S.empty[s]), CTAS);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&S.tfull[i]), 1);
@@ -179,133 +93,465 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     mbar_init(smem_u32(&S.drain), 1);
     S.abort = 0;
     fence_mbar_init();
-    tma_prefetch_desc(&tmA);
-    tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(tmA);
+    tma_prefetch_desc(tmB);
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(&S.tmem_base), kTmemCols);
+    tmem_alloc(smem_u32(&S.tmem_base), tmem_cols);
     tmem_relinquish();
   }
-  const int G = p.offsets ? p.G : 1;
   if (warp == 0) {
-    // Row-tile prefix over the groups: mpref[g] = sum_{g' < g} ceil(rows_g' / 128).
     int carry = 0;
-    if (lane == 0) S.mpref[0] = 0;
+    if (lane == 0) S.pref[0] = 0;
     for (int base = 0; base < G; base += 32) {
       const int g = base + lane;
-      int mt = 0;
+      int units = 0;
       if (g < G) {
         const int64_t rows = p.offsets ? (p.offsets[g + 1] - p.offsets[g]) : p.m_rows;
-        mt = rows > 0 ? static_cast<int>((rows + TC_BM - 1) / TC_BM) : 0;
+        units = rows > 0 ? static_cast<int>((rows + unit - 1) / unit) : 0;
       }
-      int v = mt;
+      int v = units;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int n = __shfl_up_sync(0xffffffffu, v, o);
         if (lane >= o) v += n;
       }
-      if (g < G) S.mpref[g + 1] = carry + v;
+      if (g < G) S.pref[g + 1] = carry + v;
       carry += __shfl_sync(0xffffffffu, v, 31);
     }
   }
   tc_fence_before();
-  __syncthreads();
+  if (CTAS > 1)
+    cluster_sync_all();  // peers' barriers are initialised before anyone multicasts
+  else
+    __syncthreads();
   tc_fence_after();
+}
 
-  const uint32_t tmem_base = S.tmem_base;
-  const int NB = (p.N + BN - 1) / BN;
-  const int total = S.mpref[G] * NB;
+// Group of a tile: the g with pref[g]*per <= tile < pref[g+1]*per.
+__device__ __forceinline__ int find_group(const int* pref, int G, int per, int tile) {
+  int lo = 0, hi = G;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (pref[mid] * per <= tile) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+// Warp 0, lane 0, over tiles first, first + step, ...  decode(tile) -> coordinates
+// with the stage's byte count in .bytes; load(coords, kb, smem_a, smem_b, bar).
+template <int STAGES, class Smem, class Decode, class Load>
+__device__ __forceinline__ void run_producer(Smem& S, int first, int step, int total, int KB,
+                                             Decode decode, Load load, volatile int* abort,
+                                             int* flags) {
+  int s = 0;
+  uint32_t ph = 0, issued = 0, issued_par = 0;
+  bool ok = true;
+  for (int tile = first; ok && tile < total; tile += step) {
+    const auto c = decode(tile);
+    for (int kb = 0; kb < KB; ++kb) {
+      if (!mbar_wait_bounded(smem_u32(&S.empty[s]), ph ^ 1u, abort, flags)) {
+        ok = false;
+        break;
+      }
+      const uint32_t fb = smem_u32(&S.full[s]);
+      mbar_arrive_expect_tx(fb, c.bytes);
+      load(c, kb, smem_u32(S.a[s]), smem_u32(S.b[s]), fb);
+      issued |= 1u << s;
+      issued_par = (issued_par & ~(1u << s)) | (ph << s);
+      if (++s == STAGES) {
+        s = 0;
+        ph ^= 1u;
+      }
+    }
+  }
+  if (!ok) {
+    // Unwinding: let this CTA's copies in flight land before it exits.
+    for (int q = 0; q < STAGES; ++q)
+      if ((issued >> q) & 1u) mbar_wait_unwind(smem_u32(&S.full[q]), (issued_par >> q) & 1u);
+  }
+}
+
+// Warp 1, lane 0.  idesc_of(tile) -> instruction descriptor of the tile's MMAs.
+// With CTAS = 2 each stage is released on both CTAs of the cluster.
+template <int STAGES, int ACC_COLS, int CTAS, class Smem, class Idesc>
+__device__ __forceinline__ void run_mma(Smem& S, int first, int step, int total, int KB,
+                                        uint32_t tmem_base, Idesc idesc_of, volatile int* abort,
+                                        int* flags) {
+  int s = 0, acc = 0;
+  uint32_t ph = 0, aph = 0;
+  bool ok = true, issued_any = false;
+  for (int tile = first; ok && tile < total; tile += step) {
+    const uint32_t idesc = idesc_of(tile);
+    if (!mbar_wait_bounded(smem_u32(&S.tempty[acc]), aph ^ 1u, abort, flags)) {
+      ok = false;
+      break;
+    }
+    tc_fence_after();
+    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * ACC_COLS);
+    for (int kb = 0; kb < KB; ++kb) {
+      if (!mbar_wait_bounded(smem_u32(&S.full[s]), ph, abort, flags)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t a0 = smem_u32(S.a[s]), b0 = smem_u32(S.b[s]);
+#pragma unroll
+      for (int kk = 0; kk < TC_BK / 16; ++kk)
+        tc_mma_bf16(d_tmem, sw128_kmajor_desc(a0 + kk * 32), sw128_kmajor_desc(b0 + kk * 32),
+                    idesc, (kb | kk) != 0 ? 1u : 0u);
+      issued_any = true;
+      if (CTAS > 1)
+        tc_commit_multicast(smem_u32(&S.empty[s]), static_cast<uint16_t>((1u << CTAS) - 1u));
+      else
+        tc_commit(smem_u32(&S.empty[s]));
+      if (++s == STAGES) {
+        s = 0;
+        ph ^= 1u;
+      }
+    }
+    if (!ok) break;
+    tc_commit(smem_u32(&S.tfull[acc]));
+    acc ^= 1;
+    if (acc == 0) aph ^= 1u;
+  }
+  // Unwinding: every MMA issued by this thread completes before TMEM is released.
+  // (On the normal path the epilogue has already waited for all of them.)
+  if (!ok && issued_any) {
+    tc_commit(smem_u32(&S.drain));
+    mbar_wait_unwind(smem_u32(&S.drain), 0);
+  }
+}
+
+// With CTAS > 1 no CTA leaves before its peer has stopped writing into its shared
+// memory (multicast copies, commit arrivals).
+template <int CTAS, class Smem>
+__device__ __forceinline__ void pipe_teardown(Smem& S, uint32_t tmem_cols) {
+  tc_fence_before();
+  __syncthreads();
+  if ((threadIdx.x >> 5) == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(S.tmem_base, tmem_cols);
+  }
+  if (CTAS > 1) cluster_sync_all();
+}
+
+template <class Smem>
+__device__ __forceinline__ Smem& smem_aligned() {
+  extern __shared__ uint8_t smem_raw[];
+  return *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                  ~static_cast<uintptr_t>(1023));
+}
+
+__device__ __forceinline__ float silu(float x) { return x / (1.f + __expf(-x)); }
+
+// ------------------------------------------------------------- expert FFN GEMM
+// A = weight block [128 x 64] of W[g] (3-D map over [G, N, K]); B = token block of
+// up to TB rows, loaded as 32-row boxes (2-D map over [rows_alloc, K]) and shared by
+// the two CTAs of a cluster; D[128 x ntok] in TMEM, lane = output feature, column =
+// token.
+constexpr int TOK_BOX = 32;
+
+template <int TB, int STAGES, int EPI>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
+    tc_ffn_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                  const GemmArgs p) {
+  static_assert(TB >= TOK_BOX && TB <= 256 && (TB & (TB - 1)) == 0,
+                "TB: power of two in [32, 256]");
+  static_assert(EPI == EPI_BIAS_SILU || EPI == EPI_BIAS, "expert epilogues only");
+  constexpr int CTAS = 2;
+  constexpr uint32_t kTmemCols = 2 * TB;
+  constexpr uint32_t kWeightBytes = TILE_M * TC_BK * 2;
+  constexpr uint32_t kBoxBytes = TOK_BOX * TC_BK * 2;
+  using Smem = PipeSmem<TILE_M * TC_BK * 2, TB * TC_BK * 2, STAGES>;
+  Smem& S = smem_aligned<Smem>();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rank = static_cast<int>(cluster_ctarank());
+  const int G = p.G;
+  pipe_prologue<Smem, STAGES, CTAS>(S, kTmemCols, p, G, TB, &tmW, &tmX);
+
+  const int MB = (p.N + TILE_M - 1) / TILE_M;  // weight blocks per group
+  const int MP = (MB + 1) / 2;                  // weight-block pairs per group
+  const int total = S.pref[G] * MP;
   const int KB = (p.K + TC_BK - 1) / TC_BK;
+  const int first = static_cast<int>(blockIdx.x) / CTAS, step = static_cast<int>(gridDim.x) / CTAS;
   volatile int* abort = &S.abort;
 
+  struct Coord {
+    int g, n0, ntok, nbox;
+    uint32_t bytes;
+    int64_t row0, row_end;
+  };
+  auto decode = [&](int tile) {
+    Coord c;
+    c.g = find_group(S.pref, G, MP, tile);
+    const int nt = S.pref[c.g + 1] - S.pref[c.g];
+    const int local = tile - S.pref[c.g] * MP;
+    c.n0 = (2 * (local / nt) + rank) * TILE_M;
+    const int64_t base = p.offsets[c.g], end = p.offsets[c.g + 1];
+    const int64_t bsz = (((end - base) + nt - 1) / nt + 15) & ~int64_t{15};
+    c.row0 = base + (local % nt) * bsz;
+    c.row_end = c.row0 + bsz < end ? c.row0 + bsz : end;
+    c.ntok = static_cast<int>((c.row_end - c.row0 + 15) & ~int64_t{15});
+    c.nbox = (c.ntok + TOK_BOX - 1) / TOK_BOX;
+    c.bytes = kWeightBytes + static_cast<uint32_t>(c.nbox) * kBoxBytes;
+    return c;
+  };
+
   if (warp == 0) {
-    if (lane == 0) {
-      // ------------------------------------------------ TMA producer
-      int s = 0;
-      uint32_t ph = 0, issued = 0, issued_par = 0;
-      bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-        const TileCoord c = decode_tile(tile, S.mpref, G, NB, p, BN);
-        for (int kb = 0; kb < KB; ++kb) {
-          if (!mbar_wait_bounded(smem_u32(&S.empty[s]), ph ^ 1u, abort, p.flags)) {
-            ok = false;
-            break;
-          }
-          const uint32_t fb = smem_u32(&S.full[s]);
-          mbar_arrive_expect_tx(fb, kStageBytes);
-          tma_load_2d(smem_u32(S.a[s]), &tmA, fb, kb * TC_BK, static_cast<int>(c.row0));
-          tma_load_3d(smem_u32(S.b[s]), &tmB, fb, kb * TC_BK, c.n0, c.g);
-          issued |= 1u << s;
-          issued_par = (issued_par & ~(1u << s)) | (ph << s);
-          if (++s == STAGES) {
-            s = 0;
-            ph ^= 1u;
-          }
-        }
-      }
-      if (!ok) {
-        // Unwinding: let this CTA's copies in flight land before it exits.
-        for (int q = 0; q < STAGES; ++q)
-          if ((issued >> q) & 1u) mbar_wait_unwind(smem_u32(&S.full[q]), (issued_par >> q) & 1u);
-      }
-    }
+    if (lane == 0)
+      run_producer<STAGES>(
+          S, first, step, total, KB, decode,
+          [&](const Coord& c, int kb, uint32_t sa, uint32_t sb, uint32_t bar) {
+            tma_load_3d(sa, &tmW, bar, kb * TC_BK, c.n0, c.g);
+            for (int j = rank; j < c.nbox; j += CTAS)
+              tma_load_2d_multicast(sb + j * kBoxBytes, &tmX, bar, kb * TC_BK,
+                                    static_cast<int>(c.row0) + j * TOK_BOX, 0x3);
+          },
+          abort, p.flags);
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ------------------------------------------------ MMA issuer
-      int s = 0, acc = 0;
-      uint32_t ph = 0, aph = 0;
-      bool ok = true, issued_any = false;
-      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-        if (!mbar_wait_bounded(smem_u32(&S.tempty[acc]), aph ^ 1u, abort, p.flags)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-        for (int kb = 0; kb < KB; ++kb) {
-          if (!mbar_wait_bounded(smem_u32(&S.full[s]), ph, abort, p.flags)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t a0 = smem_u32(S.a[s]), b0 = smem_u32(S.b[s]);
-#pragma unroll
-          for (int kk = 0; kk < TC_BK / 16; ++kk)
-            tc_mma_bf16(d_tmem, sw128_kmajor_desc(a0 + kk * 32), sw128_kmajor_desc(b0 + kk * 32),
-                        kIdesc, (kb | kk) != 0 ? 1u : 0u);
-          issued_any = true;
-          tc_commit(smem_u32(&S.empty[s]));
-          if (++s == STAGES) {
-            s = 0;
-            ph ^= 1u;
-          }
-        }
-        if (!ok) break;
-        tc_commit(smem_u32(&S.tfull[acc]));
-        acc ^= 1;
-        if (acc == 0) aph ^= 1u;
-      }
-      // Unwinding: every MMA issued by this thread completes before TMEM is released.
-      // (On the normal path the epilogue has already waited for all of them.)
-      if (!ok && issued_any) {
-        tc_commit(smem_u32(&S.drain));
-        mbar_wait_unwind(smem_u32(&S.drain), 0);
-      }
-    }
+    if (lane == 0)
+      run_mma<STAGES, TB, CTAS>(
+          S, first, step, total, KB, S.tmem_base,
+          [&](int tile) { return bf16_idesc(TILE_M, decode(tile).ntok); }, abort, p.flags);
   } else {
-    // -------------------------------------------------- epilogue (warps 2..5)
     const int quad = warp & 3;  // TMEM lanes this warp may read: 32*quad .. 32*quad+31
-    const int r_in = quad * 32 + lane;
     int acc = 0;
     uint32_t aph = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-      const TileCoord c = decode_tile(tile, S.mpref, G, NB, p, BN);
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
+    const __nv_bfloat16* bias = static_cast<const __nv_bfloat16*>(p.bias);
+    for (int tile = first; tile < total; tile += step) {
+      const Coord c = decode(tile);
+      const int n = c.n0 + quad * 32 + lane;
+      const bool n_ok = n < p.N;
+      const float b = (bias && n_ok) ? __bfloat162float(bias[static_cast<int64_t>(c.g) * p.N + n])
+                                     : 0.f;
       const bool got = mbar_wait_bounded(smem_u32(&S.tfull[acc]), aph, abort, p.flags);
       if (!__all_sync(0xffffffffu, got)) break;  // the warp-collective loads need every lane
       tc_fence_after();
-      const int64_t row = c.row0 + r_in;
+      const uint32_t t_row = S.tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
+                             static_cast<uint32_t>(acc * TB);
+      const int nrows = static_cast<int>(c.row_end - c.row0);
+#pragma unroll 1
+      for (int col = 0; col < c.ntok; col += 32) {
+        float v[32];
+        tmem_ld_32cols(t_row + col, v);
+        tc_wait_ld();
+        if (n_ok) {
+          __nv_bfloat16* o = out + (c.row0 + col) * p.N + n;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            if (col + i < nrows) {
+              float x = v[i] + b;
+              if (EPI == EPI_BIAS_SILU) x = silu(x);
+              o[static_cast<int64_t>(i) * p.N] = __float2bfloat16_rn(x);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(smem_u32(&S.tempty[acc]));
+      acc ^= 1;
+      if (acc == 0) aph ^= 1u;
+    }
+  }
+  pipe_teardown<CTAS>(S, kTmemCols);
+}
+
+// ------------------------------------------------------------- expert FFN, row tiles
+// A = token block [128 x 64] of the row buffer (2-D map); B = weight block [BN x 64]
+// of W[g] (3-D map over [G, N, K]); D[128 x BN] in TMEM, lane = token row, column =
+// output feature.  Used for large expert groups (hundreds of rows and more), where a
+// 128-row tile is mostly full.  The epilogue writes each row's 32-column pieces as
+// 16-byte stores; rows past the group's end belong to the next expert and are not
+// written.
+template <int BN, int STAGES, int EPI>
+__global__ void __launch_bounds__(TC_THREADS, 1)
+    tc_rows_ffn_kernel(const __grid_constant__ CUtensorMap tmX,
+                       const __grid_constant__ CUtensorMap tmW, const GemmArgs p) {
+  static_assert(BN % 32 == 0 && BN <= 256 && (BN & (BN - 1)) == 0, "BN: power of two, <= 256");
+  static_assert(EPI == EPI_BIAS_SILU || EPI == EPI_BIAS, "expert epilogues only");
+  constexpr uint32_t kTmemCols = 2 * BN;
+  constexpr uint32_t kIdesc = bf16_idesc(TILE_M, BN);
+  constexpr uint32_t kStageBytes = (TILE_M + BN) * TC_BK * 2;
+  using Smem = PipeSmem<TILE_M * TC_BK * 2, BN * TC_BK * 2, STAGES>;
+  Smem& S = smem_aligned<Smem>();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = p.G;
+  pipe_prologue<Smem, STAGES, 1>(S, kTmemCols, p, G, TILE_M, &tmX, &tmW);
+
+  const int NB = (p.N + BN - 1) / BN;
+  const int total = S.pref[G] * NB;
+  const int KB = (p.K + TC_BK - 1) / TC_BK;
+  volatile int* abort = &S.abort;
+
+  struct Coord {
+    int g, n0;
+    uint32_t bytes;
+    int64_t row0, row_end;
+  };
+  auto decode = [&](int tile) {
+    Coord c;
+    c.g = find_group(S.pref, G, NB, tile);
+    const int mt = S.pref[c.g + 1] - S.pref[c.g];
+    const int local = tile - S.pref[c.g] * NB;
+    c.n0 = (local / mt) * BN;
+    c.row0 = p.offsets[c.g] + static_cast<int64_t>(local % mt) * TILE_M;
+    c.row_end = p.offsets[c.g + 1];
+    c.bytes = kStageBytes;
+    return c;
+  };
+
+  if (warp == 0) {
+    if (lane == 0)
+      run_producer<STAGES>(
+          S, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), total, KB, decode,
+          [&](const Coord& c, int kb, uint32_t sa, uint32_t sb, uint32_t bar) {
+            tma_load_2d(sa, &tmX, bar, kb * TC_BK, static_cast<int>(c.row0));
+            tma_load_3d(sb, &tmW, bar, kb * TC_BK, c.n0, c.g);
+          },
+          abort, p.flags);
+  } else if (warp == 1) {
+    if (lane == 0)
+      run_mma<STAGES, BN, 1>(S, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), total,
+                             KB, S.tmem_base, [](int) { return kIdesc; }, abort, p.flags);
+  } else {
+    const int quad = warp & 3;  // TMEM lanes this warp may read: 32*quad .. 32*quad+31
+    const __nv_bfloat16* bias_base = static_cast<const __nv_bfloat16*>(p.bias);
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
+    int acc = 0;
+    uint32_t aph = 0;
+    for (int tile = static_cast<int>(blockIdx.x); tile < total; tile += static_cast<int>(gridDim.x)) {
+      const Coord c = decode(tile);
+      const bool got = mbar_wait_bounded(smem_u32(&S.tfull[acc]), aph, abort, p.flags);
+      if (!__all_sync(0xffffffffu, got)) break;  // the warp-collective loads need every lane
+      tc_fence_after();
+      const int64_t row = c.row0 + quad * 32 + lane;
       const bool valid = row < c.row_end;
-      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
+      const uint32_t t_row = S.tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
+                             static_cast<uint32_t>(acc * BN);
+      const __nv_bfloat16* bias =
+          bias_base ? bias_base + static_cast<int64_t>(c.g) * p.N + c.n0 : nullptr;
+#pragma unroll 1
+      for (int col = 0; col < BN; col += 32) {
+        float v[32];
+        tmem_ld_32cols(t_row + col, v);
+        tc_wait_ld();
+        if (!valid || c.n0 + col >= p.N) continue;
+        __nv_bfloat16* o = out + row * p.N + c.n0 + col;
+        const bool whole = c.n0 + col + 32 <= p.N;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          float b[8];
+          if (bias && whole) {
+            const uint4 bv = __ldg(reinterpret_cast<const uint4*>(bias + col + 8 * q));
+            const __nv_bfloat162* bh = reinterpret_cast<const __nv_bfloat162*>(&bv);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float2 f = __bfloat1622float2(bh[i]);
+              b[2 * i] = f.x;
+              b[2 * i + 1] = f.y;
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              b[i] = (bias && c.n0 + col + 8 * q + i < p.N) ? __bfloat162float(bias[col + 8 * q + i])
+                                                              : 0.f;
+          }
+          uint4 packed;
+          __nv_bfloat162* ph = reinterpret_cast<__nv_bfloat162*>(&packed);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            float x0 = v[8 * q + 2 * i] + b[2 * i];
+            float x1 = v[8 * q + 2 * i + 1] + b[2 * i + 1];
+            if (EPI == EPI_BIAS_SILU) {
+              x0 = silu(x0);
+              x1 = silu(x1);
+            }
+            ph[i] = __floats2bfloat162_rn(x0, x1);
+          }
+          if (whole) {
+            *reinterpret_cast<uint4*>(o + 8 * q) = packed;
+          } else {
+            const __nv_bfloat16* pv = reinterpret_cast<const __nv_bfloat16*>(&packed);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              if (c.n0 + col + 8 * q + i < p.N) o[8 * q + i] = pv[i];
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(smem_u32(&S.tempty[acc]));
+      acc ^= 1;
+      if (acc == 0) aph ^= 1u;
+    }
+  }
+  pipe_teardown<1>(S, kTmemCols);
+}
+
+// ------------------------------------------------------------- router GEMM
+// A = token block [128 x 64] of x; B = expert block [BN x 64] of W_g; D[128 x BN],
+// lane = token, column = expert; fp32 output plus the fp32 logit bias.
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(TC_THREADS, 1)
+    tc_router_kernel(const __grid_constant__ CUtensorMap tmX,
+                     const __grid_constant__ CUtensorMap tmW, const GemmArgs p) {
+  static_assert(BN >= 16 && BN <= 256 && (BN & (BN - 1)) == 0, "BN: power of two in [16, 256]");
+  constexpr uint32_t kTmemCols = (2 * BN < 32) ? 32 : 2 * BN;
+  constexpr uint32_t kIdesc = bf16_idesc(TILE_M, BN);
+  constexpr uint32_t kStageBytes = (TILE_M + BN) * TC_BK * 2;
+  constexpr int CH = BN < 32 ? BN : 32;
+  using Smem = PipeSmem<TILE_M * TC_BK * 2, BN * TC_BK * 2, STAGES>;
+  Smem& S = smem_aligned<Smem>();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pipe_prologue<Smem, STAGES, 1>(S, kTmemCols, p, 1, TILE_M, &tmX, &tmW);
+
+  const int NB = (p.N + BN - 1) / BN;
+  const int total = S.pref[1] * NB;
+  const int KB = (p.K + TC_BK - 1) / TC_BK;
+  volatile int* abort = &S.abort;
+
+  struct Coord {
+    int n0;
+    uint32_t bytes;
+    int64_t row0;
+  };
+  auto decode = [&](int tile) {
+    Coord c;
+    c.bytes = kStageBytes;
+    const int mt = S.pref[1];
+    c.n0 = (tile / mt) * BN;
+    c.row0 = static_cast<int64_t>(tile % mt) * TILE_M;
+    return c;
+  };
+
+  if (warp == 0) {
+    if (lane == 0)
+      run_producer<STAGES>(
+          S, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), total, KB, decode,
+          [&](const Coord& c, int kb, uint32_t sa, uint32_t sb, uint32_t bar) {
+            tma_load_2d(sa, &tmX, bar, kb * TC_BK, static_cast<int>(c.row0));
+            tma_load_3d(sb, &tmW, bar, kb * TC_BK, c.n0, 0);
+          },
+          abort, p.flags);
+  } else if (warp == 1) {
+    if (lane == 0)
+      run_mma<STAGES, BN, 1>(S, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), total,
+                             KB, S.tmem_base, [](int) { return kIdesc; }, abort, p.flags);
+  } else {
+    const int quad = warp & 3;
+    int acc = 0;
+    uint32_t aph = 0;
+    float* out = static_cast<float*>(p.out);
+    const float* bias = static_cast<const float*>(p.bias);
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      const Coord c = decode(tile);
+      const bool got = mbar_wait_bounded(smem_u32(&S.tfull[acc]), aph, abort, p.flags);
+      if (!__all_sync(0xffffffffu, got)) break;
+      tc_fence_after();
+      const int64_t row = c.row0 + quad * 32 + lane;
+      const uint32_t t_row = S.tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
                              static_cast<uint32_t>(acc * BN);
 #pragma unroll 1
       for (int col = 0; col < BN; col += CH) {
@@ -315,7 +561,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         else
           tmem_ld_16cols(t_row + col, v);
         tc_wait_ld();
-        if (valid) epilogue_store<EPI, CH>(p, c.g, row, c.n0 + col, v);
+        if (row < p.m_rows) {
+#pragma unroll
+          for (int i = 0; i < CH; ++i) {
+            const int e = c.n0 + col + i;
+            if (e < p.N) out[row * p.N + e] = v[i] + (bias ? bias[e] : 0.f);
+          }
+        }
       }
       tc_fence_before();
       mbar_arrive(smem_u32(&S.tempty[acc]));
@@ -323,14 +575,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       if (acc == 0) aph ^= 1u;
     }
   }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    __syncwarp();
-    tc_fence_after();
-    tmem_dealloc(tmem_base, kTmemCols);
-  }
+  pipe_teardown<1>(S, kTmemCols);
 }
 
 // ------------------------------------------------------------------ host side
@@ -360,51 +605,132 @@ bool encode_bf16_map(CUtensorMap* m, const void* base, int rank, const cuuint64_
   return r == CUDA_SUCCESS;
 }
 
-template <int BN, int STAGES, int EPI>
-cudaError_t launch_tc(const GemmArgs& a, int sm_count, cudaStream_t stream) {
-  CUtensorMap tmA, tmB;
-  const int64_t a_rows = a.offsets ? a.rows_alloc : a.m_rows;
-  const cuuint64_t a_dims[2] = {static_cast<cuuint64_t>(a.K), static_cast<cuuint64_t>(a_rows)};
-  const cuuint64_t a_str[1] = {static_cast<cuuint64_t>(a.K) * 2};
-  const cuuint32_t a_box[2] = {TC_BK, TC_BM};
-  const int G = a.offsets ? a.G : 1;
-  const cuuint64_t b_dims[3] = {static_cast<cuuint64_t>(a.K), static_cast<cuuint64_t>(a.N),
-                                static_cast<cuuint64_t>(G)};
-  const cuuint64_t b_str[2] = {static_cast<cuuint64_t>(a.K) * 2,
-                               static_cast<cuuint64_t>(a.N) * a.K * 2};
-  const cuuint32_t b_box[3] = {TC_BK, BN, 1};
-  if (!encode_bf16_map(&tmA, a.A, 2, a_dims, a_str, a_box) ||
-      !encode_bf16_map(&tmB, a.B, 3, b_dims, b_str, b_box))
-    return cudaErrorInvalidValue;
+// 2-D map over a row-major [rows, K] bf16 matrix, box [box_rows x box_cols].
+bool rows_map(CUtensorMap* m, const void* base, int64_t rows, int K, int box_rows,
+              int box_cols = TC_BK) {
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t str[1] = {static_cast<cuuint64_t>(K) * 2};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
+  return encode_bf16_map(m, base, 2, dims, str, box);
+}
 
-  const int64_t mtiles = a.offsets ? (a.rows_alloc + TC_BM - 1) / TC_BM + G
-                                   : (a.m_rows + TC_BM - 1) / TC_BM;
-  const int64_t bound = mtiles * ((a.N + BN - 1) / BN);
-  const int grid = static_cast<int>(std::min<int64_t>(bound, sm_count));
+// 3-D map over stacked [G, N, K] bf16 weights, box [box_rows x 64] of one group.
+bool stacked_map(CUtensorMap* m, const void* base, int G, int N, int K, int box_rows) {
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(N),
+                              static_cast<cuuint64_t>(G)};
+  const cuuint64_t str[2] = {static_cast<cuuint64_t>(K) * 2, static_cast<cuuint64_t>(N) * K * 2};
+  const cuuint32_t box[3] = {TC_BK, static_cast<cuuint32_t>(box_rows), 1};
+  return encode_bf16_map(m, base, 3, dims, str, box);
+}
+
+template <class Kern>
+cudaError_t launch_pipe(Kern kern, size_t smem, int grid, const CUtensorMap& a,
+                        const CUtensorMap& b, const GemmArgs& args, cudaStream_t stream) {
   if (grid <= 0) return cudaSuccess;
-  const size_t smem = sizeof(TcSmem<BN, STAGES>) + 1024;
-  auto kern = tc_gemm_kernel<BN, STAGES, EPI>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  kern<<<grid, TC_THREADS, smem, stream>>>(tmA, tmB, a);
+  kern<<<grid, TC_THREADS, smem, stream>>>(a, b, args);
   return cudaGetLastError();
 }
+
+// Clusters of two that can be resident at once (one CTA per SM), per device.
+template <class Kern>
+int resident_clusters(Kern kern, size_t smem, int sm_count) {
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return sm_count / 2;
+  if (cached[dev] > 0) return cached[dev];
+  int n = 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(sm_count / 2 * 2));
+  cfg.blockDim = dim3(TC_THREADS);
+  cfg.dynamicSmemBytes = smem;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
+    (void)cudaGetLastError();
+    n = sm_count / 2;
+  }
+  cached[dev] = n;
+  return n;
+}
+
+template <int TB, int STAGES, int EPI>
+cudaError_t launch_ffn(const GemmArgs& a, int sm_count, cudaStream_t stream) {
+  CUtensorMap tmW, tmX;
+  if (!stacked_map(&tmW, a.B, a.G, a.N, a.K, TILE_M) ||
+      !rows_map(&tmX, a.A, a.rows_alloc, a.K, TOK_BOX))
+    return cudaErrorInvalidValue;
+  using Smem = PipeSmem<TILE_M * TC_BK * 2, TB * TC_BK * 2, STAGES>;
+  const size_t smem = sizeof(Smem) + 1024;
+  auto kern = tc_ffn_kernel<TB, STAGES, EPI>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  // Upper bound on tile pairs: sum_g ceil(rows_g / TB) <= rows_alloc / TB + G.
+  const int64_t bound =
+      ((a.rows_alloc + TB - 1) / TB + a.G) * (((a.N + TILE_M - 1) / TILE_M + 1) / 2);
+  const int64_t clusters =
+      std::min<int64_t>(bound, resident_clusters(kern, smem, sm_count));
+  if (clusters <= 0) return cudaSuccess;
+  kern<<<static_cast<unsigned>(2 * clusters), TC_THREADS, smem, stream>>>(tmW, tmX, a);
+  return cudaGetLastError();
+}
+
+template <int BN, int STAGES, int EPI>
+cudaError_t launch_rows_ffn(const GemmArgs& a, int sm_count, cudaStream_t stream) {
+  CUtensorMap tmX, tmW;
+  if (!rows_map(&tmX, a.A, a.rows_alloc, a.K, TILE_M) || !stacked_map(&tmW, a.B, a.G, a.N, a.K, BN))
+    return cudaErrorInvalidValue;
+  // Upper bound on tiles: sum_g ceil(rows_g / 128) <= rows_alloc / 128 + G.
+  const int64_t bound = ((a.rows_alloc + TILE_M - 1) / TILE_M + a.G) * ((a.N + BN - 1) / BN);
+  const int grid = static_cast<int>(std::min<int64_t>(bound, sm_count));
+  using Smem = PipeSmem<TILE_M * TC_BK * 2, BN * TC_BK * 2, STAGES>;
+  return launch_pipe(tc_rows_ffn_kernel<BN, STAGES, EPI>, sizeof(Smem) + 1024, grid, tmX, tmW, a,
+                     stream);
+}
+
+template <int BN, int STAGES>
+cudaError_t launch_router(const GemmArgs& a, int sm_count, cudaStream_t stream) {
+  CUtensorMap tmX, tmW;
+  if (!rows_map(&tmX, a.A, a.m_rows, a.K, TILE_M) || !stacked_map(&tmW, a.B, 1, a.N, a.K, BN))
+    return cudaErrorInvalidValue;
+  const int64_t bound = ((a.m_rows + TILE_M - 1) / TILE_M) * ((a.N + BN - 1) / BN);
+  const int grid = static_cast<int>(std::min<int64_t>(bound, sm_count));
+  using Smem = PipeSmem<TILE_M * TC_BK * 2, BN * TC_BK * 2, STAGES>;
+  return launch_pipe(tc_router_kernel<BN, STAGES>, sizeof(Smem) + 1024, grid, tmX, tmW, a, stream);
+}
+
+// Token-block height for an expert GEMM: the smallest power of two (32..256) that
+// holds the largest group the routing can produce.
+template <int EPI>
+cudaError_t launch_ffn_for(const GemmArgs& a, int max_group, int sm_count, cudaStream_t stream) {
+  if (max_group <= 32) return launch_ffn<32, 8, EPI>(a, sm_count, stream);
+  if (max_group <= 64) return launch_ffn<64, 8, EPI>(a, sm_count, stream);
+  if (max_group <= 128) return launch_ffn<128, 6, EPI>(a, sm_count, stream);
+  return launch_ffn<256, 4, EPI>(a, sm_count, stream);
+}
+
+// Largest expert group (rows) for which the weights-as-M cluster kernel is used:
+// there a 128-row tile would be mostly padding, while 128 weight rows always fill
+// the MMA's M side.  Larger groups use row tiles, whose main loop measured faster.
+constexpr int kSmallGroup = 128;
 
 }  // namespace
 
 cudaError_t launch_tc_gemm_bf16(const GemmArgs& a, int epi, int sm_count, cudaStream_t stream) {
   switch (epi) {
     case EPI_BIAS_SILU:
-      return launch_tc<256, 4, EPI_BIAS_SILU>(a, sm_count, stream);
+      return a.max_group > kSmallGroup ? launch_rows_ffn<256, 4, EPI_BIAS_SILU>(a, sm_count, stream)
+                                       : launch_ffn_for<EPI_BIAS_SILU>(a, a.max_group, sm_count, stream);
     case EPI_BIAS:
-      return launch_tc<256, 4, EPI_BIAS>(a, sm_count, stream);
+      return a.max_group > kSmallGroup ? launch_rows_ffn<256, 4, EPI_BIAS>(a, sm_count, stream)
+                                       : launch_ffn_for<EPI_BIAS>(a, a.max_group, sm_count, stream);
     default:
       // Router: N = E columns; the narrowest power-of-two tile that covers them, at most 128.
-      if (a.N <= 16) return launch_tc<16, 8, EPI_ROUTER_F32>(a, sm_count, stream);
-      if (a.N <= 32) return launch_tc<32, 8, EPI_ROUTER_F32>(a, sm_count, stream);
-      if (a.N <= 64) return launch_tc<64, 8, EPI_ROUTER_F32>(a, sm_count, stream);
-      return launch_tc<128, 6, EPI_ROUTER_F32>(a, sm_count, stream);
+      if (a.N <= 16) return launch_router<16, 8>(a, sm_count, stream);
+      if (a.N <= 32) return launch_router<32, 8>(a, sm_count, stream);
+      if (a.N <= 64) return launch_router<64, 8>(a, sm_count, stream);
+      return launch_router<128, 6>(a, sm_count, stream);
   }
 }
 

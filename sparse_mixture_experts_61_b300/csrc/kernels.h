@@ -48,6 +48,7 @@ struct GemmArgs {
   const int32_t* offsets; // [G+1] device, or nullptr
   int64_t m_rows;         // rows when offsets == nullptr
   int G, N, K;
+  int max_group;          // upper bound on any group's rows (sizes the token tile)
   int* flags;
 };
 

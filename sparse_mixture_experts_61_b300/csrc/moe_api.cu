@@ -147,6 +147,10 @@ moe_status run_expert_ffn(const moe_config& c, const void* x_perm, const int32_t
   g1.G = c.E;
   g1.N = c.h;
   g1.K = c.d;
+  // A valid routing gives an expert at most T rows (one per token), and at most C
+  // with a capacity; the tile height follows this bound.
+  const int64_t C = capacity_of(c);
+  g1.max_group = static_cast<int>(C >= 0 && C < c.T ? C : c.T);
   g1.flags = flags;
   GemmArgs g2 = g1;
   g2.A = h_buf;
