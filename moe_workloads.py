@@ -77,6 +77,12 @@ WORKLOADS = {
                        gate=GATE_TOPK_SOFTMAX, capacity_factor=0.0, logit_bias="normal1.5"),
 }
 
+# Same per-expert shape as the 256-expert workload (d=7168, h=2048, top-8, ~256 rows
+# per expert) with 32 experts and 1024 tokens: 1.9 GB of weights, small enough for
+# multi-pass profiler captures while keeping the weights far larger than L2.
+WORKLOADS["deepseek_fine_e32"] = WORKLOADS["deepseek_fine"].scaled(name="deepseek_fine_e32",
+                                                                  T=1024, E=32)
+
 # Reduced-size variants with each workload's structure (expert count, k, gate, capacity,
 # bias recipe) that the oracle evaluates in full in seconds, while still spanning several
 # 128-row tiles, several 256-column tiles and a ragged tail.

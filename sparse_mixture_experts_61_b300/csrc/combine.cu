@@ -1,8 +1,8 @@
 // Combine: y[t,:] = sum_{j kept} w[t,j] * y_perm[slot_row[t,j], :]
 // ("MoE mixture-of-experts routing mechanism": y = sum_{i<=K} G(x)_i E_i(x); the
 // MoELayer listing adds each slot's weighted expert output in slot order).
-// One warp per token; each lane owns 16-byte column vectors; the k slot
-// contributions are added in slot order in fp32 and rounded once.  No atomics.
+// One thread per 16-byte output vector; the k slot contributions are added in slot
+// order in fp32 and rounded once.  No atomics.
 
 #include "common.cuh"
 #include "kernels.h"
@@ -10,7 +10,7 @@
 namespace moe {
 namespace {
 
-constexpr int kWarps = 8;
+constexpr int kThreads = 128;
 
 template <typename T>
 struct Vec;
@@ -47,47 +47,42 @@ struct Vec<__nv_bfloat16> {
   }
 };
 
+// Block (t, cb): token t, 16-byte column vectors cb*kThreads .. +kThreads-1; each
+// thread owns one vector.  The token's k slots are read once into shared memory.
 template <typename T>
-__global__ void __launch_bounds__(kWarps * 32)
+__global__ void __launch_bounds__(kThreads)
     combine_kernel(const T* __restrict__ y_perm, const int32_t* __restrict__ slot_row,
-                   const float* __restrict__ topk_w, int64_t ntok, int d, int k, int64_t rows,
+                   const float* __restrict__ topk_w, int d, int k, int64_t rows,
                    T* __restrict__ y, int* flags) {
   constexpr int V = Vec<T>::N;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t t = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
-  if (t >= ntok) return;
-  int r[kMaxK];
-  float w[kMaxK];
+  __shared__ int s_row[kMaxK];
+  __shared__ float s_w[kMaxK];
+  const int64_t t = blockIdx.x;
+  if (threadIdx.x < k) {
+    int q = slot_row[t * k + threadIdx.x];
+    if (q < -1 || q >= rows) {
+      if (blockIdx.y == 0) raise_flag(flags, MOE_DEVERR_BAD_ROW);
+      q = -1;
+    }
+    s_row[threadIdx.x] = q;
+    s_w[threadIdx.x] = topk_w[t * k + threadIdx.x];
+  }
+  __syncthreads();
+  const int v = blockIdx.y * kThreads + threadIdx.x;
+  if (v >= d / V) return;
+  float acc[V];
+#pragma unroll
+  for (int i = 0; i < V; ++i) acc[i] = 0.f;
 #pragma unroll
   for (int j = 0; j < kMaxK; ++j) {
-    r[j] = -1;
-    w[j] = 0.f;
-    if (j < k) {
-      int q = slot_row[t * k + j];
-      if (q < -1 || q >= rows) {
-        if (lane == 0) raise_flag(flags, MOE_DEVERR_BAD_ROW);
-        q = -1;
-      }
-      r[j] = q;
-      w[j] = topk_w[t * k + j];
+    if (j < k && s_row[j] >= 0) {
+      float val[V];
+      Vec<T>::load(y_perm + static_cast<int64_t>(s_row[j]) * d + v * V, val);
+#pragma unroll
+      for (int i = 0; i < V; ++i) acc[i] = fmaf(s_w[j], val[i], acc[i]);
     }
   }
-  const int nvec = d / V;
-  for (int v = lane; v < nvec; v += 32) {
-    float acc[V];
-#pragma unroll
-    for (int i = 0; i < V; ++i) acc[i] = 0.f;
-#pragma unroll
-    for (int j = 0; j < kMaxK; ++j) {
-      if (j < k && r[j] >= 0) {
-        float val[V];
-        Vec<T>::load(y_perm + static_cast<int64_t>(r[j]) * d + v * V, val);
-#pragma unroll
-        for (int i = 0; i < V; ++i) acc[i] = fmaf(w[j], val[i], acc[i]);
-      }
-    }
-    Vec<T>::store(y + t * d + v * V, acc);
-  }
+  Vec<T>::store(y + t * d + v * V, acc);
 }
 
 }  // namespace
@@ -96,15 +91,16 @@ cudaError_t launch_combine(int dtype, const void* y_perm, const int32_t* slot_ro
                            const float* topk_w, int64_t T, int d, int k, void* y, int* flags,
                            cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
-  const unsigned grid = static_cast<unsigned>((T + kWarps - 1) / kWarps);
+  const int vec = dtype == MOE_F32 ? Vec<float>::N : Vec<__nv_bfloat16>::N;
+  const dim3 grid(static_cast<unsigned>(T), static_cast<unsigned>((d / vec + kThreads - 1) / kThreads));
   const int64_t rows = T * k;
   if (dtype == MOE_F32)
-    combine_kernel<float><<<grid, kWarps * 32, 0, stream>>>(
-        static_cast<const float*>(y_perm), slot_row, topk_w, T, d, k, rows,
-        static_cast<float*>(y), flags);
+    combine_kernel<float><<<grid, kThreads, 0, stream>>>(static_cast<const float*>(y_perm),
+                                                         slot_row, topk_w, d, k, rows,
+                                                         static_cast<float*>(y), flags);
   else
-    combine_kernel<__nv_bfloat16><<<grid, kWarps * 32, 0, stream>>>(
-        static_cast<const __nv_bfloat16*>(y_perm), slot_row, topk_w, T, d, k, rows,
+    combine_kernel<__nv_bfloat16><<<grid, kThreads, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(y_perm), slot_row, topk_w, d, k, rows,
         static_cast<__nv_bfloat16*>(y), flags);
   return cudaGetLastError();
 }

@@ -12,7 +12,11 @@
 // a per-chunk expert histogram is scanned over chunks (route.cu, finalize) to
 // give each chunk's first position per expert, and inside a chunk the position
 // of an assignment is that base plus the number of earlier assignments of the
-// chunk (in token-then-slot order) with the same expert.
+// chunk (in token-then-slot order) with the same expert.  The row copy into the
+// expert-contiguous buffer is a separate grid-stride kernel over all kept rows, so
+// that it uses the whole GPU whatever the number of chunks.
+
+#include <algorithm>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -43,15 +47,12 @@ __global__ void __launch_bounds__(kThreads)
     hist[static_cast<int64_t>(blockIdx.x) * E + e] = s_hist[e];
 }
 
-template <typename Tin>
 __global__ void __launch_bounds__(kThreads)
     dispatch_place_kernel(const int32_t* __restrict__ topk_idx, int64_t T, int E, int k, int64_t C,
                           const int32_t* __restrict__ chunk_base,
                           const int32_t* __restrict__ offsets, int32_t* __restrict__ slot_row,
-                          int32_t* __restrict__ row_token, const Tin* __restrict__ x,
-                          Tin* __restrict__ x_perm, int d, int* flags) {
+                          int32_t* __restrict__ row_token, int* flags) {
   __shared__ int s_idx[kChunk * kMaxK];
-  __shared__ int s_row[kChunk * kMaxK];
   const int c = blockIdx.x;
   const int64_t t0 = static_cast<int64_t>(c) * kChunk;
   const int ntok = static_cast<int>(T - t0 < kChunk ? T - t0 : kChunk);
@@ -71,21 +72,8 @@ __global__ void __launch_bounds__(kThreads)
     } else {
       raise_flag(flags, MOE_DEVERR_BAD_INDEX);
     }
-    s_row[a] = row;
     slot_row[base + a] = row;
     if (row >= 0) row_token[row] = static_cast<int32_t>(t0 + a / k);
-  }
-  __syncthreads();
-
-  // Row gather, one warp per kept assignment, 16-byte vectors.
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nvec = d * static_cast<int>(sizeof(Tin)) / 16;
-  for (int a = warp; a < npairs; a += kThreads / 32) {
-    const int row = s_row[a];
-    if (row < 0) continue;
-    const uint4* src = reinterpret_cast<const uint4*>(x + (t0 + a / k) * d);
-    uint4* dst = reinterpret_cast<uint4*>(x_perm + static_cast<int64_t>(row) * d);
-    for (int v = lane; v < nvec; v += 32) dst[v] = __ldg(src + v);
   }
 
   // Rows past the kept total carry no token.
@@ -93,6 +81,33 @@ __global__ void __launch_bounds__(kThreads)
   for (int64_t r = M + static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; r < T * k;
        r += static_cast<int64_t>(gridDim.x) * blockDim.x)
     row_token[r] = -1;
+}
+
+// Row gather Xp[r, :] = x[row_token[r], :] for r < M = offsets[E]: one warp per row,
+// grid-stride over rows, four independent 16-byte loads in flight per lane.
+template <typename Tin>
+__global__ void __launch_bounds__(kThreads)
+    gather_rows_kernel(const int32_t* __restrict__ row_token, const int32_t* __restrict__ offsets,
+                       int E, const Tin* __restrict__ x, Tin* __restrict__ x_perm, int d) {
+  const int64_t M = offsets[E];
+  const int nvec = d * static_cast<int>(sizeof(Tin)) / 16;
+  const int lane = threadIdx.x & 31;
+  const int64_t wpb = kThreads / 32;
+  for (int64_t r = static_cast<int64_t>(blockIdx.x) * wpb + (threadIdx.x >> 5); r < M;
+       r += static_cast<int64_t>(gridDim.x) * wpb) {
+    const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<int64_t>(row_token[r]) * d);
+    uint4* dst = reinterpret_cast<uint4*>(x_perm + r * d);
+    int v = lane;
+    for (; v + 96 < nvec; v += 128) {
+      const uint4 a = __ldg(src + v), b = __ldg(src + v + 32), c = __ldg(src + v + 64),
+                  e = __ldg(src + v + 96);
+      dst[v] = a;
+      dst[v + 32] = b;
+      dst[v + 64] = c;
+      dst[v + 96] = e;
+    }
+    for (; v < nvec; v += 32) dst[v] = __ldg(src + v);
+  }
 }
 
 }  // namespace
@@ -112,15 +127,21 @@ cudaError_t launch_dispatch_place(int dtype, const int32_t* topk_idx, int64_t T,
                                   void* x_perm, int d, int* flags, cudaStream_t stream) {
   const int64_t nchunks = (T + kChunk - 1) / kChunk;
   if (nchunks == 0) return cudaSuccess;
-  const unsigned grid = static_cast<unsigned>(nchunks);
+  dispatch_place_kernel<<<static_cast<unsigned>(nchunks), kThreads, 0, stream>>>(
+      topk_idx, T, E, k, C, chunk_base, offsets, slot_row, row_token, flags);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  // Enough warps for every possible row, capped; the kernel strides over the rest.
+  const int64_t rows = T * k;
+  const unsigned grid =
+      static_cast<unsigned>(std::min<int64_t>((rows + kThreads / 32 - 1) / (kThreads / 32), 4096));
   if (dtype == MOE_F32)
-    dispatch_place_kernel<float><<<grid, kThreads, 0, stream>>>(
-        topk_idx, T, E, k, C, chunk_base, offsets, slot_row, row_token,
-        static_cast<const float*>(x), static_cast<float*>(x_perm), d, flags);
+    gather_rows_kernel<float><<<grid, kThreads, 0, stream>>>(
+        row_token, offsets, E, static_cast<const float*>(x), static_cast<float*>(x_perm), d);
   else
-    dispatch_place_kernel<__nv_bfloat16><<<grid, kThreads, 0, stream>>>(
-        topk_idx, T, E, k, C, chunk_base, offsets, slot_row, row_token,
-        static_cast<const __nv_bfloat16*>(x), static_cast<__nv_bfloat16*>(x_perm), d, flags);
+    gather_rows_kernel<__nv_bfloat16><<<grid, kThreads, 0, stream>>>(
+        row_token, offsets, E, static_cast<const __nv_bfloat16*>(x),
+        static_cast<__nv_bfloat16*>(x_perm), d);
   return cudaGetLastError();
 }
 

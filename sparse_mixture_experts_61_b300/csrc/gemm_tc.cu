@@ -139,9 +139,10 @@ __device__ __forceinline__ int find_group(const int* pref, int G, int per, int t
 }
 
 // Warp 0, lane 0, over tiles first, first + step, ...  decode(tile) -> coordinates
-// with the stage's byte count in .bytes; load(coords, kb, smem_a, smem_b, bar).
+// with the stage's byte count in .bytes and the tile's k-blocks [.kb0, .kb1);
+// load(coords, kb, smem_a, smem_b, bar).
 template <int STAGES, class Smem, class Decode, class Load>
-__device__ __forceinline__ void run_producer(Smem& S, int first, int step, int total, int KB,
+__device__ __forceinline__ void run_producer(Smem& S, int first, int step, int total,
                                              Decode decode, Load load, volatile int* abort,
                                              int* flags) {
   int s = 0;
@@ -149,7 +150,7 @@ __device__ __forceinline__ void run_producer(Smem& S, int first, int step, int t
   bool ok = true;
   for (int tile = first; ok && tile < total; tile += step) {
     const auto c = decode(tile);
-    for (int kb = 0; kb < KB; ++kb) {
+    for (int kb = c.kb0; kb < c.kb1; ++kb) {
       if (!mbar_wait_bounded(smem_u32(&S.empty[s]), ph ^ 1u, abort, flags)) {
         ok = false;
         break;
@@ -172,24 +173,26 @@ __device__ __forceinline__ void run_producer(Smem& S, int first, int step, int t
   }
 }
 
-// Warp 1, lane 0.  idesc_of(tile) -> instruction descriptor of the tile's MMAs.
-// With CTAS = 2 each stage is released on both CTAs of the cluster.
-template <int STAGES, int ACC_COLS, int CTAS, class Smem, class Idesc>
-__device__ __forceinline__ void run_mma(Smem& S, int first, int step, int total, int KB,
-                                        uint32_t tmem_base, Idesc idesc_of, volatile int* abort,
-                                        int* flags) {
+// Warp 1, lane 0.  decode(tile) -> coordinates with the k-block range [.kb0, .kb1);
+// idesc_of(coords) -> instruction descriptor of the tile's MMAs.  With CTAS = 2 each
+// stage is released on both CTAs of the cluster.
+template <int STAGES, int ACC_COLS, int CTAS, class Smem, class Decode, class Idesc>
+__device__ __forceinline__ void run_mma(Smem& S, int first, int step, int total,
+                                        uint32_t tmem_base, Decode decode, Idesc idesc_of,
+                                        volatile int* abort, int* flags) {
   int s = 0, acc = 0;
   uint32_t ph = 0, aph = 0;
   bool ok = true, issued_any = false;
   for (int tile = first; ok && tile < total; tile += step) {
-    const uint32_t idesc = idesc_of(tile);
+    const auto c = decode(tile);
+    const uint32_t idesc = idesc_of(c);
     if (!mbar_wait_bounded(smem_u32(&S.tempty[acc]), aph ^ 1u, abort, flags)) {
       ok = false;
       break;
     }
     tc_fence_after();
     const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * ACC_COLS);
-    for (int kb = 0; kb < KB; ++kb) {
+    for (int kb = c.kb0; kb < c.kb1; ++kb) {
       if (!mbar_wait_bounded(smem_u32(&S.full[s]), ph, abort, flags)) {
         ok = false;
         break;
@@ -199,7 +202,7 @@ __device__ __forceinline__ void run_mma(Smem& S, int first, int step, int total,
 #pragma unroll
       for (int kk = 0; kk < TC_BK / 16; ++kk)
         tc_mma_bf16(d_tmem, sw128_kmajor_desc(a0 + kk * 32), sw128_kmajor_desc(b0 + kk * 32),
-                    idesc, (kb | kk) != 0 ? 1u : 0u);
+                    idesc, (kb != c.kb0 || kk != 0) ? 1u : 0u);
       issued_any = true;
       if (CTAS > 1)
         tc_commit_multicast(smem_u32(&S.empty[s]), static_cast<uint16_t>((1u << CTAS) - 1u));
@@ -279,7 +282,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
   volatile int* abort = &S.abort;
 
   struct Coord {
-    int g, n0, ntok, nbox;
+    int g, n0, ntok, nbox, kb0, kb1;
     uint32_t bytes;
     int64_t row0, row_end;
   };
@@ -296,13 +299,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
     c.ntok = static_cast<int>((c.row_end - c.row0 + 15) & ~int64_t{15});
     c.nbox = (c.ntok + TOK_BOX - 1) / TOK_BOX;
     c.bytes = kWeightBytes + static_cast<uint32_t>(c.nbox) * kBoxBytes;
+    c.kb0 = 0;
+    c.kb1 = KB;
     return c;
   };
 
   if (warp == 0) {
     if (lane == 0)
       run_producer<STAGES>(
-          S, first, step, total, KB, decode,
+          S, first, step, total, decode,
           [&](const Coord& c, int kb, uint32_t sa, uint32_t sb, uint32_t bar) {
             tma_load_3d(sa, &tmW, bar, kb * TC_BK, c.n0, c.g);
             for (int j = rank; j < c.nbox; j += CTAS)
@@ -313,8 +318,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
   } else if (warp == 1) {
     if (lane == 0)
       run_mma<STAGES, TB, CTAS>(
-          S, first, step, total, KB, S.tmem_base,
-          [&](int tile) { return bf16_idesc(TILE_M, decode(tile).ntok); }, abort, p.flags);
+          S, first, step, total, S.tmem_base, decode,
+          [](const Coord& c) { return bf16_idesc(TILE_M, c.ntok); }, abort, p.flags);
   } else {
     const int quad = warp & 3;  // TMEM lanes this warp may read: 32*quad .. 32*quad+31
     int acc = 0;
@@ -387,7 +392,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   volatile int* abort = &S.abort;
 
   struct Coord {
-    int g, n0;
+    int g, n0, kb0, kb1;
     uint32_t bytes;
     int64_t row0, row_end;
   };
@@ -400,13 +405,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     c.row0 = p.offsets[c.g] + static_cast<int64_t>(local % mt) * TILE_M;
     c.row_end = p.offsets[c.g + 1];
     c.bytes = kStageBytes;
+    c.kb0 = 0;
+    c.kb1 = KB;
     return c;
   };
 
   if (warp == 0) {
     if (lane == 0)
       run_producer<STAGES>(
-          S, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), total, KB, decode,
+          S, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), total, decode,
           [&](const Coord& c, int kb, uint32_t sa, uint32_t sb, uint32_t bar) {
             tma_load_2d(sa, &tmX, bar, kb * TC_BK, static_cast<int>(c.row0));
             tma_load_3d(sb, &tmW, bar, kb * TC_BK, c.n0, c.g);
@@ -415,7 +422,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   } else if (warp == 1) {
     if (lane == 0)
       run_mma<STAGES, BN, 1>(S, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), total,
-                             KB, S.tmem_base, [](int) { return kIdesc; }, abort, p.flags);
+                             S.tmem_base, decode, [](const Coord&) { return kIdesc; }, abort,
+                             p.flags);
   } else {
     const int quad = warp & 3;  // TMEM lanes this warp may read: 32*quad .. 32*quad+31
     const __nv_bfloat16* bias_base = static_cast<const __nv_bfloat16*>(p.bias);
@@ -492,7 +500,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 
 // ------------------------------------------------------------- router GEMM
 // A = token block [128 x 64] of x; B = expert block [BN x 64] of W_g; D[128 x BN],
-// lane = token, column = expert; fp32 output plus the fp32 logit bias.
+// lane = token, column = expert.  When there are too few tiles to fill the GPU the
+// K dimension is split across CTAs: split s writes its partial sums to
+// out + s * split_stride, and the softmax/top-k kernel adds the splits in order and
+// the logit bias (so every logit is one fixed-order fp32 sum).
 template <int BN, int STAGES>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     tc_router_kernel(const __grid_constant__ CUtensorMap tmX,
@@ -508,28 +519,34 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   pipe_prologue<Smem, STAGES, 1>(S, kTmemCols, p, 1, TILE_M, &tmX, &tmW);
 
   const int NB = (p.N + BN - 1) / BN;
-  const int total = S.pref[1] * NB;
+  const int MT = S.pref[1];
   const int KB = (p.K + TC_BK - 1) / TC_BK;
+  const int splits = p.ksplit > 1 ? p.ksplit : 1;
+  const int kb_per = (KB + splits - 1) / splits;
+  const int total = MT * NB * splits;
   volatile int* abort = &S.abort;
 
   struct Coord {
-    int n0;
+    int n0, split, kb0, kb1;
     uint32_t bytes;
     int64_t row0;
   };
   auto decode = [&](int tile) {
     Coord c;
     c.bytes = kStageBytes;
-    const int mt = S.pref[1];
-    c.n0 = (tile / mt) * BN;
-    c.row0 = static_cast<int64_t>(tile % mt) * TILE_M;
+    c.split = tile / (MT * NB);
+    const int rem = tile % (MT * NB);
+    c.n0 = (rem / MT) * BN;
+    c.row0 = static_cast<int64_t>(rem % MT) * TILE_M;
+    c.kb0 = c.split * kb_per;
+    c.kb1 = c.kb0 + kb_per < KB ? c.kb0 + kb_per : KB;
     return c;
   };
 
   if (warp == 0) {
     if (lane == 0)
       run_producer<STAGES>(
-          S, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), total, KB, decode,
+          S, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), total, decode,
           [&](const Coord& c, int kb, uint32_t sa, uint32_t sb, uint32_t bar) {
             tma_load_2d(sa, &tmX, bar, kb * TC_BK, static_cast<int>(c.row0));
             tma_load_3d(sb, &tmW, bar, kb * TC_BK, c.n0, 0);
@@ -538,15 +555,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   } else if (warp == 1) {
     if (lane == 0)
       run_mma<STAGES, BN, 1>(S, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), total,
-                             KB, S.tmem_base, [](int) { return kIdesc; }, abort, p.flags);
+                             S.tmem_base, decode, [](const Coord&) { return kIdesc; }, abort,
+                             p.flags);
   } else {
     const int quad = warp & 3;
     int acc = 0;
     uint32_t aph = 0;
-    float* out = static_cast<float*>(p.out);
-    const float* bias = static_cast<const float*>(p.bias);
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
       const Coord c = decode(tile);
+      float* out = static_cast<float*>(p.out) + static_cast<int64_t>(c.split) * p.split_stride;
       const bool got = mbar_wait_bounded(smem_u32(&S.tfull[acc]), aph, abort, p.flags);
       if (!__all_sync(0xffffffffu, got)) break;
       tc_fence_after();
@@ -565,7 +582,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 #pragma unroll
           for (int i = 0; i < CH; ++i) {
             const int e = c.n0 + col + i;
-            if (e < p.N) out[row * p.N + e] = v[i] + (bias ? bias[e] : 0.f);
+            if (e < p.N) out[row * p.N + e] = v[i];
           }
         }
       }
@@ -694,7 +711,8 @@ cudaError_t launch_router(const GemmArgs& a, int sm_count, cudaStream_t stream) 
   CUtensorMap tmX, tmW;
   if (!rows_map(&tmX, a.A, a.m_rows, a.K, TILE_M) || !stacked_map(&tmW, a.B, 1, a.N, a.K, BN))
     return cudaErrorInvalidValue;
-  const int64_t bound = ((a.m_rows + TILE_M - 1) / TILE_M) * ((a.N + BN - 1) / BN);
+  const int64_t bound = ((a.m_rows + TILE_M - 1) / TILE_M) * ((a.N + BN - 1) / BN) *
+                        (a.ksplit > 1 ? a.ksplit : 1);
   const int grid = static_cast<int>(std::min<int64_t>(bound, sm_count));
   using Smem = PipeSmem<TILE_M * TC_BK * 2, BN * TC_BK * 2, STAGES>;
   return launch_pipe(tc_router_kernel<BN, STAGES>, sizeof(Smem) + 1024, grid, tmX, tmW, a, stream);
@@ -715,7 +733,21 @@ cudaError_t launch_ffn_for(const GemmArgs& a, int max_group, int sm_count, cudaS
 // the MMA's M side.  Larger groups use row tiles, whose main loop measured faster.
 constexpr int kSmallGroup = 128;
 
+// Router tile width for E experts: the narrowest power of two that covers them, at
+// most 128.
+int router_bn(int E) { return E <= 16 ? 16 : E <= 32 ? 32 : E <= 64 ? 64 : 128; }
+
 }  // namespace
+
+int router_splits(int64_t T, int E, int d, int sms) {
+  const int64_t tiles = ((T + TILE_M - 1) / TILE_M) * ((E + router_bn(E) - 1) / router_bn(E));
+  const int64_t kb = (d + TC_BK - 1) / TC_BK;
+  const int64_t by_fill = tiles > 0 ? sms / tiles : 1;
+  const int64_t s = std::max<int64_t>(1, std::min<int64_t>(by_fill, kb / 4));
+  // The same number of k-blocks per split as the kernel uses; no empty split.
+  const int64_t per = (kb + s - 1) / s;
+  return static_cast<int>((kb + per - 1) / per);
+}
 
 cudaError_t launch_tc_gemm_bf16(const GemmArgs& a, int epi, int sm_count, cudaStream_t stream) {
   switch (epi) {
@@ -726,11 +758,12 @@ cudaError_t launch_tc_gemm_bf16(const GemmArgs& a, int epi, int sm_count, cudaSt
       return a.max_group > kSmallGroup ? launch_rows_ffn<256, 4, EPI_BIAS>(a, sm_count, stream)
                                        : launch_ffn_for<EPI_BIAS>(a, a.max_group, sm_count, stream);
     default:
-      // Router: N = E columns; the narrowest power-of-two tile that covers them, at most 128.
-      if (a.N <= 16) return launch_router<16, 8>(a, sm_count, stream);
-      if (a.N <= 32) return launch_router<32, 8>(a, sm_count, stream);
-      if (a.N <= 64) return launch_router<64, 8>(a, sm_count, stream);
-      return launch_router<128, 6>(a, sm_count, stream);
+      switch (router_bn(a.N)) {
+        case 16: return launch_router<16, 8>(a, sm_count, stream);
+        case 32: return launch_router<32, 8>(a, sm_count, stream);
+        case 64: return launch_router<64, 8>(a, sm_count, stream);
+        default: return launch_router<128, 6>(a, sm_count, stream);
+      }
   }
 }
 

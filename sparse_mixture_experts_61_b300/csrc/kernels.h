@@ -8,10 +8,13 @@
 namespace moe {
 
 // R2 + R3: softmax, top-k, gate weights, per-chunk expert histogram and per-chunk
-// softmax column sums over fp32 logits [T,E].
-cudaError_t launch_route_topk(const float* logits, int64_t T, int E, int k, int gate,
-                              int32_t* topk_idx, float* topk_w, int32_t* hist, float* psum,
-                              int* flags, cudaStream_t stream);
+// softmax column sums.  The logits of token t are
+//   l[t,e] = sum_{s < nsplit} src[s * split_stride + t*E + e]  (+ bias[e] if bias)
+// added in that order; when logits_out is given they are written there.
+cudaError_t launch_route_topk(const float* src, int nsplit, int64_t split_stride,
+                              const float* bias, float* logits_out, int64_t T, int E, int k,
+                              int gate, int32_t* topk_idx, float* topk_w, int32_t* hist,
+                              float* psum, int* flags, cudaStream_t stream);
 
 // R4 + D1: reduces the per-chunk histograms (and, when psum != nullptr, the softmax
 // sums into the balance loss), then applies the capacity and scans the offsets.
@@ -49,8 +52,17 @@ struct GemmArgs {
   int64_t m_rows;         // rows when offsets == nullptr
   int G, N, K;
   int max_group;          // upper bound on any group's rows (sizes the token tile)
+  int ksplit;             // router: K splits; split s writes out + s * split_stride
+  int64_t split_stride;
   int* flags;
 };
+
+// K splits of the bf16 router contraction for T tokens, E experts, model width d on a
+// GPU with `sms` SMs: enough (tile, split) work units to fill the GPU, at least four
+// 64-deep k-blocks per split.  Depends only on its arguments, so the workspace size
+// can bound it with an upper limit on the SM count.
+int router_splits(int64_t T, int E, int d, int sms);
+constexpr int kMaxSmsForSizing = 160;
 
 enum Epilogue { EPI_BIAS_SILU = 0, EPI_BIAS = 1, EPI_ROUTER_F32 = 2 };
 

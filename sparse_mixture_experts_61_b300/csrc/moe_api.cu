@@ -21,7 +21,9 @@ constexpr size_t kAlign = 256;
 size_t align_up(size_t v) { return (v + kAlign - 1) & ~(kAlign - 1); }
 
 // Workspace layout: [flags | per-chunk hist | chunk bases | per-chunk softmax sums |
-// logits] = the stage workspace, then the forward-only intermediates.
+// router output] = the stage workspace, then the forward-only intermediates.  The
+// router output region holds the [T,E] fp32 logits (fp32 layers) or the K-split
+// partial sums of the bf16 router GEMM.
 struct Layout {
   size_t flags, hist, chunk_base, psum, logits, stage_end;
   size_t idx, w, counts, aux, offsets, kept, slot_row, row_token, dropped, x_perm, h_buf, y_perm;
@@ -39,7 +41,9 @@ Layout make_layout(const moe_config& c) {
   L.hist = o; o = align_up(o + L.nchunks * E * 4);
   L.chunk_base = o; o = align_up(o + L.nchunks * E * 4);
   L.psum = o; o = align_up(o + L.nchunks * E * 4);
-  L.logits = o; o = align_up(o + T * E * 4);
+  const int64_t splits =
+      c.dtype == MOE_BF16 ? router_splits(c.T, c.E, c.d, kMaxSmsForSizing) : 1;
+  L.logits = o; o = align_up(o + splits * T * E * 4);
   L.stage_end = o;
   L.idx = o; o = align_up(o + T * k * 4);
   L.w = o; o = align_up(o + T * k * 4);
@@ -112,24 +116,43 @@ T* at(void* ws, size_t off) {
     if ((call) != cudaSuccess) return MOE_ERR_CUDA; \
   } while (0)
 
-// R1: logits[T,E] (fp32) = x . W_g^T + logit_bias.
-moe_status run_router_logits(const moe_config& c, const void* x, const void* w_gate,
-                             const float* logit_bias, float* logits, int* flags, int sms,
-                             cudaStream_t st) {
+// R1 + R2 + R3: the router contraction, then softmax / top-k / weights / per-chunk
+// histogram and softmax sums.  fp32 layers: a SIMT GEMM writes the biased logits
+// (into `logits`, or the workspace).  bf16 layers: the tensor-core GEMM writes
+// K-split partial sums into the workspace; the top-k kernel adds them and the logit
+// bias and writes the logits to `logits` when given.
+moe_status run_router(const moe_config& c, const Layout& L, void* ws, const void* x,
+                      const void* w_gate, const float* logit_bias, float* logits,
+                      int32_t* topk_idx, float* topk_w, int* flags, int sms, cudaStream_t st) {
   GemmArgs g{};
   g.A = x;
   g.rows_alloc = c.T;
   g.B = w_gate;
-  g.bias = logit_bias;
-  g.out = logits;
   g.offsets = nullptr;
   g.m_rows = c.T;
   g.G = 1;
   g.N = c.E;
   g.K = c.d;
   g.flags = flags;
-  MOE_CUDA(c.dtype == MOE_F32 ? launch_simt_gemm_f32(g, EPI_ROUTER_F32, sms, st)
-                              : launch_tc_gemm_bf16(g, EPI_ROUTER_F32, sms, st));
+  float* region = at<float>(ws, L.logits);
+  int32_t* hist = at<int32_t>(ws, L.hist);
+  float* psum = at<float>(ws, L.psum);
+  if (c.dtype == MOE_F32) {
+    float* lg = logits ? logits : region;
+    g.bias = logit_bias;
+    g.out = lg;
+    MOE_CUDA(launch_simt_gemm_f32(g, EPI_ROUTER_F32, sms, st));
+    MOE_CUDA(launch_route_topk(lg, 1, 0, nullptr, nullptr, c.T, c.E, c.k, c.gate, topk_idx,
+                               topk_w, hist, psum, flags, st));
+  } else {
+    g.bias = nullptr;
+    g.out = region;
+    g.ksplit = router_splits(c.T, c.E, c.d, sms < kMaxSmsForSizing ? sms : kMaxSmsForSizing);
+    g.split_stride = c.T * c.E;
+    MOE_CUDA(launch_tc_gemm_bf16(g, EPI_ROUTER_F32, sms, st));
+    MOE_CUDA(launch_route_topk(region, g.ksplit, g.split_stride, logit_bias, logits, c.T, c.E,
+                               c.k, c.gate, topk_idx, topk_w, hist, psum, flags, st));
+  }
   return MOE_OK;
 }
 
@@ -236,10 +259,9 @@ MOE_EXPORT moe_status moe_route(const moe_config* cfg, const void* x, const void
   }
   const int sms = sm_count();
   if (sms <= 0) return MOE_ERR_CUDA;
-  float* lg = logits ? logits : at<float>(ws, L.logits);
-  if ((s = run_router_logits(c, x, w_gate, logit_bias, lg, flags, sms, st)) != MOE_OK) return s;
-  MOE_CUDA(launch_route_topk(lg, c.T, c.E, c.k, c.gate, topk_idx, topk_w, at<int32_t>(ws, L.hist),
-                             at<float>(ws, L.psum), flags, st));
+  if ((s = run_router(c, L, ws, x, w_gate, logit_bias, logits, topk_idx, topk_w, flags, sms,
+                      st)) != MOE_OK)
+    return s;
   if (counts || aux_loss)
     MOE_CUDA(launch_route_finalize(at<int32_t>(ws, L.hist), at<float>(ws, L.psum),
                                    static_cast<int>(L.nchunks), c.E, c.T, -1, counts, aux_loss,
@@ -334,7 +356,6 @@ MOE_EXPORT moe_status moe_forward(const moe_config* cfg, const moe_forward_args*
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   int* flags = at<int>(ws, L.flags);
   MOE_CUDA(cudaMemsetAsync(flags, 0, sizeof(int), st));
-  float* logits = a->logits ? a->logits : at<float>(ws, L.logits);
   int32_t* idx = a->topk_idx ? a->topk_idx : at<int32_t>(ws, L.idx);
   float* w = a->topk_w ? a->topk_w : at<float>(ws, L.w);
   int32_t* counts = a->counts ? a->counts : at<int32_t>(ws, L.counts);
@@ -361,9 +382,9 @@ MOE_EXPORT moe_status moe_forward(const moe_config* cfg, const moe_forward_args*
   void* y_perm = at<void>(ws, L.y_perm);
   const int64_t C = capacity_of(c);
 
-  if ((s = run_router_logits(c, a->x, a->w_gate, a->logit_bias, logits, flags, sms, st)) != MOE_OK)
+  if ((s = run_router(c, L, ws, a->x, a->w_gate, a->logit_bias, a->logits, idx, w, flags, sms,
+                      st)) != MOE_OK)
     return s;
-  MOE_CUDA(launch_route_topk(logits, c.T, c.E, c.k, c.gate, idx, w, hist, psum, flags, st));
   MOE_CUDA(launch_route_finalize(hist, psum, static_cast<int>(L.nchunks), c.E, c.T, C, counts, aux,
                                  chunk_base, kept, offsets, dropped, st));
   MOE_CUDA(launch_dispatch_place(c.dtype, idx, c.T, c.E, c.k, C, chunk_base, offsets, slot_row,

@@ -22,16 +22,18 @@
 namespace moe {
 namespace {
 
-constexpr int kRouteWarps = 8;
+constexpr int kRouteWarps = 32;
 constexpr int kTokensPerWarp = kChunk / kRouteWarps;
 
 // One CTA per chunk of kChunk tokens, one warp per token at a time.  Lane l holds
 // experts l, l+32, ... (EPL of them).
 template <int EPL>
 __global__ void __launch_bounds__(kRouteWarps * 32)
-    route_topk_kernel(const float* __restrict__ logits, int64_t T, int E, int k, int gate,
-                      int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
-                      int32_t* __restrict__ hist, float* __restrict__ psum, int* flags) {
+    route_topk_kernel(const float* __restrict__ src, int nsplit, int64_t split_stride,
+                      const float* __restrict__ bias, float* __restrict__ logits_out, int64_t T,
+                      int E, int k, int gate, int32_t* __restrict__ topk_idx,
+                      float* __restrict__ topk_w, int32_t* __restrict__ hist,
+                      float* __restrict__ psum, int* flags) {
   __shared__ int s_hist[kMaxExperts];
   __shared__ float s_ps[kRouteWarps][kMaxExperts];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -46,14 +48,20 @@ __global__ void __launch_bounds__(kRouteWarps * 32)
   for (int i = 0; i < kTokensPerWarp; ++i) {
     const int64_t t = t_first + i;
     if (t >= T) break;  // warp-uniform
-    const float* lrow = logits + t * E;
     float v[EPL];
     bool bad = false;
 #pragma unroll
     for (int q = 0; q < EPL; ++q) {
       const int e = lane + 32 * q;
-      v[q] = e < E ? lrow[e] : -INFINITY;
-      if (e < E && !isfinite(v[q])) bad = true;
+      v[q] = -INFINITY;
+      if (e < E) {
+        float l = src[t * E + e];
+        for (int sp = 1; sp < nsplit; ++sp) l += src[sp * split_stride + t * E + e];
+        if (bias) l += bias[e];
+        if (logits_out) logits_out[t * E + e] = l;
+        v[q] = l;
+        if (!isfinite(l)) bad = true;
+      }
     }
     if (__any_sync(0xffffffffu, bad) && lane == 0) raise_flag(flags, MOE_DEVERR_NONFINITE);
 
@@ -153,9 +161,10 @@ __global__ void __launch_bounds__(kRouteWarps * 32)
 // Single CTA of 256 threads; thread e owns expert e.
 __global__ void __launch_bounds__(kMaxExperts)
     route_finalize_kernel(const int32_t* __restrict__ hist, const float* __restrict__ psum,
-                          int nchunks, int E, int64_t T, int64_t C, int32_t* counts, float* aux,
-                          int32_t* chunk_base, int32_t* kept, int32_t* offsets,
-                          int32_t* dropped) {
+                          int nchunks, int E, int64_t T, int64_t C, int32_t* __restrict__ counts,
+                          float* __restrict__ aux, int32_t* __restrict__ chunk_base,
+                          int32_t* __restrict__ kept, int32_t* __restrict__ offsets,
+                          int32_t* __restrict__ dropped) {
   __shared__ double s_red[kMaxExperts];
   __shared__ int s_scan[kMaxExperts];
   __shared__ int s_drop;
@@ -164,10 +173,26 @@ __global__ void __launch_bounds__(kMaxExperts)
   int cnt = 0;
   double ps = 0.0;
   if (e < E) {
-    for (int c = 0; c < nchunks; ++c) {
-      if (chunk_base) chunk_base[static_cast<int64_t>(c) * E + e] = cnt;
-      cnt += hist[static_cast<int64_t>(c) * E + e];
-      if (psum) ps += static_cast<double>(psum[static_cast<int64_t>(c) * E + e]);
+    // Eight chunks at a time: the loads are issued together, then added in order.
+    constexpr int B = 8;
+    for (int c0 = 0; c0 < nchunks; c0 += B) {
+      int hv[B];
+      float pv[B];
+#pragma unroll
+      for (int i = 0; i < B; ++i) {
+        const int c = c0 + i;
+        hv[i] = c < nchunks ? hist[static_cast<int64_t>(c) * E + e] : 0;
+        pv[i] = (psum && c < nchunks) ? psum[static_cast<int64_t>(c) * E + e] : 0.f;
+      }
+#pragma unroll
+      for (int i = 0; i < B; ++i) {
+        const int c = c0 + i;
+        if (c < nchunks) {
+          if (chunk_base) chunk_base[static_cast<int64_t>(c) * E + e] = cnt;
+          cnt += hv[i];
+          ps += static_cast<double>(pv[i]);
+        }
+      }
     }
     if (counts) counts[e] = cnt;
   }
@@ -204,24 +229,26 @@ __global__ void __launch_bounds__(kMaxExperts)
 
 }  // namespace
 
-cudaError_t launch_route_topk(const float* logits, int64_t T, int E, int k, int gate,
-                              int32_t* topk_idx, float* topk_w, int32_t* hist, float* psum,
-                              int* flags, cudaStream_t stream) {
+cudaError_t launch_route_topk(const float* src, int nsplit, int64_t split_stride,
+                              const float* bias, float* logits_out, int64_t T, int E, int k,
+                              int gate, int32_t* topk_idx, float* topk_w, int32_t* hist,
+                              float* psum, int* flags, cudaStream_t stream) {
   const int64_t nchunks = (T + kChunk - 1) / kChunk;
   if (nchunks == 0) return cudaSuccess;
   const dim3 grid(static_cast<unsigned>(nchunks)), block(kRouteWarps * 32);
+#define MOE_TOPK_LAUNCH(EPL)                                                                  \
+  route_topk_kernel<EPL><<<grid, block, 0, stream>>>(src, nsplit, split_stride, bias, logits_out, \
+                                                     T, E, k, gate, topk_idx, topk_w, hist, psum, \
+                                                     flags)
   if (E <= 32)
-    route_topk_kernel<1><<<grid, block, 0, stream>>>(logits, T, E, k, gate, topk_idx, topk_w, hist,
-                                                     psum, flags);
+    MOE_TOPK_LAUNCH(1);
   else if (E <= 64)
-    route_topk_kernel<2><<<grid, block, 0, stream>>>(logits, T, E, k, gate, topk_idx, topk_w, hist,
-                                                     psum, flags);
+    MOE_TOPK_LAUNCH(2);
   else if (E <= 128)
-    route_topk_kernel<4><<<grid, block, 0, stream>>>(logits, T, E, k, gate, topk_idx, topk_w, hist,
-                                                     psum, flags);
+    MOE_TOPK_LAUNCH(4);
   else
-    route_topk_kernel<8><<<grid, block, 0, stream>>>(logits, T, E, k, gate, topk_idx, topk_w, hist,
-                                                     psum, flags);
+    MOE_TOPK_LAUNCH(8);
+#undef MOE_TOPK_LAUNCH
   return cudaGetLastError();
 }
 
