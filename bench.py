@@ -49,9 +49,10 @@ DEFAULT_WORKLOAD = "mixtral_prefill"
 L2_FLUSH_BYTES = 256 << 20
 KERNELS_PER_FORWARD = 7   # router GEMM, softmax/top-k, finalize/scan, place/gather, GEMM1, GEMM2, combine
 
-# dram__bytes_read.sum + dram__bytes_write.sum per launch of the grouped GEMM pair, from
-# the ncu capture summarised in profiles/ (None until a capture of the current kernel).
-NCU_TRAFFIC_BYTES = {}
+# dram__bytes_read.sum + dram__bytes_write.sum per launch of the grouped GEMM pair
+# (G1 + G2), from the ncu capture summarised in profiles/traffic_ffn_mixtral_prefill.md.
+# Only workloads whose current kernels were captured appear here; others report null.
+NCU_TRAFFIC_BYTES = {"mixtral_prefill": 1010024704 + 213667328 + 1434962176 + 60748032}
 
 
 def load_peaks():
