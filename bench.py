@@ -47,7 +47,7 @@ METRIC = "MoE-layer fwd tokens/s at 1 B300; grouped-GEMM % BF16 peak; decode % H
 UNIT = "tokens/s"
 DEFAULT_WORKLOAD = "mixtral_prefill"
 L2_FLUSH_BYTES = 256 << 20
-KERNELS_PER_FORWARD = 7   # router GEMM, softmax/top-k, finalize/scan, place/gather, GEMM1, GEMM2, combine
+KERNELS_PER_FORWARD = 8   # router GEMM, softmax/top-k, finalize/scan, place, gather, GEMM1, GEMM2, combine
 
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the grouped GEMM pair
 # (G1 + G2), from the ncu capture summarised in profiles/traffic_ffn_mixtral_prefill.md.

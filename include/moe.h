@@ -75,6 +75,24 @@ typedef enum {
   MOE_GATE_SOFTMAX_TOPK_RENORM = 1
 } moe_gate;
 
+/* Routing statistics of the pre-drop per-expert counts, in this order (load_e =
+   count_e / sum(count); sample standard deviations, divisor E-1, 0 when E = 1):
+   cv = std(load)/mean(load); dead_ratio = share of experts with load < 1e-4;
+   max_over_avg = max(load)/mean(load); entropy = -sum load ln(load + 1e-10);
+   effective_experts = exp(entropy); count_cv_loss = std(count)/(mean(count) + 1e-6).
+   From the monitoring script of "LLM MoE guide" (walkerchi.com) section 4.1 and the
+   router load loss of the sparse-inference article (lpnh.cn) sections 2.3 and 3.2.
+   All zero when there are no assignments. */
+#define MOE_ROUTING_STATS 6
+enum {
+  MOE_STAT_CV = 0,
+  MOE_STAT_DEAD_RATIO = 1,
+  MOE_STAT_MAX_OVER_AVG = 2,
+  MOE_STAT_ENTROPY = 3,
+  MOE_STAT_EFFECTIVE_EXPERTS = 4,
+  MOE_STAT_COUNT_CV_LOSS = 5
+};
+
 /* Bits of the device flag word (moe_device_error). */
 enum {
   MOE_DEVERR_BAD_INDEX = 1, /* an expert index outside [0,E) reached dispatch; that slot was dropped */
@@ -116,6 +134,7 @@ typedef struct moe_forward_args {
   int32_t* slot_row;        /* [T,k], or NULL */
   int32_t* row_token;       /* [T*k], or NULL */
   int32_t* dropped;         /* [1], or NULL */
+  float* routing_stats;     /* [MOE_ROUTING_STATS] fp32, or NULL (see moe_route) */
 } moe_forward_args;
 
 /* Human-readable name of a status code.  Never NULL. */
@@ -141,12 +160,13 @@ moe_status moe_stage_workspace_size(const moe_config* cfg, size_t* bytes);
    topk_w[t,j]  : gate weight of that expert by cfg->gate
    counts[e]    : number of (t,j) with topk_idx[t,j] == e (before any capacity drop)
    aux_loss[0]  : E * sum_e f_e P_e, f_e = mean_t softmax(logits)[t,e], P_e = counts[e]/T
-   logits may be NULL (kept in the workspace).  Selection and weights are
-   computed from exactly the fp32 logits written.  Results are deterministic. */
+   routing_stats: the MOE_ROUTING_STATS statistics of counts (above)
+   logits, counts, aux_loss and routing_stats may be NULL.  Selection and weights
+   are computed from exactly the fp32 logits written.  Results are deterministic. */
 moe_status moe_route(const moe_config* cfg, const void* x, const void* w_gate,
                      const float* logit_bias, float* logits, int32_t* topk_idx, float* topk_w,
-                     int32_t* counts, float* aux_loss, void* ws, size_t ws_bytes,
-                     moe_stream_t stream);
+                     int32_t* counts, float* aux_loss, float* routing_stats, void* ws,
+                     size_t ws_bytes, moe_stream_t stream);
 
 /* Dispatch (capacity section; grouping by expert id of "Breaking the MoE
    trilemma" 3.3).  Visiting assignments token by token, slot by slot, expert e
@@ -191,6 +211,16 @@ moe_status moe_forward(const moe_config* cfg, const moe_forward_args* args, void
    *flags (may be NULL).  Returns MOE_ERR_DEVICE when any bit is set, MOE_OK
    otherwise, MOE_ERR_CUDA if the wait or the read failed. */
 moe_status moe_device_error(const void* ws, moe_stream_t stream, int32_t* flags);
+
+/* Diagnostic of the bounded waits.  Every mbarrier wait in the GEMM pipelines gives
+   up after a time limit instead of spinning forever: it sets MOE_DEVERR_TIMEOUT, lets
+   the CTA's own copies and MMAs land, frees tensor memory and returns.  This call runs
+   that same wait routine on a barrier phase nothing completes, for limit_ns
+   nanoseconds (1 .. 2e9), in one small kernel on `stream`; afterwards *device_flags (a
+   [1] int32 device buffer, cleared first) holds MOE_DEVERR_TIMEOUT and the GPU context
+   is unaffected.  The pages have no counterpart. */
+moe_status moe_selftest_wait_timeout(int32_t* device_flags, uint64_t limit_ns,
+                                     moe_stream_t stream);
 
 /* Table cells (ceil(T/64) * E) that moe_dispatch_static's library-held scratch holds:
    2 MiB of device memory in every GPU that loads the library. */

@@ -39,6 +39,7 @@ def lib():
         L.orc_gate_weights.argtypes = [_I64, _I, _I, _I, _P, _P, _P]
         L.orc_aux_loss.argtypes = [_I64, _I, _I, _P, _P, _P, _P, _P]
         L.orc_aux_loss.restype = _D
+        L.orc_routing_stats.argtypes = [_I, _P, _P]
         L.orc_capacity.argtypes = [_I64, _I, _D]
         L.orc_capacity.restype = _I64
         L.orc_dispatch.argtypes = [_I64, _I, _I, _I64, _P, _P, _P, _P, _P, _P]
@@ -153,6 +154,18 @@ def aux_loss(p, idx):
     P = np.empty(E, np.float64)
     loss = lib().orc_aux_loss(T, E, k, _ptr(p), _ptr(idx), _ptr(counts), _ptr(f), _ptr(P))
     return loss, counts, f, P
+
+
+ROUTING_STATS = ("cv", "dead_ratio", "max_over_avg", "entropy", "effective_experts",
+                 "count_cv_loss")
+
+
+def routing_stats(counts):
+    """O4s: the six routing statistics of per-expert counts (order: ROUTING_STATS)."""
+    counts = np.ascontiguousarray(counts, np.int64)
+    out = np.empty(6, np.float64)
+    lib().orc_routing_stats(int(counts.shape[0]), _ptr(counts), _ptr(out))
+    return out
 
 
 def capacity(T, E, capacity_factor):

@@ -170,6 +170,49 @@ double orc_aux_loss(int64_t T, int E, int k, const double* p, const int32_t* idx
   return (double)E * loss;
 }
 
+// O4s. Routing statistics of the per-expert assignment counts (before any drop),
+// from the monitoring script of "LLM MoE guide" section 4.1 and the load loss of
+// the sparse-inference article's router (sections 2.3 / 3.2).  With load_e =
+// count_e / sum(count), mean = sum(load)/E and the sample standard deviation
+// (divisor E - 1, the default of the std the pages call; 0 when E = 1):
+//   stats[0] cv                = std(load) / mean(load)
+//   stats[1] dead_ratio        = #{e : load_e < 1e-4} / E
+//   stats[2] max_over_avg      = max(load) / mean(load)
+//   stats[3] entropy           = -sum_e load_e * ln(load_e + 1e-10)
+//   stats[4] effective_experts = exp(entropy)
+//   stats[5] count_cv_loss     = std(count) / (mean(count) + 1e-6)
+// With no assignments at all every statistic is 0.
+void orc_routing_stats(int E, const int64_t* counts, double* stats) {
+  double total = 0.0;
+  for (int e = 0; e < E; ++e) total += (double)counts[e];
+  for (int i = 0; i < 6; ++i) stats[i] = 0.0;
+  if (total <= 0.0) return;
+  std::vector<double> load(E);
+  for (int e = 0; e < E; ++e) load[e] = (double)counts[e] / total;
+  double lsum = 0.0, csum = 0.0;
+  for (int e = 0; e < E; ++e) {
+    lsum += load[e];
+    csum += (double)counts[e];
+  }
+  const double lmean = lsum / E, cmean = csum / E;
+  double lvar = 0.0, cvar = 0.0, lmax = load[0], dead = 0.0, ent = 0.0;
+  for (int e = 0; e < E; ++e) {
+    lvar += (load[e] - lmean) * (load[e] - lmean);
+    cvar += ((double)counts[e] - cmean) * ((double)counts[e] - cmean);
+    if (load[e] > lmax) lmax = load[e];
+    if (load[e] < 1e-4) dead += 1.0;
+    ent -= load[e] * std::log(load[e] + 1e-10);
+  }
+  const double lstd = E > 1 ? std::sqrt(lvar / (E - 1)) : 0.0;
+  const double cstd = E > 1 ? std::sqrt(cvar / (E - 1)) : 0.0;
+  stats[0] = lstd / lmean;
+  stats[1] = dead / E;
+  stats[2] = lmax / lmean;
+  stats[3] = ent;
+  stats[4] = std::exp(ent);
+  stats[5] = cstd / (cmean + 1e-6);
+}
+
 // O5a. Capacity ([P5] capacity = tokens_per_batch / num_experts * capacity_factor),
 // rounded up to a whole token.  capacity_factor <= 0 means no limit (returns -1).
 int64_t orc_capacity(int64_t T, int E, double capacity_factor) {

@@ -36,7 +36,7 @@ MOE_DEVERR_TIMEOUT = 8
 # Every C symbol include/moe.h declares.
 EXPORTED = ("moe_status_str", "moe_capacity", "moe_workspace_size", "moe_stage_workspace_size",
             "moe_route", "moe_dispatch", "moe_expert_ffn", "moe_combine", "moe_forward",
-            "moe_device_error", "moe_dispatch_static")
+            "moe_device_error", "moe_dispatch_static", "moe_selftest_wait_timeout")
 
 # Table cells of moe_dispatch_static's library-held scratch (include/moe.h).
 MOE_DISPATCH_STATIC_MAX_CELLS = 262144
@@ -57,7 +57,8 @@ class MoeConfig(ctypes.Structure):
 class MoeForwardArgs(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in (
         "x", "w_gate", "logit_bias", "w1", "b1", "w2", "b2", "y", "logits", "topk_idx", "topk_w",
-        "counts", "aux_loss", "offsets", "kept_counts", "slot_row", "row_token", "dropped")]
+        "counts", "aux_loss", "offsets", "kept_counts", "slot_row", "row_token", "dropped",
+        "routing_stats")]
 
 
 _lib = None
@@ -78,13 +79,14 @@ def lib():
         L.moe_capacity.argtypes = [cfg, ctypes.POINTER(ctypes.c_int64)]
         L.moe_workspace_size.argtypes = [cfg, ctypes.POINTER(S)]
         L.moe_stage_workspace_size.argtypes = [cfg, ctypes.POINTER(S)]
-        L.moe_route.argtypes = [cfg, P, P, P, P, P, P, P, P, P, S, P]
+        L.moe_route.argtypes = [cfg, P, P, P, P, P, P, P, P, P, P, S, P]
         L.moe_dispatch.argtypes = [cfg, P, P, P, P, P, P, P, P, P, S, P]
         L.moe_expert_ffn.argtypes = [cfg, P, P, P, P, P, P, P, P, P, S, P]
         L.moe_combine.argtypes = [cfg, P, P, P, P, P, S, P]
         L.moe_forward.argtypes = [cfg, ctypes.POINTER(MoeForwardArgs), P, S, P]
         L.moe_device_error.argtypes = [P, P, ctypes.POINTER(ctypes.c_int32)]
         L.moe_dispatch_static.argtypes = [cfg, P, P, P, P, P, P, P, P, P, P]
+        L.moe_selftest_wait_timeout.argtypes = [P, ctypes.c_uint64, P]
         for name in EXPORTED:
             if name != "moe_status_str":
                 getattr(L, name).restype = ctypes.c_int
@@ -143,10 +145,10 @@ def moe_stage_workspace_size(cfg: MoeConfig) -> int:
 
 
 def moe_route(cfg, x, w_gate, logit_bias, logits, topk_idx, topk_w, counts, aux_loss, ws,
-              stream=None):
+              stream=None, routing_stats=None):
     _check(lib().moe_route(ctypes.byref(cfg), _p(x), _p(w_gate), _p(logit_bias), _p(logits),
-                           _p(topk_idx), _p(topk_w), _p(counts), _p(aux_loss), _p(ws),
-                           ws.numel() * ws.element_size(), _stream(stream)), "moe_route")
+                           _p(topk_idx), _p(topk_w), _p(counts), _p(aux_loss), _p(routing_stats),
+                           _p(ws), ws.numel() * ws.element_size(), _stream(stream)), "moe_route")
 
 
 def moe_dispatch(cfg, x, topk_idx, offsets, kept_counts, slot_row, row_token, dropped, x_perm, ws,
@@ -172,7 +174,11 @@ def moe_combine(cfg, y_perm, slot_row, topk_w, y, ws, stream=None):
 
 FORWARD_INPUTS = ("x", "w_gate", "logit_bias", "w1", "b1", "w2", "b2")
 FORWARD_OUTPUTS = ("y", "logits", "topk_idx", "topk_w", "counts", "aux_loss", "offsets",
-                   "kept_counts", "slot_row", "row_token", "dropped")
+                   "kept_counts", "slot_row", "row_token", "dropped", "routing_stats")
+
+# Order of the routing statistics (include/moe.h, MOE_STAT_*).
+ROUTING_STATS = ("cv", "dead_ratio", "max_over_avg", "entropy", "effective_experts",
+                 "count_cv_loss")
 
 
 def forward_args(inputs: dict, outputs: dict) -> MoeForwardArgs:
@@ -212,3 +218,9 @@ def moe_dispatch_static(cfg, x, topk_idx, offsets, kept_counts, slot_row, row_to
                                      _p(kept_counts), _p(slot_row), _p(row_token), _p(dropped),
                                      _p(x_perm), _p(device_flags), _stream(stream)),
            "moe_dispatch_static")
+
+
+def moe_selftest_wait_timeout(device_flags, limit_ns: int, stream=None) -> None:
+    """Runs the bounded pipeline wait on a barrier nothing completes (see moe.h)."""
+    _check(lib().moe_selftest_wait_timeout(_p(device_flags), int(limit_ns), _stream(stream)),
+           "moe_selftest_wait_timeout")

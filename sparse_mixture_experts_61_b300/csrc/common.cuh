@@ -89,17 +89,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 // Waits for the phase of `bar` with parity `parity` to complete.  Returns false
-// (after raising the flag and setting *abort) when the limit passes, or when
+// (after raising the flag and setting *abort) when `limit_ns` passes, or when
 // another role of the CTA has already set *abort.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
-                                                  volatile int* abort, int* flags) {
+                                                  volatile int* abort, int* flags,
+                                                  uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 0u) {
       if (*abort) return false;
-      if (global_ns() - t0 > kWaitLimitNs) {
+      if (global_ns() - t0 > limit_ns) {
         raise_flag(flags, MOE_DEVERR_TIMEOUT);
         *abort = 1;
         return false;

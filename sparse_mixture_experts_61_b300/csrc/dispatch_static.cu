@@ -108,7 +108,7 @@ extern "C" __attribute__((visibility("default"))) moe_status moe_dispatch_static
   int32_t* chunk_base = hist + kCells;
   if (moe::launch_dispatch_hist(topk_idx, c.T, c.E, c.k, hist, flags, st) != cudaSuccess ||
       moe::launch_route_finalize(hist, nullptr, static_cast<int>(nchunks), c.E, c.T, C, nullptr,
-                                 nullptr, chunk_base, kept_counts, offsets, dropped,
+                                 nullptr, chunk_base, kept_counts, offsets, dropped, nullptr,
                                  st) != cudaSuccess ||
       moe::launch_dispatch_place(c.dtype, topk_idx, c.T, c.E, c.k, C, chunk_base, offsets,
                                  slot_row, row_token, x, x_perm, c.d, flags, st) != cudaSuccess)

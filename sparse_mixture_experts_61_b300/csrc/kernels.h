@@ -17,12 +17,13 @@ cudaError_t launch_route_topk(const float* src, int nsplit, int64_t split_stride
                               float* psum, int* flags, cudaStream_t stream);
 
 // R4 + D1: reduces the per-chunk histograms (and, when psum != nullptr, the softmax
-// sums into the balance loss), then applies the capacity and scans the offsets.
-// Any of counts/aux/chunk_base/kept/offsets/dropped may be nullptr.
+// sums into the balance loss), then applies the capacity and scans the offsets;
+// with stats != nullptr also writes the six routing statistics of the counts.
+// Any of counts/aux/chunk_base/kept/offsets/dropped/stats may be nullptr.
 cudaError_t launch_route_finalize(const int32_t* hist, const float* psum, int nchunks, int E,
                                   int64_t T, int64_t C, int32_t* counts, float* aux,
                                   int32_t* chunk_base, int32_t* kept, int32_t* offsets,
-                                  int32_t* dropped, cudaStream_t stream);
+                                  int32_t* dropped, float* stats, cudaStream_t stream);
 
 // Per-chunk expert histogram of caller-provided indices (moe_dispatch on its own).
 cudaError_t launch_dispatch_hist(const int32_t* topk_idx, int64_t T, int E, int k, int32_t* hist,

@@ -240,13 +240,15 @@ MOE_EXPORT moe_status moe_stage_workspace_size(const moe_config* cfg, size_t* by
 
 MOE_EXPORT moe_status moe_route(const moe_config* cfg, const void* x, const void* w_gate,
                                 const float* logit_bias, float* logits, int32_t* topk_idx,
-                                float* topk_w, int32_t* counts, float* aux_loss, void* ws,
-                                size_t ws_bytes, moe_stream_t stream) {
+                                float* topk_w, int32_t* counts, float* aux_loss,
+                                float* routing_stats, void* ws, size_t ws_bytes,
+                                moe_stream_t stream) {
   moe_status s = check_config(cfg);
   if (s != MOE_OK) return s;
   const moe_config& c = *cfg;
   if (!tok16(c, x) || !need16(w_gate) || !opt4(logit_bias) || !opt16(logits) ||
-      !tok4(c, topk_idx) || !tok4(c, topk_w) || !opt4(counts) || !opt4(aux_loss))
+      !tok4(c, topk_idx) || !tok4(c, topk_w) || !opt4(counts) || !opt4(aux_loss) ||
+      !opt4(routing_stats))
     return MOE_ERR_INVALID_ARGUMENT;
   const Layout L = make_layout(c);
   if (!ws || !al16(ws) || ws_bytes < L.stage_end) return MOE_ERR_WORKSPACE;
@@ -255,6 +257,7 @@ MOE_EXPORT moe_status moe_route(const moe_config* cfg, const void* x, const void
   MOE_CUDA(cudaMemsetAsync(flags, 0, sizeof(int), st));
   if (c.T == 0) {
     if ((s = zero_async(counts, sizeof(int32_t) * c.E, st)) != MOE_OK) return s;
+    if ((s = zero_async(routing_stats, sizeof(float) * MOE_ROUTING_STATS, st)) != MOE_OK) return s;
     return zero_async(aux_loss, sizeof(float), st);
   }
   const int sms = sm_count();
@@ -262,10 +265,10 @@ MOE_EXPORT moe_status moe_route(const moe_config* cfg, const void* x, const void
   if ((s = run_router(c, L, ws, x, w_gate, logit_bias, logits, topk_idx, topk_w, flags, sms,
                       st)) != MOE_OK)
     return s;
-  if (counts || aux_loss)
+  if (counts || aux_loss || routing_stats)
     MOE_CUDA(launch_route_finalize(at<int32_t>(ws, L.hist), at<float>(ws, L.psum),
                                    static_cast<int>(L.nchunks), c.E, c.T, -1, counts, aux_loss,
-                                   nullptr, nullptr, nullptr, nullptr, st));
+                                   nullptr, nullptr, nullptr, nullptr, routing_stats, st));
   return MOE_OK;
 }
 
@@ -294,7 +297,7 @@ MOE_EXPORT moe_status moe_dispatch(const moe_config* cfg, const void* x, const i
   MOE_CUDA(launch_dispatch_hist(topk_idx, c.T, c.E, c.k, hist, flags, st));
   MOE_CUDA(launch_route_finalize(hist, nullptr, static_cast<int>(L.nchunks), c.E, c.T,
                                  capacity_of(c), nullptr, nullptr, chunk_base, kept_counts, offsets,
-                                 dropped, st));
+                                 dropped, nullptr, st));
   MOE_CUDA(launch_dispatch_place(c.dtype, topk_idx, c.T, c.E, c.k, capacity_of(c), chunk_base,
                                  offsets, slot_row, row_token, x, x_perm, c.d, flags, st));
   return MOE_OK;
@@ -349,7 +352,7 @@ MOE_EXPORT moe_status moe_forward(const moe_config* cfg, const moe_forward_args*
       !opt16(a->b1) || !need16(a->w2) || !opt16(a->b2) || !tok16(c, a->y) || !opt16(a->logits) ||
       !opt4(a->topk_idx) || !opt4(a->topk_w) || !opt4(a->counts) || !opt4(a->aux_loss) ||
       !opt4(a->offsets) || !opt4(a->kept_counts) || !opt4(a->slot_row) || !opt4(a->row_token) ||
-      !opt4(a->dropped))
+      !opt4(a->dropped) || !opt4(a->routing_stats))
     return MOE_ERR_INVALID_ARGUMENT;
   const Layout L = make_layout(c);
   if (!ws || !al16(ws) || ws_bytes < L.total) return MOE_ERR_WORKSPACE;
@@ -370,6 +373,8 @@ MOE_EXPORT moe_status moe_forward(const moe_config* cfg, const moe_forward_args*
     if ((s = zero_async(aux, sizeof(float), st)) != MOE_OK) return s;
     if ((s = zero_async(offsets, sizeof(int32_t) * (c.E + 1), st)) != MOE_OK) return s;
     if ((s = zero_async(kept, sizeof(int32_t) * c.E, st)) != MOE_OK) return s;
+    if ((s = zero_async(a->routing_stats, sizeof(float) * MOE_ROUTING_STATS, st)) != MOE_OK)
+      return s;
     return zero_async(dropped, sizeof(int32_t), st);
   }
   const int sms = sm_count();
@@ -386,7 +391,7 @@ MOE_EXPORT moe_status moe_forward(const moe_config* cfg, const moe_forward_args*
                       st)) != MOE_OK)
     return s;
   MOE_CUDA(launch_route_finalize(hist, psum, static_cast<int>(L.nchunks), c.E, c.T, C, counts, aux,
-                                 chunk_base, kept, offsets, dropped, st));
+                                 chunk_base, kept, offsets, dropped, a->routing_stats, st));
   MOE_CUDA(launch_dispatch_place(c.dtype, idx, c.T, c.E, c.k, C, chunk_base, offsets, slot_row,
                                  row_token, a->x, x_perm, c.d, flags, st));
   if ((s = run_expert_ffn(c, x_perm, offsets, a->w1, a->b1, a->w2, a->b2, h_buf, y_perm, flags,

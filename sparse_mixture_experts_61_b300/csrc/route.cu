@@ -2,8 +2,9 @@
 //   R2  softmax over the experts, top-k selection on the logits (value desc,
 //       lower expert index on equality) and the gate weights of the kept experts,
 //   R3  per-chunk expert histogram and per-chunk softmax column sums,
-//   R4  balance loss E * sum_e f_e P_e, and (shared with dispatch) D1: capacity,
-//       kept counts, exclusive-scan offsets and the per-chunk position bases.
+//   R4  balance loss E * sum_e f_e P_e, the routing statistics of the counts, and
+//       (shared with dispatch) D1: capacity, kept counts, exclusive-scan offsets and
+//       the per-chunk position bases.
 // Formulas: gating formula G(x)=softmax(TopK(x.W_g)) and TopKRouter.forward /
 // load_balancing_loss of "MoE mixture-of-experts routing mechanism: principles
 // and sparse activation"; capacity from its "Expert Choice routing and
@@ -164,7 +165,7 @@ __global__ void __launch_bounds__(kMaxExperts)
                           int nchunks, int E, int64_t T, int64_t C, int32_t* __restrict__ counts,
                           float* __restrict__ aux, int32_t* __restrict__ chunk_base,
                           int32_t* __restrict__ kept, int32_t* __restrict__ offsets,
-                          int32_t* __restrict__ dropped) {
+                          int32_t* __restrict__ dropped, float* __restrict__ stats) {
   __shared__ double s_red[kMaxExperts];
   __shared__ int s_scan[kMaxExperts];
   __shared__ int s_drop;
@@ -225,6 +226,55 @@ __global__ void __launch_bounds__(kMaxExperts)
     if (e == E - 1) offsets[E] = s_scan[e];
   }
   if (e == 0 && dropped) dropped[0] = s_drop;
+
+  // Routing statistics of the pre-drop counts (every thread takes part: the block
+  // reductions synchronise).  load_e = count_e / total; sample standard deviations.
+  if (stats) {
+    auto block_sum = [&](double v) {
+      __syncthreads();
+      s_red[e] = v;
+      __syncthreads();
+      for (int o = kMaxExperts / 2; o > 0; o >>= 1) {
+        if (e < o) s_red[e] += s_red[e + o];
+        __syncthreads();
+      }
+      return s_red[0];
+    };
+    auto block_max = [&](double v) {
+      __syncthreads();
+      s_red[e] = v;
+      __syncthreads();
+      for (int o = kMaxExperts / 2; o > 0; o >>= 1) {
+        if (e < o) s_red[e] = fmax(s_red[e], s_red[e + o]);
+        __syncthreads();
+      }
+      return s_red[0];
+    };
+    const bool own = e < E;
+    const double c = own ? static_cast<double>(cnt) : 0.0;
+    const double total = block_sum(c);
+    const double load = (own && total > 0.0) ? c / total : 0.0;
+    const double lmean = block_sum(load) / E, cmean = total / E;
+    const double lvar = block_sum(own ? (load - lmean) * (load - lmean) : 0.0);
+    const double cvar = block_sum(own ? (c - cmean) * (c - cmean) : 0.0);
+    const double lmax = block_max(own ? load : 0.0);
+    const double dead = block_sum((own && load < 1e-4) ? 1.0 : 0.0);
+    const double ent = block_sum(own ? -load * log(load + 1e-10) : 0.0);
+    if (e == 0) {
+      if (total > 0.0) {
+        const double lstd = E > 1 ? sqrt(lvar / (E - 1)) : 0.0;
+        const double cstd = E > 1 ? sqrt(cvar / (E - 1)) : 0.0;
+        stats[0] = static_cast<float>(lstd / lmean);
+        stats[1] = static_cast<float>(dead / E);
+        stats[2] = static_cast<float>(lmax / lmean);
+        stats[3] = static_cast<float>(ent);
+        stats[4] = static_cast<float>(exp(ent));
+        stats[5] = static_cast<float>(cstd / (cmean + 1e-6));
+      } else {
+        for (int i = 0; i < 6; ++i) stats[i] = 0.f;
+      }
+    }
+  }
 }
 
 }  // namespace
@@ -255,9 +305,9 @@ cudaError_t launch_route_topk(const float* src, int nsplit, int64_t split_stride
 cudaError_t launch_route_finalize(const int32_t* hist, const float* psum, int nchunks, int E,
                                   int64_t T, int64_t C, int32_t* counts, float* aux,
                                   int32_t* chunk_base, int32_t* kept, int32_t* offsets,
-                                  int32_t* dropped, cudaStream_t stream) {
+                                  int32_t* dropped, float* stats, cudaStream_t stream) {
   route_finalize_kernel<<<1, kMaxExperts, 0, stream>>>(hist, psum, nchunks, E, T, C, counts, aux,
-                                                       chunk_base, kept, offsets, dropped);
+                                                       chunk_base, kept, offsets, dropped, stats);
   return cudaGetLastError();
 }
 

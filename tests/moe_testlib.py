@@ -16,6 +16,7 @@ import sparse_mixture_experts_61_b300 as moe
 TOL_Y = {"bf16": 2e-2, "f32": 1e-4}
 TOL_W = 2e-6          # gate weights, absolute
 TOL_AUX = 1e-5        # balance loss, relative
+TOL_STATS = 1e-5      # routing statistics (fp32 output of a double computation), relative
 NEAR_TIE = 1e-4       # k-th / (k+1)-th logit gap below which routing may flip
 
 
@@ -47,6 +48,7 @@ def alloc_outputs(w, device="cuda") -> dict:
         slot_row=torch.full((T, k), -7, **i32),
         row_token=torch.full((T * k,), -7, **i32),
         dropped=torch.full((1,), -7, **i32),
+        routing_stats=torch.full((6,), float("nan"), **f32),
     )
 
 

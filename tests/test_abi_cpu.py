@@ -54,7 +54,7 @@ def test_library_exports_every_declared_symbol(L):
 def test_struct_layouts_match_header():
     assert ctypes.sizeof(moe.MoeConfig) == 40
     assert moe.MoeConfig.capacity_factor.offset == 32
-    assert ctypes.sizeof(moe.MoeForwardArgs) == 18 * 8
+    assert ctypes.sizeof(moe.MoeForwardArgs) == 19 * 8
 
 
 def test_status_strings(L):
@@ -84,8 +84,7 @@ def test_config_validation(L, kw, status):
                         base["gate"], base["capacity_factor"])
     n = ctypes.c_size_t()
     assert L.moe_workspace_size(ctypes.byref(cfg), ctypes.byref(n)) == status
-    assert L.moe_route(ctypes.byref(cfg), FAKE, FAKE, None, None, FAKE, FAKE, None, None, FAKE,
-                       1 << 40, None) == status
+    assert L.moe_route(ctypes.byref(cfg), FAKE, FAKE, None, None, FAKE, FAKE, None, None, None, FAKE, 1 << 40, None) == status
 
 
 def test_null_config_and_outputs(L):
@@ -116,9 +115,9 @@ def test_required_pointers_and_alignment(L):
     big = 1 << 40
     INV = moe.MOE_ERR_INVALID_ARGUMENT
     # moe_route: x, w_gate, topk_idx, topk_w required; x 16-byte aligned
-    assert L.moe_route(ctypes.byref(cfg), None, FAKE, None, None, FAKE, FAKE, None, None, FAKE, big, None) == INV
-    assert L.moe_route(ctypes.byref(cfg), FAKE_ODD, FAKE, None, None, FAKE, FAKE, None, None, FAKE, big, None) == INV
-    assert L.moe_route(ctypes.byref(cfg), FAKE, FAKE, None, None, None, FAKE, None, None, FAKE, big, None) == INV
+    assert L.moe_route(ctypes.byref(cfg), None, FAKE, None, None, FAKE, FAKE, None, None, None, FAKE, big, None) == INV
+    assert L.moe_route(ctypes.byref(cfg), FAKE_ODD, FAKE, None, None, FAKE, FAKE, None, None, None, FAKE, big, None) == INV
+    assert L.moe_route(ctypes.byref(cfg), FAKE, FAKE, None, None, None, FAKE, None, None, None, FAKE, big, None) == INV
     # moe_dispatch: x_perm required
     assert L.moe_dispatch(ctypes.byref(cfg), FAKE, FAKE, FAKE, None, FAKE, FAKE, None, None, FAKE, big, None) == INV
     # moe_expert_ffn: w1 required, b1 optional but aligned
@@ -132,8 +131,8 @@ def test_workspace_too_small_is_rejected_before_launch(L):
     cfg = moe.config(64, 64, 128, 8, 2)
     stage, full = _ws(cfg)
     WS = moe.MOE_ERR_WORKSPACE
-    assert L.moe_route(ctypes.byref(cfg), FAKE, FAKE, None, None, FAKE, FAKE, None, None, FAKE, stage - 1, None) == WS
-    assert L.moe_route(ctypes.byref(cfg), FAKE, FAKE, None, None, FAKE, FAKE, None, None, None, stage, None) == WS
+    assert L.moe_route(ctypes.byref(cfg), FAKE, FAKE, None, None, FAKE, FAKE, None, None, None, FAKE, stage - 1, None) == WS
+    assert L.moe_route(ctypes.byref(cfg), FAKE, FAKE, None, None, FAKE, FAKE, None, None, None, None, stage, None) == WS
     assert L.moe_dispatch(ctypes.byref(cfg), FAKE, FAKE, FAKE, None, FAKE, FAKE, None, FAKE, FAKE, stage - 1, None) == WS
     assert L.moe_expert_ffn(ctypes.byref(cfg), FAKE, FAKE, FAKE, None, FAKE, None, FAKE, FAKE, FAKE, 16, None) == WS
     assert L.moe_combine(ctypes.byref(cfg), FAKE, FAKE, FAKE, FAKE, FAKE, 0, None) == WS
@@ -147,3 +146,10 @@ def test_workspace_too_small_is_rejected_before_launch(L):
 def test_capacity_matches_oracle(L, T, E, cf):
     cfg = moe.config(T, 64, 64, E, 1, "bf16", 1, cf)
     assert moe.moe_capacity(cfg) == oracle.capacity(T, E, cf if cf > 0 else None)
+
+
+def test_selftest_validation_before_launch(L):
+    assert L.moe_selftest_wait_timeout(None, 1000, None) == moe.MOE_ERR_INVALID_ARGUMENT
+    assert L.moe_selftest_wait_timeout(FAKE_ODD + 1, 1000, None) == moe.MOE_ERR_INVALID_ARGUMENT
+    assert L.moe_selftest_wait_timeout(FAKE, 0, None) == moe.MOE_ERR_INVALID_ARGUMENT
+    assert L.moe_selftest_wait_timeout(FAKE, 3 * 10**9, None) == moe.MOE_ERR_INVALID_ARGUMENT

@@ -39,6 +39,8 @@ def check_routing_exact(g, ref):
     assert int(g["dropped"][0]) == ref["dropped"]
     assert float(np.abs(g["topk_w"] - ref["w"]).max()) <= tl.TOL_W
     assert abs(float(g["aux_loss"][0]) - ref["aux"]) <= tl.TOL_AUX * abs(ref["aux"])
+    st = oracle.routing_stats(ref["counts"])
+    np.testing.assert_allclose(g["routing_stats"], st, rtol=tl.TOL_STATS, atol=1e-7)
 
 
 @pytest.mark.parametrize("name", list(PARITY_WORKLOADS))
@@ -93,7 +95,9 @@ def test_stage_calls_match_forward(name):
     wts = torch.empty((T, k), **f32)
     counts = torch.empty((E,), **i32)
     aux = torch.empty((1,), **f32)
-    moe.moe_route(cfg, dev["x"], dev["w_gate"], dev["logit_bias"], logits, idx, wts, counts, aux, ws)
+    stats = torch.empty((6,), **f32)
+    moe.moe_route(cfg, dev["x"], dev["w_gate"], dev["logit_bias"], logits, idx, wts, counts, aux, ws,
+                  routing_stats=stats)
     assert moe.moe_device_error(ws) == 0
     # logits kept inside the workspace instead of a caller buffer: same decisions
     idx2 = torch.empty_like(idx)
@@ -118,7 +122,8 @@ def test_stage_calls_match_forward(name):
     assert moe.moe_device_error(ws) == 0
 
     for key, t in [("logits", logits), ("topk_idx", idx), ("topk_w", wts), ("counts", counts),
-                   ("aux_loss", aux), ("offsets", offsets), ("kept_counts", kept),
+                   ("aux_loss", aux), ("routing_stats", stats), ("offsets", offsets),
+                   ("kept_counts", kept),
                    ("slot_row", slot_row), ("row_token", row_token), ("dropped", dropped), ("y", y)]:
         got = t.float().cpu().numpy() if t.dtype == torch.bfloat16 else t.cpu().numpy()
         np.testing.assert_array_equal(got, fw[key], err_msg=key)
@@ -213,6 +218,7 @@ def test_empty_batch():
     assert moe.moe_device_error(ws) == 0
     assert outs["counts"].eq(0).all() and outs["offsets"].eq(0).all()
     assert outs["dropped"].item() == 0 and outs["aux_loss"].item() == 0.0
+    assert outs["routing_stats"].eq(0).all()
 
 
 def test_dispatch_flags_out_of_range_index():

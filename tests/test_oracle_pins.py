@@ -324,3 +324,49 @@ def test_parity_workloads_are_finite_and_routing_valid():
     assert np.isfinite(out["y"]).all()
     assert out["idx"].min() >= 0 and out["idx"].max() < w.E
     assert all(len(set(r)) == w.k for r in out["idx"].tolist())
+
+
+@pytest.mark.parametrize("E", [1, 4, 8, 64, 256])
+def test_routing_stats_uniform_load(E):
+    """Perfectly even counts: CV 0, no dead expert, max/avg 1, entropy ln E, E effective."""
+    st = oracle.routing_stats(np.full(E, 37))
+    np.testing.assert_allclose(st[[0, 1, 5]], 0.0, atol=1e-12)
+    assert st[2] == pytest.approx(1.0, rel=1e-12)
+    # entropy = -sum (1/E) ln(1/E + 1e-10) = -ln(1/E + 1e-10)
+    assert st[3] == pytest.approx(-math.log(1.0 / E + 1e-10), rel=1e-13)
+    assert st[4] == pytest.approx(1.0 / (1.0 / E + 1e-10), rel=1e-12)
+
+
+@pytest.mark.parametrize("E", [2, 8, 128])
+def test_routing_stats_single_expert_takes_all(E):
+    """All assignments on one expert: load = (1, 0, ...): sample std 1/sqrt(E), so
+    CV = sqrt(E); dead ratio (E-1)/E; max/avg = E; entropy ~ 0; one effective expert."""
+    counts = np.zeros(E, np.int64)
+    counts[E // 2] = 5000
+    st = oracle.routing_stats(counts)
+    assert st[0] == pytest.approx(math.sqrt(E), rel=1e-12)
+    assert st[1] == pytest.approx((E - 1) / E, rel=1e-12)
+    assert st[2] == pytest.approx(E, rel=1e-12)
+    assert st[3] == pytest.approx(-math.log(1.0 + 1e-10), abs=1e-15)
+    assert st[4] == pytest.approx(1.0, abs=1e-9)
+    # counts (N, 0, ...): sample std N/sqrt(E), mean N/E -> (N/sqrt(E)) / (N/E + 1e-6)
+    N = 5000.0
+    assert st[5] == pytest.approx((N / math.sqrt(E)) / (N / E + 1e-6), rel=1e-12)
+
+
+def test_routing_stats_match_library_routines():
+    rng = np.random.default_rng(3)
+    counts = rng.integers(0, 500, 64)
+    counts[::7] = 0
+    st = oracle.routing_stats(counts)
+    load = counts / counts.sum()
+    assert st[0] == pytest.approx(np.std(load, ddof=1) / np.mean(load), rel=1e-12)
+    assert st[1] == pytest.approx(np.mean(load < 1e-4), rel=1e-12)
+    assert st[2] == pytest.approx(load.max() / load.mean(), rel=1e-12)
+    from scipy.stats import entropy as scipy_entropy
+    assert st[3] == pytest.approx(scipy_entropy(load), rel=1e-7)   # +1e-10 inside the log
+    assert st[5] == pytest.approx(np.std(counts, ddof=1) / (np.mean(counts) + 1e-6), rel=1e-12)
+
+
+def test_routing_stats_empty():
+    np.testing.assert_array_equal(oracle.routing_stats(np.zeros(8, np.int64)), 0.0)
