@@ -56,8 +56,19 @@ __global__ void __launch_bounds__(kRouteWarps * 32)
       const int e = lane + 32 * q;
       v[q] = -INFINITY;
       if (e < E) {
-        float l = src[t * E + e];
-        for (int sp = 1; sp < nsplit; ++sp) l += src[sp * split_stride + t * E + e];
+        // Splits added in order; their loads are issued four at a time.
+        const float* p0 = src + t * E + e;
+        float l = p0[0];
+        int sp = 1;
+        for (; sp + 3 < nsplit; sp += 4) {
+          const float a = p0[sp * split_stride], b = p0[(sp + 1) * split_stride],
+                      c = p0[(sp + 2) * split_stride], d = p0[(sp + 3) * split_stride];
+          l += a;
+          l += b;
+          l += c;
+          l += d;
+        }
+        for (; sp < nsplit; ++sp) l += p0[sp * split_stride];
         if (bias) l += bias[e];
         if (logits_out) logits_out[t * E + e] = l;
         v[q] = l;
