@@ -75,6 +75,26 @@ typedef enum {
   MOE_GATE_SOFTMAX_TOPK_RENORM = 1
 } moe_gate;
 
+/* Routing noise.  The random draws are an input, noise[T,E] fp32, supplied by the
+   caller (so a run is reproducible and testable); the library applies the variant's
+   arithmetic to the router logits l and selects the top-k of the resulting scores:
+   - MOE_NOISE_GUMBEL: noise holds uniform draws u in (0,1); score = l + g with
+     g = -log(-log(u + 1e-9) + 1e-9) (Gumbel top-k of the sparse-inference article
+     (lpnh.cn), sections 2.3 and 3.2).  Gate weights and f use the scores as logits.
+   - MOE_NOISE_PROB_GAUSS: noise holds scaled Gaussian draws n; score = softmax(l) + n
+     (noise on the probabilities, MoE overview (cnnetsun.cn) section 2.1).  Gate
+     weights and f use the clean logits l of the selected experts.
+   - MOE_NOISE_LOGIT_SOFTMAX: noise holds scaled draws n; score = l + n * softmax(l)
+     (noise injection of the routing-mechanism page, router-collapse section).  Gate
+     weights and f use the scores as logits.
+   With noise, the `logits` output holds the scores the selection used. */
+typedef enum {
+  MOE_NOISE_NONE = 0,
+  MOE_NOISE_GUMBEL = 1,
+  MOE_NOISE_PROB_GAUSS = 2,
+  MOE_NOISE_LOGIT_SOFTMAX = 3
+} moe_noise;
+
 /* Routing statistics of the pre-drop per-expert counts, in this order (load_e =
    count_e / sum(count); sample standard deviations, divisor E-1, 0 when E = 1):
    cv = std(load)/mean(load); dead_ratio = share of experts with load < 1e-4;
@@ -111,6 +131,7 @@ typedef struct moe_config {
   int32_t gate;           /* moe_gate */
   double capacity_factor; /* > 0: capacity C = ceil(T * capacity_factor / E) kept assignments
                              per expert, later ones dropped; <= 0: no limit */
+  int32_t noise;          /* moe_noise: routing noise applied before selection */
 } moe_config;
 
 /* Inputs and outputs of moe_forward.  Outputs marked "or NULL" are optional;
@@ -119,6 +140,7 @@ typedef struct moe_forward_args {
   const void* x;            /* [T,d] dtype */
   const void* w_gate;       /* [E,d] dtype */
   const float* logit_bias;  /* [E] fp32 added to every token's logits, or NULL */
+  const float* noise;       /* [T,E] fp32 random draws when cfg->noise != NONE, else NULL */
   const void* w1;           /* [E,h,d] dtype */
   const void* b1;           /* [E,h] dtype, or NULL for zero */
   const void* w2;           /* [E,d,h] dtype */
@@ -161,10 +183,12 @@ moe_status moe_stage_workspace_size(const moe_config* cfg, size_t* bytes);
    counts[e]    : number of (t,j) with topk_idx[t,j] == e (before any capacity drop)
    aux_loss[0]  : E * sum_e f_e P_e, f_e = mean_t softmax(logits)[t,e], P_e = counts[e]/T
    routing_stats: the MOE_ROUTING_STATS statistics of counts (above)
+   noise        : [T,E] draws for cfg->noise (required then, else ignored)
    logits, counts, aux_loss and routing_stats may be NULL.  Selection and weights
    are computed from exactly the fp32 logits written.  Results are deterministic. */
 moe_status moe_route(const moe_config* cfg, const void* x, const void* w_gate,
-                     const float* logit_bias, float* logits, int32_t* topk_idx, float* topk_w,
+                     const float* logit_bias, const float* noise, float* logits,
+                     int32_t* topk_idx, float* topk_w,
                      int32_t* counts, float* aux_loss, float* routing_stats, void* ws,
                      size_t ws_bytes, moe_stream_t stream);
 

@@ -40,6 +40,7 @@ def lib():
         L.orc_aux_loss.argtypes = [_I64, _I, _I, _P, _P, _P, _P, _P]
         L.orc_aux_loss.restype = _D
         L.orc_routing_stats.argtypes = [_I, _P, _P]
+        L.orc_noisy_scores.argtypes = [_I64, _I, _I, _P, _P, _P]
         L.orc_capacity.argtypes = [_I64, _I, _D]
         L.orc_capacity.restype = _I64
         L.orc_dispatch.argtypes = [_I64, _I, _I, _I64, _P, _P, _P, _P, _P, _P]
@@ -156,6 +157,20 @@ def aux_loss(p, idx):
     return loss, counts, f, P
 
 
+NOISE_NONE, NOISE_GUMBEL, NOISE_PROB_GAUSS, NOISE_LOGIT_SOFTMAX = 0, 1, 2, 3
+
+
+def noisy_scores(lg, noise, mode):
+    """O2n: selection scores under routing noise `mode` (1 Gumbel on logits from uniform
+    draws, 2 Gaussian draws added to probabilities, 3 logits + draws * softmax)."""
+    lg = np.ascontiguousarray(lg, np.float64)
+    noise = np.ascontiguousarray(noise, np.float32)
+    T, E = lg.shape
+    out = np.empty_like(lg)
+    lib().orc_noisy_scores(T, E, int(mode), _ptr(lg), _ptr(noise), _ptr(out))
+    return out
+
+
 ROUTING_STATS = ("cv", "dead_ratio", "max_over_avg", "entropy", "effective_experts",
                  "count_cv_loss")
 
@@ -263,6 +278,25 @@ def forward_dense(inp, k, mode, capacity_factor=None):
                             _ptr(xr), _ptr(wg), _ptr(lb), _ptr(w1), _ptr(b1), _ptr(w2), _ptr(b2),
                             _ptr(y))
     return y
+
+
+def noisy_routed_reference(k, mode, capacity_factor, gpu_scores, noise_mode, clean_logits):
+    """Routing stages on given fp32 selection scores (the GPU's) under routing noise.
+
+    Top-k, counts, capacity and placement follow the scores exactly.  Gate weights and
+    the balance loss's f use the scores as logits for the logit-noise modes (1, 3); for
+    noise on the probabilities (mode 2) they use `clean_logits` (double), since the
+    noisy scores are not a distribution."""
+    sc = np.asarray(gpu_scores, dtype=np.float32).astype(np.float64)
+    T, E = sc.shape
+    idx = topk(sc, k)
+    base = sc if noise_mode in (NOISE_GUMBEL, NOISE_LOGIT_SOFTMAX) else np.asarray(clean_logits,
+                                                                                 np.float64)
+    w = gate_weights(base, idx, mode)
+    aux, counts, f, P = aux_loss(softmax(base), idx)
+    C = capacity(T, E, capacity_factor)
+    disp = dispatch(idx, E, C)
+    return dict(idx=idx, w=w, counts=counts, aux=aux, f=f, P=P, C=C, **disp)
 
 
 def routed_reference(inp, k, mode, capacity_factor, gpu_logits):

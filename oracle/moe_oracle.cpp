@@ -144,6 +144,35 @@ void orc_gate_weights(int64_t T, int E, int k, int mode, const double* logits,
   }
 }
 
+// O2n. Noisy routing scores: the values top-k selects on when routing noise is
+// applied.  The random draws are inputs (noise[T,E]), so both implementations see
+// the same numbers.
+//   mode 1 (the sparse-inference article, section 3.2: Gumbel top-k): noise holds
+//          uniform draws u; g = -log(-log(u + 1e-9) + 1e-9); score = logit + g.
+//   mode 2 (MoE overview, section 2.1: noise added to the probabilities): noise holds
+//          the scaled Gaussian draws n; score = softmax(logits) + n.
+//   mode 3 (routing-mechanism page, router collapse: logits + noise * softmax(logits)):
+//          noise holds the scaled draws n; score = logit + n * softmax(logits).
+void orc_noisy_scores(int64_t T, int E, int mode, const double* logits, const float* noise,
+                      double* scores) {
+  std::vector<double> p(E);
+  for (int64_t t = 0; t < T; ++t) {
+    const double* l = logits + t * E;
+    const float* n = noise + t * E;
+    orc_softmax(1, E, l, p.data());
+    for (int e = 0; e < E; ++e) {
+      double v;
+      if (mode == 1)
+        v = l[e] - std::log(-std::log((double)n[e] + 1e-9) + 1e-9);
+      else if (mode == 2)
+        v = p[e] + (double)n[e];
+      else
+        v = l[e] + (double)n[e] * p[e];
+      scores[t * E + e] = v;
+    }
+  }
+}
+
 // O4. Per-expert counts and the load-balancing loss ([P5] load_balancing_loss):
 //   f_e = (1/T) sum_t p[t,e]            (full softmax, every gate mode)
 //   P_e = count_e / T                   (top-k assignments before any drop; sum_e P_e = k)

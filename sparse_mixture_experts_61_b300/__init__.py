@@ -27,6 +27,10 @@ MOE_F32 = 0
 MOE_BF16 = 1
 MOE_GATE_TOPK_SOFTMAX = 0
 MOE_GATE_SOFTMAX_TOPK_RENORM = 1
+MOE_NOISE_NONE = 0
+MOE_NOISE_GUMBEL = 1
+MOE_NOISE_PROB_GAUSS = 2
+MOE_NOISE_LOGIT_SOFTMAX = 3
 
 MOE_DEVERR_BAD_INDEX = 1
 MOE_DEVERR_BAD_ROW = 2
@@ -51,12 +55,14 @@ class MoeError(RuntimeError):
 class MoeConfig(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int64), ("d", ctypes.c_int32), ("h", ctypes.c_int32),
                 ("E", ctypes.c_int32), ("k", ctypes.c_int32), ("dtype", ctypes.c_int32),
-                ("gate", ctypes.c_int32), ("capacity_factor", ctypes.c_double)]
+                ("gate", ctypes.c_int32), ("capacity_factor", ctypes.c_double),
+                ("noise", ctypes.c_int32)]
 
 
 class MoeForwardArgs(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in (
-        "x", "w_gate", "logit_bias", "w1", "b1", "w2", "b2", "y", "logits", "topk_idx", "topk_w",
+        "x", "w_gate", "logit_bias", "noise", "w1", "b1", "w2", "b2", "y", "logits", "topk_idx",
+        "topk_w",
         "counts", "aux_loss", "offsets", "kept_counts", "slot_row", "row_token", "dropped",
         "routing_stats")]
 
@@ -79,7 +85,7 @@ def lib():
         L.moe_capacity.argtypes = [cfg, ctypes.POINTER(ctypes.c_int64)]
         L.moe_workspace_size.argtypes = [cfg, ctypes.POINTER(S)]
         L.moe_stage_workspace_size.argtypes = [cfg, ctypes.POINTER(S)]
-        L.moe_route.argtypes = [cfg, P, P, P, P, P, P, P, P, P, P, S, P]
+        L.moe_route.argtypes = [cfg, P, P, P, P, P, P, P, P, P, P, P, S, P]
         L.moe_dispatch.argtypes = [cfg, P, P, P, P, P, P, P, P, P, S, P]
         L.moe_expert_ffn.argtypes = [cfg, P, P, P, P, P, P, P, P, P, S, P]
         L.moe_combine.argtypes = [cfg, P, P, P, P, P, S, P]
@@ -98,15 +104,15 @@ def status_str(status: int) -> str:
     return lib().moe_status_str(int(status)).decode()
 
 
-def config(T, d, h, E, k, dtype="bf16", gate=0, capacity_factor=0.0) -> MoeConfig:
+def config(T, d, h, E, k, dtype="bf16", gate=0, capacity_factor=0.0, noise=0) -> MoeConfig:
     dt = {"f32": MOE_F32, "bf16": MOE_BF16}[dtype] if isinstance(dtype, str) else int(dtype)
     return MoeConfig(int(T), int(d), int(h), int(E), int(k), dt, int(gate),
-                     float(capacity_factor or 0.0))
+                     float(capacity_factor or 0.0), int(noise))
 
 
-def config_from_workload(w) -> MoeConfig:
+def config_from_workload(w, noise=0) -> MoeConfig:
     """Config for an object with T, d, h, E, k, dtype, gate, capacity_factor attributes."""
-    return config(w.T, w.d, w.h, w.E, w.k, w.dtype, w.gate, w.capacity_factor)
+    return config(w.T, w.d, w.h, w.E, w.k, w.dtype, w.gate, w.capacity_factor, noise)
 
 
 def _p(t) -> Optional[int]:
@@ -145,8 +151,9 @@ def moe_stage_workspace_size(cfg: MoeConfig) -> int:
 
 
 def moe_route(cfg, x, w_gate, logit_bias, logits, topk_idx, topk_w, counts, aux_loss, ws,
-              stream=None, routing_stats=None):
-    _check(lib().moe_route(ctypes.byref(cfg), _p(x), _p(w_gate), _p(logit_bias), _p(logits),
+              stream=None, routing_stats=None, noise=None):
+    _check(lib().moe_route(ctypes.byref(cfg), _p(x), _p(w_gate), _p(logit_bias), _p(noise),
+                           _p(logits),
                            _p(topk_idx), _p(topk_w), _p(counts), _p(aux_loss), _p(routing_stats),
                            _p(ws), ws.numel() * ws.element_size(), _stream(stream)), "moe_route")
 
@@ -172,7 +179,7 @@ def moe_combine(cfg, y_perm, slot_row, topk_w, y, ws, stream=None):
            "moe_combine")
 
 
-FORWARD_INPUTS = ("x", "w_gate", "logit_bias", "w1", "b1", "w2", "b2")
+FORWARD_INPUTS = ("x", "w_gate", "logit_bias", "noise", "w1", "b1", "w2", "b2")
 FORWARD_OUTPUTS = ("y", "logits", "topk_idx", "topk_w", "counts", "aux_loss", "offsets",
                    "kept_counts", "slot_row", "row_token", "dropped", "routing_stats")
 

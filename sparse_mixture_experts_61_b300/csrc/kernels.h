@@ -11,10 +11,13 @@ namespace moe {
 // softmax column sums.  The logits of token t are
 //   l[t,e] = sum_{s < nsplit} src[s * split_stride + t*E + e]  (+ bias[e] if bias)
 // added in that order; when logits_out is given they are written there.
+// With noise_mode != 0 the selection scores follow moe.h's moe_noise (draws in
+// noise[T,E]) and logits_out receives those scores.
 cudaError_t launch_route_topk(const float* src, int nsplit, int64_t split_stride,
-                              const float* bias, float* logits_out, int64_t T, int E, int k,
-                              int gate, int32_t* topk_idx, float* topk_w, int32_t* hist,
-                              float* psum, int* flags, cudaStream_t stream);
+                              const float* bias, const float* noise, int noise_mode,
+                              float* logits_out, int64_t T, int E, int k, int gate,
+                              int32_t* topk_idx, float* topk_w, int32_t* hist, float* psum,
+                              int* flags, cudaStream_t stream);
 
 // R4 + D1: reduces the per-chunk histograms (and, when psum != nullptr, the softmax
 // sums into the balance loss), then applies the capacity and scans the offsets;

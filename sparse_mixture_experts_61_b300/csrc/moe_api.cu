@@ -67,6 +67,8 @@ moe_status check_config(const moe_config* c) {
   if (c->gate != MOE_GATE_TOPK_SOFTMAX && c->gate != MOE_GATE_SOFTMAX_TOPK_RENORM)
     return MOE_ERR_INVALID_ARGUMENT;
   if (!std::isfinite(c->capacity_factor)) return MOE_ERR_INVALID_ARGUMENT;
+  if (c->noise < MOE_NOISE_NONE || c->noise > MOE_NOISE_LOGIT_SOFTMAX)
+    return MOE_ERR_INVALID_ARGUMENT;
   if (c->T < 0 || c->k < 1 || c->k > kMaxK || c->E < c->k || c->E > kMaxExperts)
     return MOE_ERR_UNSUPPORTED;
   if (c->d < 8 || c->d % 8 != 0 || c->h < 8 || c->h % 8 != 0) return MOE_ERR_UNSUPPORTED;
@@ -122,8 +124,9 @@ T* at(void* ws, size_t off) {
 // K-split partial sums into the workspace; the top-k kernel adds them and the logit
 // bias and writes the logits to `logits` when given.
 moe_status run_router(const moe_config& c, const Layout& L, void* ws, const void* x,
-                      const void* w_gate, const float* logit_bias, float* logits,
-                      int32_t* topk_idx, float* topk_w, int* flags, int sms, cudaStream_t st) {
+                      const void* w_gate, const float* logit_bias, const float* noise,
+                      float* logits, int32_t* topk_idx, float* topk_w, int* flags, int sms,
+                      cudaStream_t st) {
   GemmArgs g{};
   g.A = x;
   g.rows_alloc = c.T;
@@ -138,20 +141,24 @@ moe_status run_router(const moe_config& c, const Layout& L, void* ws, const void
   int32_t* hist = at<int32_t>(ws, L.hist);
   float* psum = at<float>(ws, L.psum);
   if (c.dtype == MOE_F32) {
-    float* lg = logits ? logits : region;
+    // Without noise the GEMM's biased logits are the output; with noise the output is
+    // the selection scores, written by the top-k kernel.
+    const bool noisy = c.noise != MOE_NOISE_NONE;
+    float* lg = (logits && !noisy) ? logits : region;
     g.bias = logit_bias;
     g.out = lg;
     MOE_CUDA(launch_simt_gemm_f32(g, EPI_ROUTER_F32, sms, st));
-    MOE_CUDA(launch_route_topk(lg, 1, 0, nullptr, nullptr, c.T, c.E, c.k, c.gate, topk_idx,
-                               topk_w, hist, psum, flags, st));
+    MOE_CUDA(launch_route_topk(lg, 1, 0, nullptr, noise, c.noise, noisy ? logits : nullptr, c.T,
+                               c.E, c.k, c.gate, topk_idx, topk_w, hist, psum, flags, st));
   } else {
     g.bias = nullptr;
     g.out = region;
     g.ksplit = router_splits(c.T, c.E, c.d, sms < kMaxSmsForSizing ? sms : kMaxSmsForSizing);
     g.split_stride = c.T * c.E;
     MOE_CUDA(launch_tc_gemm_bf16(g, EPI_ROUTER_F32, sms, st));
-    MOE_CUDA(launch_route_topk(region, g.ksplit, g.split_stride, logit_bias, logits, c.T, c.E,
-                               c.k, c.gate, topk_idx, topk_w, hist, psum, flags, st));
+    MOE_CUDA(launch_route_topk(region, g.ksplit, g.split_stride, logit_bias, noise, c.noise,
+                               logits, c.T, c.E, c.k, c.gate, topk_idx, topk_w, hist, psum, flags,
+                               st));
   }
   return MOE_OK;
 }
@@ -239,7 +246,8 @@ MOE_EXPORT moe_status moe_stage_workspace_size(const moe_config* cfg, size_t* by
 }
 
 MOE_EXPORT moe_status moe_route(const moe_config* cfg, const void* x, const void* w_gate,
-                                const float* logit_bias, float* logits, int32_t* topk_idx,
+                                const float* logit_bias, const float* noise, float* logits,
+                                int32_t* topk_idx,
                                 float* topk_w, int32_t* counts, float* aux_loss,
                                 float* routing_stats, void* ws, size_t ws_bytes,
                                 moe_stream_t stream) {
@@ -248,7 +256,7 @@ MOE_EXPORT moe_status moe_route(const moe_config* cfg, const void* x, const void
   const moe_config& c = *cfg;
   if (!tok16(c, x) || !need16(w_gate) || !opt4(logit_bias) || !opt16(logits) ||
       !tok4(c, topk_idx) || !tok4(c, topk_w) || !opt4(counts) || !opt4(aux_loss) ||
-      !opt4(routing_stats))
+      !opt4(routing_stats) || (c.noise != MOE_NOISE_NONE ? !tok4(c, noise) : !opt4(noise)))
     return MOE_ERR_INVALID_ARGUMENT;
   const Layout L = make_layout(c);
   if (!ws || !al16(ws) || ws_bytes < L.stage_end) return MOE_ERR_WORKSPACE;
@@ -262,8 +270,8 @@ MOE_EXPORT moe_status moe_route(const moe_config* cfg, const void* x, const void
   }
   const int sms = sm_count();
   if (sms <= 0) return MOE_ERR_CUDA;
-  if ((s = run_router(c, L, ws, x, w_gate, logit_bias, logits, topk_idx, topk_w, flags, sms,
-                      st)) != MOE_OK)
+  if ((s = run_router(c, L, ws, x, w_gate, logit_bias, noise, logits, topk_idx, topk_w, flags,
+                      sms, st)) != MOE_OK)
     return s;
   if (counts || aux_loss || routing_stats)
     MOE_CUDA(launch_route_finalize(at<int32_t>(ws, L.hist), at<float>(ws, L.psum),
@@ -352,7 +360,8 @@ MOE_EXPORT moe_status moe_forward(const moe_config* cfg, const moe_forward_args*
       !opt16(a->b1) || !need16(a->w2) || !opt16(a->b2) || !tok16(c, a->y) || !opt16(a->logits) ||
       !opt4(a->topk_idx) || !opt4(a->topk_w) || !opt4(a->counts) || !opt4(a->aux_loss) ||
       !opt4(a->offsets) || !opt4(a->kept_counts) || !opt4(a->slot_row) || !opt4(a->row_token) ||
-      !opt4(a->dropped) || !opt4(a->routing_stats))
+      !opt4(a->dropped) || !opt4(a->routing_stats) ||
+      (c.noise != MOE_NOISE_NONE ? !tok4(c, a->noise) : !opt4(a->noise)))
     return MOE_ERR_INVALID_ARGUMENT;
   const Layout L = make_layout(c);
   if (!ws || !al16(ws) || ws_bytes < L.total) return MOE_ERR_WORKSPACE;
@@ -387,8 +396,8 @@ MOE_EXPORT moe_status moe_forward(const moe_config* cfg, const moe_forward_args*
   void* y_perm = at<void>(ws, L.y_perm);
   const int64_t C = capacity_of(c);
 
-  if ((s = run_router(c, L, ws, a->x, a->w_gate, a->logit_bias, a->logits, idx, w, flags, sms,
-                      st)) != MOE_OK)
+  if ((s = run_router(c, L, ws, a->x, a->w_gate, a->logit_bias, a->noise, a->logits, idx, w,
+                      flags, sms, st)) != MOE_OK)
     return s;
   MOE_CUDA(launch_route_finalize(hist, psum, static_cast<int>(L.nchunks), c.E, c.T, C, counts, aux,
                                  chunk_base, kept, offsets, dropped, a->routing_stats, st));

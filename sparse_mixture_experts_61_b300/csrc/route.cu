@@ -31,8 +31,9 @@ constexpr int kTokensPerWarp = kChunk / kRouteWarps;
 template <int EPL>
 __global__ void __launch_bounds__(kRouteWarps * 32)
     route_topk_kernel(const float* __restrict__ src, int nsplit, int64_t split_stride,
-                      const float* __restrict__ bias, float* __restrict__ logits_out, int64_t T,
-                      int E, int k, int gate, int32_t* __restrict__ topk_idx,
+                      const float* __restrict__ bias, const float* __restrict__ noise,
+                      int noise_mode, float* __restrict__ logits_out, int64_t T, int E, int k,
+                      int gate, int32_t* __restrict__ topk_idx,
                       float* __restrict__ topk_w, int32_t* __restrict__ hist,
                       float* __restrict__ psum, int* flags) {
   __shared__ int s_hist[kMaxExperts];
@@ -49,8 +50,8 @@ __global__ void __launch_bounds__(kRouteWarps * 32)
   for (int i = 0; i < kTokensPerWarp; ++i) {
     const int64_t t = t_first + i;
     if (t >= T) break;  // warp-uniform
+    // v: the router logits (split partials added in order, then the bias).
     float v[EPL];
-    bool bad = false;
 #pragma unroll
     for (int q = 0; q < EPL; ++q) {
       const int e = lane + 32 * q;
@@ -70,75 +71,133 @@ __global__ void __launch_bounds__(kRouteWarps * 32)
         }
         for (; sp < nsplit; ++sp) l += p0[sp * split_stride];
         if (bias) l += bias[e];
-        if (logits_out) logits_out[t * E + e] = l;
         v[q] = l;
-        if (!isfinite(l)) bad = true;
+      }
+    }
+    // sc: the selection scores (the logits themselves without noise).
+    float sc[EPL];
+    if (noise_mode == MOE_NOISE_PROB_GAUSS || noise_mode == MOE_NOISE_LOGIT_SOFTMAX) {
+      float mc = -INFINITY;
+#pragma unroll
+      for (int q = 0; q < EPL; ++q)
+        if (lane + 32 * q < E) mc = fmaxf(mc, v[q]);
+      mc = warp_max(mc);
+      float sc_sum = 0.f;
+#pragma unroll
+      for (int q = 0; q < EPL; ++q) {
+        sc[q] = (lane + 32 * q < E) ? expf(v[q] - mc) : 0.f;
+        sc_sum += sc[q];
+      }
+      sc_sum = warp_sum(sc_sum);
+#pragma unroll
+      for (int q = 0; q < EPL; ++q) {
+        const int e = lane + 32 * q;
+        if (e < E) {
+          const float pc = sc[q] / sc_sum;
+          const float n = noise[t * E + e];
+          sc[q] = (noise_mode == MOE_NOISE_PROB_GAUSS) ? pc + n : v[q] + n * pc;
+        } else {
+          sc[q] = -INFINITY;
+        }
+      }
+    } else {
+#pragma unroll
+      for (int q = 0; q < EPL; ++q) {
+        const int e = lane + 32 * q;
+        sc[q] = v[q];
+        if (noise_mode == MOE_NOISE_GUMBEL && e < E) {
+          // g = -log(-log(u + 1e-9) + 1e-9).  For u > 1/2, u - 1 is exact and
+          // log1p keeps -log(u + 1e-9) accurate where it is tiny (u near 1).
+          const float u = noise[t * E + e];
+          const float a = (u > 0.5f) ? -log1pf((u - 1.0f) + 1e-9f) : -logf(u + 1e-9f);
+          sc[q] = v[q] - logf(a + 1e-9f);
+        }
+      }
+    }
+    bool bad = false;
+#pragma unroll
+    for (int q = 0; q < EPL; ++q) {
+      const int e = lane + 32 * q;
+      if (e < E) {
+        if (logits_out) logits_out[t * E + e] = sc[q];
+        if (!isfinite(sc[q])) bad = true;
       }
     }
     if (__any_sync(0xffffffffu, bad) && lane == 0) raise_flag(flags, MOE_DEVERR_NONFINITE);
+    // b: the logits the gate weights and f use -- the clean ones when the noise was
+    // added to the probabilities, the scores otherwise.
+    const bool clean_base = noise_mode == MOE_NOISE_PROB_GAUSS;
 
-    // softmax: m = max, s = sum exp(l - m)
+    // softmax of b: m = max, s = sum exp(b - m)
     float m = -INFINITY;
 #pragma unroll
     for (int q = 0; q < EPL; ++q)
-      if (lane + 32 * q < E) m = fmaxf(m, v[q]);
+      if (lane + 32 * q < E) m = fmaxf(m, clean_base ? v[q] : sc[q]);
     m = warp_max(m);
     float ex[EPL];
     float s = 0.f;
 #pragma unroll
     for (int q = 0; q < EPL; ++q) {
-      ex[q] = (lane + 32 * q < E) ? expf(v[q] - m) : 0.f;
+      ex[q] = (lane + 32 * q < E) ? expf((clean_base ? v[q] : sc[q]) - m) : 0.f;
       s += ex[q];
     }
     s = warp_sum(s);
 #pragma unroll
     for (int q = 0; q < EPL; ++q) ps[q] += ex[q] / s;
 
-    // top-k: k rounds of a warp arg-max under (value desc, index asc).
+    // top-k on the scores: k rounds of a warp arg-max under (value desc, index asc).
+    // Each candidate carries its b value for the weights.
     uint32_t taken = 0;
     int sel_e[kMaxK];
-    float sel_v[kMaxK];
+    float sel_b[kMaxK];
 #pragma unroll
     for (int j = 0; j < kMaxK; ++j) {
       sel_e[j] = 0;
-      sel_v[j] = 0.f;
+      sel_b[j] = 0.f;
       if (j < k) {
-        float bv = -INFINITY;
+        float bv = -INFINITY, bb = 0.f;
         int be = E;  // sentinel: larger than any valid index
 #pragma unroll
         for (int q = 0; q < EPL; ++q) {
           const int e = lane + 32 * q;
-          if (e < E && !((taken >> q) & 1u) && (v[q] > bv || (v[q] == bv && e < be))) {
-            bv = v[q];
+          if (e < E && !((taken >> q) & 1u) && (sc[q] > bv || (sc[q] == bv && e < be))) {
+            bv = sc[q];
             be = e;
+            bb = clean_base ? v[q] : sc[q];
           }
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
           const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
           const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+          const float ob = __shfl_xor_sync(0xffffffffu, bb, o);
           if (ov > bv || (ov == bv && oe < be)) {
             bv = ov;
             be = oe;
+            bb = ob;
           }
         }
-        if (be >= E) be = 0;  // only reachable with NaN logits, already flagged
+        if (be >= E) be = 0;  // only reachable with NaN scores, already flagged
         if ((be & 31) == lane) taken |= 1u << (be >> 5);
         sel_e[j] = be;
-        sel_v[j] = bv;
+        sel_b[j] = bb;
       }
     }
 
     // gate weights of the kept experts
+    float bmax = sel_b[0];
+#pragma unroll
+    for (int j = 1; j < kMaxK; ++j)
+      if (j < k) bmax = fmaxf(bmax, sel_b[j]);
     float w[kMaxK];
     float den = 0.f;
 #pragma unroll
     for (int j = 0; j < kMaxK; ++j) {
       w[j] = 0.f;
       if (j < k) {
-        // mode 0: softmax over the kept logits, shifted by the largest (slot 0);
-        // mode 1: the full-softmax probability p_j = exp(l_j - m) / s.
-        w[j] = (gate == 0) ? expf(sel_v[j] - sel_v[0]) : expf(sel_v[j] - m) / s;
+        // mode 0: softmax over the kept logits, shifted by the largest kept one;
+        // mode 1: the full-softmax probability p_j = exp(b_j - m) / s.
+        w[j] = (gate == 0) ? expf(sel_b[j] - bmax) : expf(sel_b[j] - m) / s;
         den += w[j];
       }
     }
@@ -291,16 +350,17 @@ __global__ void __launch_bounds__(kMaxExperts)
 }  // namespace
 
 cudaError_t launch_route_topk(const float* src, int nsplit, int64_t split_stride,
-                              const float* bias, float* logits_out, int64_t T, int E, int k,
-                              int gate, int32_t* topk_idx, float* topk_w, int32_t* hist,
-                              float* psum, int* flags, cudaStream_t stream) {
+                              const float* bias, const float* noise, int noise_mode,
+                              float* logits_out, int64_t T, int E, int k, int gate,
+                              int32_t* topk_idx, float* topk_w, int32_t* hist, float* psum,
+                              int* flags, cudaStream_t stream) {
   const int64_t nchunks = (T + kChunk - 1) / kChunk;
   if (nchunks == 0) return cudaSuccess;
   const dim3 grid(static_cast<unsigned>(nchunks)), block(kRouteWarps * 32);
-#define MOE_TOPK_LAUNCH(EPL)                                                                  \
-  route_topk_kernel<EPL><<<grid, block, 0, stream>>>(src, nsplit, split_stride, bias, logits_out, \
-                                                     T, E, k, gate, topk_idx, topk_w, hist, psum, \
-                                                     flags)
+#define MOE_TOPK_LAUNCH(EPL)                                                                   \
+  route_topk_kernel<EPL><<<grid, block, 0, stream>>>(src, nsplit, split_stride, bias, noise,   \
+                                                     noise_mode, logits_out, T, E, k, gate,    \
+                                                     topk_idx, topk_w, hist, psum, flags)
   if (E <= 32)
     MOE_TOPK_LAUNCH(1);
   else if (E <= 64)

@@ -52,9 +52,10 @@ def test_library_exports_every_declared_symbol(L):
 
 
 def test_struct_layouts_match_header():
-    assert ctypes.sizeof(moe.MoeConfig) == 40
+    assert ctypes.sizeof(moe.MoeConfig) == 48
+    assert moe.MoeConfig.noise.offset == 40
     assert moe.MoeConfig.capacity_factor.offset == 32
-    assert ctypes.sizeof(moe.MoeForwardArgs) == 19 * 8
+    assert ctypes.sizeof(moe.MoeForwardArgs) == 20 * 8
 
 
 def test_status_strings(L):
@@ -76,15 +77,17 @@ def test_status_strings(L):
     (dict(dtype=7), moe.MOE_ERR_INVALID_ARGUMENT),
     (dict(gate=2), moe.MOE_ERR_INVALID_ARGUMENT),
     (dict(capacity_factor=float("nan")), moe.MOE_ERR_INVALID_ARGUMENT),
+    (dict(noise=4), moe.MOE_ERR_INVALID_ARGUMENT),
+    (dict(noise=-1), moe.MOE_ERR_INVALID_ARGUMENT),
 ])
 def test_config_validation(L, kw, status):
-    base = dict(T=64, d=64, h=128, E=8, k=2, dtype=1, gate=0, capacity_factor=0.0)
+    base = dict(T=64, d=64, h=128, E=8, k=2, dtype=1, gate=0, capacity_factor=0.0, noise=0)
     base.update(kw)
     cfg = moe.MoeConfig(base["T"], base["d"], base["h"], base["E"], base["k"], base["dtype"],
-                        base["gate"], base["capacity_factor"])
+                        base["gate"], base["capacity_factor"], base["noise"])
     n = ctypes.c_size_t()
     assert L.moe_workspace_size(ctypes.byref(cfg), ctypes.byref(n)) == status
-    assert L.moe_route(ctypes.byref(cfg), FAKE, FAKE, None, None, FAKE, FAKE, None, None, None, FAKE, 1 << 40, None) == status
+    assert L.moe_route(ctypes.byref(cfg), FAKE, FAKE, None, None, None, FAKE, FAKE, None, None, None, FAKE, 1 << 40, None) == status
 
 
 def test_null_config_and_outputs(L):
@@ -115,9 +118,9 @@ def test_required_pointers_and_alignment(L):
     big = 1 << 40
     INV = moe.MOE_ERR_INVALID_ARGUMENT
     # moe_route: x, w_gate, topk_idx, topk_w required; x 16-byte aligned
-    assert L.moe_route(ctypes.byref(cfg), None, FAKE, None, None, FAKE, FAKE, None, None, None, FAKE, big, None) == INV
-    assert L.moe_route(ctypes.byref(cfg), FAKE_ODD, FAKE, None, None, FAKE, FAKE, None, None, None, FAKE, big, None) == INV
-    assert L.moe_route(ctypes.byref(cfg), FAKE, FAKE, None, None, None, FAKE, None, None, None, FAKE, big, None) == INV
+    assert L.moe_route(ctypes.byref(cfg), None, FAKE, None, None, None, FAKE, FAKE, None, None, None, FAKE, big, None) == INV
+    assert L.moe_route(ctypes.byref(cfg), FAKE_ODD, FAKE, None, None, None, FAKE, FAKE, None, None, None, FAKE, big, None) == INV
+    assert L.moe_route(ctypes.byref(cfg), FAKE, FAKE, None, None, None, None, FAKE, None, None, None, FAKE, big, None) == INV
     # moe_dispatch: x_perm required
     assert L.moe_dispatch(ctypes.byref(cfg), FAKE, FAKE, FAKE, None, FAKE, FAKE, None, None, FAKE, big, None) == INV
     # moe_expert_ffn: w1 required, b1 optional but aligned
@@ -131,8 +134,8 @@ def test_workspace_too_small_is_rejected_before_launch(L):
     cfg = moe.config(64, 64, 128, 8, 2)
     stage, full = _ws(cfg)
     WS = moe.MOE_ERR_WORKSPACE
-    assert L.moe_route(ctypes.byref(cfg), FAKE, FAKE, None, None, FAKE, FAKE, None, None, None, FAKE, stage - 1, None) == WS
-    assert L.moe_route(ctypes.byref(cfg), FAKE, FAKE, None, None, FAKE, FAKE, None, None, None, None, stage, None) == WS
+    assert L.moe_route(ctypes.byref(cfg), FAKE, FAKE, None, None, None, FAKE, FAKE, None, None, None, FAKE, stage - 1, None) == WS
+    assert L.moe_route(ctypes.byref(cfg), FAKE, FAKE, None, None, None, FAKE, FAKE, None, None, None, None, stage, None) == WS
     assert L.moe_dispatch(ctypes.byref(cfg), FAKE, FAKE, FAKE, None, FAKE, FAKE, None, FAKE, FAKE, stage - 1, None) == WS
     assert L.moe_expert_ffn(ctypes.byref(cfg), FAKE, FAKE, FAKE, None, FAKE, None, FAKE, FAKE, FAKE, 16, None) == WS
     assert L.moe_combine(ctypes.byref(cfg), FAKE, FAKE, FAKE, FAKE, FAKE, 0, None) == WS
@@ -146,6 +149,15 @@ def test_workspace_too_small_is_rejected_before_launch(L):
 def test_capacity_matches_oracle(L, T, E, cf):
     cfg = moe.config(T, 64, 64, E, 1, "bf16", 1, cf)
     assert moe.moe_capacity(cfg) == oracle.capacity(T, E, cf if cf > 0 else None)
+
+
+def test_noise_input_required_when_noise_is_on(L):
+    cfg = moe.config(64, 64, 128, 8, 2, noise=moe.MOE_NOISE_GUMBEL)
+    assert L.moe_route(ctypes.byref(cfg), FAKE, FAKE, None, None, None, FAKE, FAKE, None, None,
+                       None, FAKE, 1 << 40, None) == moe.MOE_ERR_INVALID_ARGUMENT
+    args = moe.MoeForwardArgs(x=FAKE, w_gate=FAKE, w1=FAKE, w2=FAKE, y=FAKE)
+    assert L.moe_forward(ctypes.byref(cfg), ctypes.byref(args), FAKE, 1 << 40,
+                         None) == moe.MOE_ERR_INVALID_ARGUMENT
 
 
 def test_selftest_validation_before_launch(L):

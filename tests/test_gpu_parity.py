@@ -29,7 +29,7 @@ def _built():
     moe.lib()
 
 
-def check_routing_exact(g, ref):
+def check_routing_exact(g, ref, tol_w=tl.TOL_W):
     np.testing.assert_array_equal(g["topk_idx"], ref["idx"])
     np.testing.assert_array_equal(g["counts"], ref["counts"])
     np.testing.assert_array_equal(g["kept_counts"], ref["kept"])
@@ -37,7 +37,7 @@ def check_routing_exact(g, ref):
     np.testing.assert_array_equal(g["slot_row"], ref["slot_row"])
     np.testing.assert_array_equal(g["row_token"], ref["row_token"])
     assert int(g["dropped"][0]) == ref["dropped"]
-    assert float(np.abs(g["topk_w"] - ref["w"]).max()) <= tl.TOL_W
+    assert float(np.abs(g["topk_w"] - ref["w"]).max()) <= tol_w
     assert abs(float(g["aux_loss"][0]) - ref["aux"]) <= tl.TOL_AUX * abs(ref["aux"])
     st = oracle.routing_stats(ref["counts"])
     np.testing.assert_allclose(g["routing_stats"], st, rtol=tl.TOL_STATS, atol=1e-7)
@@ -130,6 +130,43 @@ def test_stage_calls_match_forward(name):
     M = int(offsets[-1])
     rt = row_token[:M].long()
     assert torch.equal(x_perm[:M], dev["x"][rt])
+
+
+def _noise_draws(mode, T, E, seed):
+    g = torch.Generator().manual_seed(seed)
+    if mode == moe.MOE_NOISE_GUMBEL:
+        return torch.rand((T, E), generator=g)                 # uniform draws
+    if mode == moe.MOE_NOISE_PROB_GAUSS:
+        return 0.1 * torch.randn((T, E), generator=g)          # 0.1 * N(0, 1) on probabilities
+    return torch.randn((T, E), generator=g)                    # unit amplitude * N(0, 1)
+
+
+@pytest.mark.parametrize("noise_mode", [moe.MOE_NOISE_GUMBEL, moe.MOE_NOISE_PROB_GAUSS,
+                                        moe.MOE_NOISE_LOGIT_SOFTMAX])
+@pytest.mark.parametrize("name", ["tiny_f32", "mixtral_prefill", "switch_capacity", "deepseek_fine"])
+def test_noisy_routing_parity(name, noise_mode):
+    """Routing noise: the GPU's selection scores match the oracle's (same draws); top-k,
+    counts, capacity and placement follow the GPU's scores bit-exactly; y matches."""
+    w = PARITY_WORKLOADS[name]
+    cf = capacity_factor_or_none(w)
+    inp = make_inputs(w, seed=0)
+    inp["noise"] = _noise_draws(noise_mode, w.T, w.E, 100 + noise_mode)
+    cfg = moe.config_from_workload(w, noise=noise_mode)
+    r = tl.run_forward(w, tl.to_device(inp), cfg=cfg)
+    assert r["flags"] == 0
+    g = tl.host(r["outs"])
+    lg_ref = oracle.logits(inp["x"], inp["w_gate"], inp["logit_bias"])
+    sc_ref = oracle.noisy_scores(lg_ref, inp["noise"].numpy(), noise_mode)
+    assert float(np.abs(g["logits"] - sc_ref).max()) <= tl.logits_tol(sc_ref)
+    ref = oracle.noisy_routed_reference(w.k, w.gate, cf, g["logits"], noise_mode, lg_ref)
+    # With noise on the probabilities the weights come from the clean logits, which the
+    # oracle computes itself: allow the fp32 logit error through the softmax.
+    check_routing_exact(g, ref, tl.TOL_W if noise_mode != moe.MOE_NOISE_PROB_GAUSS else 2e-5)
+    y_ref = tl.y_on_routing(inp, ref["idx"], ref["slot_row"], ref["w"])
+    assert tl.max_rel_err(g["y"], y_ref) <= tl.TOL_Y[w.dtype]
+    # the noise actually changed the routing
+    clean = oracle.topk(lg_ref, w.k)
+    assert np.any(clean != g["topk_idx"])
 
 
 @pytest.mark.parametrize("name", ["tiny_f32", "mixtral_prefill", "deepseek_fine"])

@@ -370,3 +370,46 @@ def test_routing_stats_match_library_routines():
 
 def test_routing_stats_empty():
     np.testing.assert_array_equal(oracle.routing_stats(np.zeros(8, np.int64)), 0.0)
+
+
+def test_gumbel_max_samples_the_softmax():
+    """Gumbel-max: argmax_e (l_e + g_e) with g = -log(-log U) is distributed as softmax(l).
+    The oracle's Gumbel transform (with the page's 1e-9 guards) must reproduce it."""
+    rng = np.random.default_rng(0)
+    probs = np.array([0.5, 0.25, 0.15, 0.1])
+    lg = np.tile(np.log(probs), (200000, 1))
+    u = rng.random(lg.shape, dtype=np.float64).astype(np.float32)
+    sc = oracle.noisy_scores(lg, u, oracle.NOISE_GUMBEL)
+    freq = np.bincount(oracle.topk(sc, 1)[:, 0], minlength=4) / lg.shape[0]
+    np.testing.assert_allclose(freq, probs, atol=4e-3)
+
+
+def test_gumbel_closed_form_point():
+    """u = 1/2: g = -log(-log(1/2 + 1e-9) + 1e-9)."""
+    sc = oracle.noisy_scores(np.zeros((1, 2)), np.array([[0.5, 0.5]], np.float32), oracle.NOISE_GUMBEL)
+    g = -math.log(-math.log(0.5 + 1e-9) + 1e-9)
+    np.testing.assert_allclose(sc, g, rtol=1e-14)
+    assert abs(g - (-math.log(math.log(2.0)))) < 1e-8
+
+
+def test_prob_noise_zero_is_softmax_and_large_noise_wins():
+    rng = np.random.default_rng(1)
+    lg = rng.standard_normal((20, 8))
+    sc = oracle.noisy_scores(lg, np.zeros_like(lg, dtype=np.float32), oracle.NOISE_PROB_GAUSS)
+    np.testing.assert_allclose(sc, scipy_softmax(lg, axis=1), rtol=1e-13)
+    n = np.zeros_like(lg, dtype=np.float32)
+    n[:, 5] = 2.0          # any probability plus 2 beats every probability without it
+    assert np.all(oracle.topk(oracle.noisy_scores(lg, n, oracle.NOISE_PROB_GAUSS), 1)[:, 0] == 5)
+
+
+def test_logit_softmax_noise_closed_forms():
+    """Zero draws leave the logits unchanged; with equal logits (p = 1/E) a draw c adds c/E."""
+    rng = np.random.default_rng(2)
+    lg = rng.standard_normal((10, 6))
+    z = oracle.noisy_scores(lg, np.zeros_like(lg, dtype=np.float32), oracle.NOISE_LOGIT_SOFTMAX)
+    np.testing.assert_array_equal(z, lg)
+    eq = np.full((3, 4), 0.7)
+    n = np.array([[0.0, 1.0, 2.0, 3.0]] * 3, np.float32)
+    sc = oracle.noisy_scores(eq, n, oracle.NOISE_LOGIT_SOFTMAX)
+    np.testing.assert_allclose(sc, 0.7 + n.astype(np.float64) / 4.0, rtol=1e-15)
+    assert np.all(oracle.topk(sc, 2) == np.array([3, 2]))
