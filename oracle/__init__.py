@@ -41,6 +41,8 @@ def lib():
         L.orc_aux_loss.restype = _D
         L.orc_routing_stats.argtypes = [_I, _P, _P]
         L.orc_noisy_scores.argtypes = [_I64, _I, _I, _P, _P, _P]
+        L.orc_expert_choice.argtypes = [_I64, _I, _I64, _P, _P, _P]
+        L.orc_combine_expert_choice.argtypes = [_I64, _I, _I, _I64, _P, _P, _P, _P]
         L.orc_capacity.argtypes = [_I64, _I, _D]
         L.orc_capacity.restype = _I64
         L.orc_dispatch.argtypes = [_I64, _I, _I, _I64, _P, _P, _P, _P, _P, _P]
@@ -203,6 +205,44 @@ def dispatch(idx, E, C):
         raise ValueError("expert index out of range")
     return dict(kept=kept, offsets=offsets, slot_row=slot_row, row_token=row_token,
                 dropped=int(dropped[0]))
+
+
+def expert_choice(p, C):
+    """O5e: each expert's C chosen tokens (ascending) and their weights p[t,e]:
+    (sel_token [E,C] int32, sel_w [E,C] float64)."""
+    p = np.ascontiguousarray(p, np.float64)
+    T, E = p.shape
+    tok = np.empty((E, C), np.int32)
+    w = np.empty((E, C), np.float64)
+    lib().orc_expert_choice(T, E, int(C), _ptr(p), _ptr(tok), _ptr(w))
+    return tok, w
+
+
+def combine_expert_choice(T, sel_token, sel_w, z):
+    """O7e: y[T,d] = sum over choosing experts (ascending) of w * z; z is [E*C, d]."""
+    sel_token = np.ascontiguousarray(sel_token, np.int32)
+    sel_w = np.ascontiguousarray(sel_w, np.float64)
+    z = np.ascontiguousarray(z, np.float64)
+    E, C = sel_token.shape
+    d = z.shape[1]
+    y = np.empty((T, d), np.float64)
+    lib().orc_combine_expert_choice(T, d, E, C, _ptr(sel_token), _ptr(sel_w), _ptr(z), _ptr(y))
+    return y
+
+
+def forward_expert_choice(inp, capacity_factor):
+    """Whole expert-choice layer (O1, O2, O5e, O6, O7e) on an input dict."""
+    lg = logits(inp["x"], inp["w_gate"], inp.get("logit_bias"))
+    T, E = lg.shape
+    C = min(T, capacity(T, E, capacity_factor))
+    p = softmax(lg)
+    tok, w = expert_choice(p, C)
+    z = np.zeros((E * C, inp["x"].shape[1]))
+    for e in range(E):
+        if C:
+            z[e * C:(e + 1) * C] = expert_rows(inp["x"][tok[e].tolist()], inp["w1"][e], inp["b1"][e],
+                                               inp["w2"][e], inp["b2"][e])
+    return dict(y=combine_expert_choice(T, tok, w, z), logits=lg, p=p, sel_token=tok, sel_w=w, C=C)
 
 
 def expert_rows(x_rows, w1_e, b1_e, w2_e, b2_e):

@@ -21,13 +21,15 @@
 //
 // Parity status per function (what pins it is listed in the tests):
 //   orc_logits, orc_softmax, orc_topk, orc_gate_weights, orc_aux_loss,
-//   orc_capacity, orc_dispatch, orc_expert_rows, orc_combine, orc_forward and
-//   orc_forward_dense are each pinned by closed forms, invariants, library
-//   routines or brute force in tests/test_oracle_pins.py.
+//   orc_capacity, orc_dispatch, orc_expert_rows, orc_combine, orc_forward,
+//   orc_forward_dense, orc_expert_choice and orc_combine_expert_choice are each
+//   pinned by closed forms, invariants, library routines or brute force in
+//   tests/test_oracle_pins.py.
 
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <algorithm>
 #include <vector>
 
 #ifdef _OPENMP
@@ -292,6 +294,44 @@ int orc_dispatch(int64_t T, int E, int k, int64_t C, const int32_t* idx, int32_t
     }
   if (dropped) *dropped = drop;
   return 0;
+}
+
+// O5e. Expert-choice selection ([P5], section "Expert Choice routing and capacity-factor
+// tuning": the direction of choice is reversed, each expert takes a fixed number of
+// tokens from the batch).  Scores p[T,E]
+// (the full softmax of the router logits); each expert e takes the C tokens with the
+// largest p[t,e], the lower token index winning on equality, and lists them in
+// ascending token order: sel_token[e*C + c], with weight sel_w[e*C + c] = p[t,e].
+// C must be in [0, T].
+void orc_expert_choice(int64_t T, int E, int64_t C, const double* p, int32_t* sel_token,
+                       double* sel_w) {
+  std::vector<int64_t> order(T);
+  for (int e = 0; e < E; ++e) {
+    for (int64_t t = 0; t < T; ++t) order[t] = t;
+    std::stable_sort(order.begin(), order.end(), [&](int64_t a, int64_t b) {
+      return p[a * E + e] > p[b * E + e];  // stable: equal scores keep token order
+    });
+    std::vector<int64_t> chosen(order.begin(), order.begin() + C);
+    std::sort(chosen.begin(), chosen.end());
+    for (int64_t c = 0; c < C; ++c) {
+      sel_token[e * C + c] = (int32_t)chosen[c];
+      sel_w[e * C + c] = p[chosen[c] * E + e];
+    }
+  }
+}
+
+// O7e. Expert-choice combine: y_t = sum over experts e (ascending) that chose t of
+// w(t,e) * z(t,e), where z holds each expert's output for each of its chosen rows
+// (z[(e*C + c)*d]).  Tokens no expert chose get y = 0.
+void orc_combine_expert_choice(int64_t T, int d, int E, int64_t C, const int32_t* sel_token,
+                               const double* sel_w, const double* z, double* y) {
+  for (int64_t i = 0; i < T * d; ++i) y[i] = 0.0;
+  for (int e = 0; e < E; ++e)
+    for (int64_t c = 0; c < C; ++c) {
+      const int64_t t = sel_token[e * C + c];
+      const double* zz = z + (e * C + c) * (int64_t)d;
+      for (int o = 0; o < d; ++o) y[t * d + o] += sel_w[e * C + c] * zz[o];
+    }
 }
 
 // O6. One expert on n token rows ([P5] Expert: w2(silu(w1(x))) with nn.Linear

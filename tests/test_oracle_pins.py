@@ -413,3 +413,45 @@ def test_logit_softmax_noise_closed_forms():
     sc = oracle.noisy_scores(eq, n, oracle.NOISE_LOGIT_SOFTMAX)
     np.testing.assert_allclose(sc, 0.7 + n.astype(np.float64) / 4.0, rtol=1e-15)
     assert np.all(oracle.topk(sc, 2) == np.array([3, 2]))
+
+
+@pytest.mark.parametrize("T,E,C", [(50, 4, 13), (64, 8, 1), (7, 3, 7), (100, 16, 0)])
+def test_expert_choice_matches_rank_brute_force(T, E, C):
+    """Token t is chosen by expert e iff fewer than C tokens rank above it in column e,
+    where t' ranks above t when p[t',e] > p[t,e], or they are equal and t' < t."""
+    rng = np.random.default_rng(T + E)
+    p = oracle.softmax(np.round(rng.standard_normal((T, E)), 1))   # rounding forces ties
+    tok, w = oracle.expert_choice(p, C)
+    for e in range(E):
+        above = [sum(1 for q in range(T) if p[q, e] > p[t, e] or (p[q, e] == p[t, e] and q < t))
+                 for t in range(T)]
+        chosen = [t for t in range(T) if above[t] < C]
+        assert tok[e].tolist() == chosen                 # exactly C, ascending token order
+        np.testing.assert_array_equal(w[e], p[chosen, e])
+
+
+def test_expert_choice_full_capacity_is_the_dense_mixture():
+    """With C = T every expert takes every token, so the layer is the softmax-weighted
+    mixture of all experts: y_t = sum_e softmax(l_t)_e E_e(x_t)."""
+    w = Workload("ec", T=12, d=8, h=12, E=4, k=1, dtype="f32", gate=1, capacity_factor=4.0,
+                 bias_std=0.1)
+    inp = make_inputs(w, seed=6)
+    out = oracle.forward_expert_choice(inp, 4.0)           # C = ceil(12 * 4 / 4) = 12 = T
+    assert out["C"] == 12
+    p = scipy_softmax(inp["x"].double().numpy() @ inp["w_gate"].double().numpy().T, axis=1)
+    dense = np.zeros((12, 8))
+    for e in range(4):
+        dense += p[:, e:e + 1] * oracle.expert_rows(inp["x"], inp["w1"][e], inp["b1"][e],
+                                                    inp["w2"][e], inp["b2"][e])
+    np.testing.assert_allclose(out["y"], dense, rtol=1e-12, atol=1e-13)
+
+
+def test_expert_choice_unchosen_tokens_get_zero():
+    """C = 1 with 8 experts and 40 tokens: at most 8 tokens are chosen, the rest get 0."""
+    w = Workload("ec1", T=40, d=8, h=8, E=8, k=1, dtype="f32", gate=1, capacity_factor=0.2)
+    inp = make_inputs(w, seed=7)
+    out = oracle.forward_expert_choice(inp, 0.2)           # C = ceil(40 * 0.2 / 8) = 1
+    assert out["C"] == 1
+    chosen = set(out["sel_token"].ravel().tolist())
+    for t in range(40):
+        assert np.any(out["y"][t] != 0.0) == (t in chosen)
