@@ -48,6 +48,7 @@ UNIT = "tokens/s"
 DEFAULT_WORKLOAD = "mixtral_prefill"
 L2_FLUSH_BYTES = 256 << 20
 KERNELS_PER_FORWARD = 8   # router GEMM, softmax/top-k, finalize/scan, place, gather, GEMM1, GEMM2, combine
+KERNELS_PER_EC_FORWARD = 7  # router GEMM, softmax, per-expert select, gather, GEMM1, GEMM2, combine
 
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the grouped GEMM pair
 # (G1 + G2), from the ncu capture summarised in profiles/traffic_ffn_mixtral_prefill.md.
@@ -189,6 +190,40 @@ def oracle_tokens_step(w, host, fetch, tokens):
     return spent
 
 
+def oracle_ec_tokens_step(w, host, fetch, tokens):
+    """The oracle's expert-choice layer on the given tokens as a batch of their own
+    (C from the batch size).  Returns the seconds spent inside oracle calls."""
+    import oracle
+
+    xs = host["x"][torch.as_tensor(tokens)]
+    spent = 0.0
+    t = time.perf_counter()
+    lg = oracle.logits(xs, host["w_gate"], host["logit_bias"])
+    p = oracle.softmax(lg)
+    C = min(len(tokens), oracle.capacity(len(tokens), w.E, w.capacity_factor))
+    sel, sel_w = oracle.expert_choice(p, C)
+    spent += time.perf_counter() - t
+    z = np.zeros((w.E * C, w.d))
+    for e in range(w.E):
+        if C == 0:
+            break
+        w1, b1, w2, b2 = fetch(e)
+        rows = xs[sel[e].tolist()]
+        t = time.perf_counter()
+        z[e * C:(e + 1) * C] = oracle.expert_rows(rows, w1, b1, w2, b2)
+        spent += time.perf_counter() - t
+    t = time.perf_counter()
+    oracle.combine_expert_choice(len(tokens), sel, sel_w, z)
+    spent += time.perf_counter() - t
+    return spent
+
+
+def tokens_step(w, host, fetch, tokens):
+    if w.routing == "expert_choice":
+        return oracle_ec_tokens_step(w, host, fetch, tokens)
+    return oracle_tokens_step(w, host, fetch, tokens)
+
+
 def host_view(inp):
     host = {"x": inp["x"].cpu(), "w_gate": inp["w_gate"].cpu(),
             "logit_bias": inp["logit_bias"].cpu() if inp["logit_bias"] is not None else None}
@@ -213,7 +248,7 @@ def cpu_baseline(w, inp, budget_s=12.0):
     done, spent, batch = 0, 0.0, 1
     while spent < budget_s and done < w.T:
         toks = list(range(done, min(w.T, done + batch)))
-        spent += oracle_tokens_step(w, host, fetch, toks)
+        spent += tokens_step(w, host, fetch, toks)
         done += len(toks)
         batch = min(batch * 2, 256)
     return dict(value=done / spent, unit=UNIT, cores=oracle.num_threads(), kind="oracle",
@@ -261,21 +296,35 @@ def run_ours(args, world, rank, local):
     inp = make_inputs(w, seed=rank, device=str(dev))
     cfg = moe.config_from_workload(w)
     i32 = dict(dtype=torch.int32, device=dev)
-    outs = dict(y=torch.empty((w.T, w.d), dtype=w.torch_dtype, device=dev),
-                offsets=torch.empty((w.E + 1,), **i32), kept_counts=torch.empty((w.E,), **i32))
-    ws = torch.empty(moe.moe_workspace_size(cfg), dtype=torch.uint8, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    fwd_args = moe.forward_args(inp, outs)
     stream = torch.cuda.current_stream()
+    ec = w.routing == "expert_choice"
+    if ec:
+        C = moe.moe_expert_choice_capacity(cfg)
+        outs = dict(y=torch.empty((w.T, w.d), dtype=w.torch_dtype, device=dev),
+                    sel_token=torch.empty((w.E, C), **i32))
+        ws = torch.empty(moe.moe_expert_choice_workspace_size(cfg), dtype=torch.uint8, device=dev)
+        ec_args = moe.expert_choice_args(inp, outs)
 
-    def step():
-        moe.moe_forward(cfg, inp, outs, ws, stream, args=fwd_args)
+        def step():
+            moe.moe_expert_choice_forward(cfg, inp, outs, ws, stream, args=ec_args)
+    else:
+        outs = dict(y=torch.empty((w.T, w.d), dtype=w.torch_dtype, device=dev),
+                    offsets=torch.empty((w.E + 1,), **i32), kept_counts=torch.empty((w.E,), **i32))
+        ws = torch.empty(moe.moe_workspace_size(cfg), dtype=torch.uint8, device=dev)
+        fwd_args = moe.forward_args(inp, outs)
+
+        def step():
+            moe.moe_forward(cfg, inp, outs, ws, stream, args=fwd_args)
 
     for _ in range(args.warmup):
         step()
     assert moe.moe_device_error(ws) == 0
-    M = int(outs["offsets"][-1])
-    nonempty = int((outs["kept_counts"] > 0).sum())
+    if ec:
+        M, nonempty = w.E * C, (w.E if C > 0 else 0)
+    else:
+        M = int(outs["offsets"][-1])
+        nonempty = int((outs["kept_counts"] > 0).sum())
 
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
@@ -300,25 +349,36 @@ def run_ours(args, world, rank, local):
     assert moe.moe_device_error(ws) == 0
 
     # The grouped expert GEMM pair alone (same rows, same stream), for the roofline.
-    sws = torch.empty(moe.moe_stage_workspace_size(cfg), dtype=torch.uint8, device=dev)
+    # Expert choice: the same moe_expert_ffn call on its E groups of C rows, through a
+    # top-k configuration with capacity C (identical tile height and row count).
+    ffn_cfg = cfg
+    if ec:
+        ffn_cfg = moe.config(w.T, w.d, w.h, w.E, w.k, w.dtype, w.gate, w.capacity_factor)
+        assert moe.moe_capacity(ffn_cfg) == C and M <= w.T * w.k
+    sws = torch.empty(moe.moe_stage_workspace_size(ffn_cfg), dtype=torch.uint8, device=dev)
     rows = w.T * w.k
     x_perm = torch.empty((rows, w.d), dtype=w.torch_dtype, device=dev)
     h_buf = torch.empty((rows, w.h), dtype=w.torch_dtype, device=dev)
     y_perm = torch.empty((rows, w.d), dtype=w.torch_dtype, device=dev)
-    idx = torch.empty((w.T, w.k), **i32)
-    wts = torch.empty((w.T, w.k), dtype=torch.float32, device=dev)
-    slot_row = torch.empty((w.T, w.k), **i32)
-    row_token = torch.empty((rows,), **i32)
     offsets = torch.empty((w.E + 1,), **i32)
-    moe.moe_route(cfg, inp["x"], inp["w_gate"], inp["logit_bias"], None, idx, wts, None, None, sws)
-    moe.moe_dispatch(cfg, inp["x"], idx, offsets, None, slot_row, row_token, None, x_perm, sws)
+    if ec:
+        torch.index_select(inp["x"], 0, outs["sel_token"].flatten().long(), out=x_perm[:M])
+        offsets.copy_(torch.arange(w.E + 1, dtype=torch.int32, device=dev) * C)
+    else:
+        idx = torch.empty((w.T, w.k), **i32)
+        wts = torch.empty((w.T, w.k), dtype=torch.float32, device=dev)
+        slot_row = torch.empty((w.T, w.k), **i32)
+        row_token = torch.empty((rows,), **i32)
+        moe.moe_route(cfg, inp["x"], inp["w_gate"], inp["logit_bias"], None, idx, wts, None, None,
+                      sws)
+        moe.moe_dispatch(cfg, inp["x"], idx, offsets, None, slot_row, row_token, None, x_perm, sws)
     ffn_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(args.steps)]
     for i in range(args.steps + args.warmup):
         flush.zero_()
         if i >= args.warmup:
             ffn_ev[i - args.warmup][0].record(stream)
-        moe.moe_expert_ffn(cfg, x_perm, offsets, inp["w1"], inp["b1"], inp["w2"], inp["b2"],
+        moe.moe_expert_ffn(ffn_cfg, x_perm, offsets, inp["w1"], inp["b1"], inp["w2"], inp["b2"],
                            h_buf, y_perm, sws)
         if i >= args.warmup:
             ffn_ev[i - args.warmup][1].record(stream)
@@ -362,6 +422,7 @@ def run_ours(args, world, rank, local):
         "dtype": w.dtype,
         "data": "synthetic",
         "config": {"workload": w.name, "T": w.T, "d": w.d, "h": w.h, "E": w.E, "k": w.k,
+                   "routing": w.routing,
                    "gate": ["topk_softmax", "softmax_topk_renorm"][w.gate],
                    "capacity_factor": w.capacity_factor, "kept_rows": M,
                    "nonempty_experts": nonempty, "inputs": input_recipe(w),
@@ -371,7 +432,7 @@ def run_ours(args, world, rank, local):
         "e2e": {"value": round(world * w.T / (e2e_ms / 1e3), 1), "unit": UNIT,
                 "h2d_bytes_per_step": x_host.numel() * x_host.element_size(),
                 "d2h_bytes_per_step": y_host.numel() * y_host.element_size()},
-        "gpu_launches": KERNELS_PER_FORWARD * args.steps,
+        "gpu_launches": (KERNELS_PER_EC_FORWARD if ec else KERNELS_PER_FORWARD) * args.steps,
         "clocks": clocks.summary(t0, t1) if clocks else None,
     }
     if world == 1 and not args.no_cpu_baseline:
@@ -391,7 +452,7 @@ def run_reference(args, world, rank, local):
     inp = make_inputs(w, seed=0, device=gen_dev)
     host, fetch = host_view(inp)
     # Size one step's sample from the cost of one token so the whole run stays short.
-    probe = oracle_tokens_step(w, host, fetch, [0])
+    probe = tokens_step(w, host, fetch, [0])
     per_token = max(probe, 1e-4)
     total_steps = args.steps + args.warmup
     target = max(0.05, min(5.0, 150.0 / max(total_steps, 1)))
@@ -400,7 +461,7 @@ def run_reference(args, world, rank, local):
     for i in range(total_steps):
         start = (i * S) % w.T
         toks = [(start + q) % w.T for q in range(S)]
-        t = oracle_tokens_step(w, host, fetch, toks)
+        t = tokens_step(w, host, fetch, toks)
         if i >= args.warmup:
             times.append(t)
     mean_s = statistics.fmean(times) if times else probe
@@ -421,6 +482,7 @@ def run_reference(args, world, rank, local):
         "dtype": "f64",
         "data": "synthetic",
         "config": {"workload": w.name, "T": w.T, "d": w.d, "h": w.h, "E": w.E, "k": w.k,
+                   "routing": w.routing,
                    "gate": ["topk_softmax", "softmax_topk_renorm"][w.gate],
                    "capacity_factor": w.capacity_factor, "inputs": input_recipe(w)},
         "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": oracle.num_threads(),

@@ -231,6 +231,54 @@ moe_status moe_combine(const moe_config* cfg, const void* y_perm, const int32_t*
 moe_status moe_forward(const moe_config* cfg, const moe_forward_args* args, void* ws,
                        size_t ws_bytes, moe_stream_t stream);
 
+/* ---- Expert-choice routing -------------------------------------------------
+   The selection direction reversed (routing-mechanism page, section "Expert Choice
+   routing and capacity-factor tuning"): instead of each token taking k experts,
+   each expert takes a fixed number C of tokens, which balances the load by
+   construction.  With p = softmax(logits) over the experts of each token:
+     C             = min(T, ceil(T * capacity_factor / E))      (capacity rule)
+     expert e takes the C tokens with the largest p[t,e] (equal p: lower t first)
+     y[t,:]        = sum over experts e that took t, in ascending e, of
+                     p[t,e] * E_e(x_t), accumulated in fp32 and rounded once;
+                     a token no expert took gets exactly 0 (it leaves the layer
+                     through the residual path).
+   cfg->k and cfg->gate are not read; cfg->noise must be MOE_NOISE_NONE and
+   cfg->capacity_factor > 0.  Selection is decided on exactly the fp32 p written to
+   `probs`.  Supported range: 1 <= E <= 256, d and h as above, E*C < 2^31.
+   Results are deterministic. */
+typedef struct moe_expert_choice_args {
+  const void* x;            /* [T,d] dtype */
+  const void* w_gate;       /* [E,d] dtype */
+  const float* logit_bias;  /* [E] fp32, or NULL */
+  const void* w1;           /* [E,h,d] dtype */
+  const void* b1;           /* [E,h] dtype, or NULL for zero */
+  const void* w2;           /* [E,d,h] dtype */
+  const void* b2;           /* [E,d] dtype, or NULL for zero */
+  void* y;                  /* [T,d] dtype, required */
+  float* logits;            /* [T,E] fp32, or NULL */
+  float* probs;             /* [T,E] fp32 softmax of the logits, or NULL */
+  int32_t* sel_token;       /* [E,C]: expert e's chosen tokens, ascending, or NULL */
+  float* sel_w;             /* [E,C] fp32: p[sel_token, e], or NULL */
+  int32_t* token_experts;   /* [T]: how many experts took each token, or NULL */
+  int32_t* unrouted;        /* [1]: tokens no expert took, or NULL */
+} moe_expert_choice_args;
+
+/* C of the expert-choice layer (above).  Host only. */
+moe_status moe_expert_choice_capacity(const moe_config* cfg, int64_t* capacity);
+
+/* Workspace bytes moe_expert_choice_forward needs: router output, the [E,T]
+   transposed probabilities and row map, and the row buffers [E*C,d] + [E*C,h] +
+   [E*C,d].  Host only. */
+moe_status moe_expert_choice_workspace_size(const moe_config* cfg, size_t* bytes);
+
+/* The expert-choice layer on one stream: router contraction, softmax, per-expert
+   top-C selection, row gather into expert-contiguous order (expert e owns rows
+   [e*C, (e+1)*C)), the expert FFN on those rows (same kernels as moe_expert_ffn)
+   and the per-token combine.  Device flags: MOE_DEVERR_NONFINITE (a non-finite
+   logit), MOE_DEVERR_TIMEOUT (a GEMM wait gave up). */
+moe_status moe_expert_choice_forward(const moe_config* cfg, const moe_expert_choice_args* args,
+                                     void* ws, size_t ws_bytes, moe_stream_t stream);
+
 /* Waits for `stream`, then reads the device flag word at the start of `ws` into
    *flags (may be NULL).  Returns MOE_ERR_DEVICE when any bit is set, MOE_OK
    otherwise, MOE_ERR_CUDA if the wait or the read failed. */

@@ -49,6 +49,7 @@ class Workload:
     bias_std: float = 0.0      # expert biases b1, b2 (0 -> zeros)
     logit_bias: str = "none"   # "none" | "zipf" | "normal1.5"
     wg_std: Optional[float] = None   # default 1/sqrt(d)
+    routing: str = "topk"      # "topk" (tokens choose k experts) | "expert_choice"
 
     @property
     def torch_dtype(self):
@@ -83,6 +84,14 @@ WORKLOADS = {
 WORKLOADS["deepseek_fine_e32"] = WORKLOADS["deepseek_fine"].scaled(name="deepseek_fine_e32",
                                                                   T=1024, E=32)
 
+# Expert-choice routing over the same layer shapes: each expert takes C =
+# ceil(T * capacity_factor / E) tokens.  A capacity factor of k gives the top-k layer's
+# number of expert rows (T*k), so the expert FFN does the same work as its top-k twin.
+WORKLOADS["mixtral_prefill_ec"] = WORKLOADS["mixtral_prefill"].scaled(
+    name="mixtral_prefill_ec", routing="expert_choice", capacity_factor=2.0)
+WORKLOADS["deepseek_fine_ec"] = WORKLOADS["deepseek_fine"].scaled(
+    name="deepseek_fine_ec", routing="expert_choice", capacity_factor=8.0)
+
 # Reduced-size variants with each workload's structure (expert count, k, gate, capacity,
 # bias recipe) that the oracle evaluates in full in seconds, while still spanning several
 # 128-row tiles, several 256-column tiles and a ragged tail.
@@ -92,6 +101,19 @@ PARITY_WORKLOADS = {
     "switch_capacity": WORKLOADS["switch_capacity"].scaled(T=2048, d=256, h=512),
     "deepseek_fine": WORKLOADS["deepseek_fine"].scaled(T=389, d=512, h=256),
     "decode": WORKLOADS["decode"].scaled(d=512, h=768),
+}
+
+# Expert-choice parity cases: several capacities (C from 1 row to every token), both
+# dtypes, 8 to 256 experts, token counts with a ragged tail.
+EC_PARITY_WORKLOADS = {
+    "tiny_f32_ec": WORKLOADS["tiny_f32"].scaled(name="tiny_f32_ec", routing="expert_choice",
+                                                capacity_factor=2.0),
+    "mixtral_prefill_ec": WORKLOADS["mixtral_prefill_ec"].scaled(T=777, d=512, h=1024),
+    "switch_ec": WORKLOADS["switch_capacity"].scaled(name="switch_ec", routing="expert_choice",
+                                                     T=2048, d=256, h=512, capacity_factor=1.25),
+    "deepseek_fine_ec": WORKLOADS["deepseek_fine_ec"].scaled(T=389, d=512, h=256),
+    "decode_ec": WORKLOADS["decode"].scaled(name="decode_ec", routing="expert_choice", d=512,
+                                            h=768, capacity_factor=1.0),
 }
 
 
@@ -156,5 +178,7 @@ def input_recipe(w: Workload) -> str:
     lb = {"none": "no logit bias", "zipf": "logit bias b_e=2.0*ln(1/(e+1)^1.1)",
           "normal1.5": "logit bias ~N(0,1.5) (std sqrt(1.5))"}[w.logit_bias]
     bias = f"biases ~N(0,{w.bias_std**2:g})" if w.bias_std > 0 else "zero biases"
-    return (f"T={w.T} d={w.d} h={w.h} E={w.E} k={w.k} {w.dtype} gate={w.gate} "
-            f"cf={w.capacity_factor:g}; x~N(0,1), weights ~N(0,1/fan_in), {bias}, {lb}")
+    head = (f"T={w.T} d={w.d} h={w.h} E={w.E} k={w.k} {w.dtype} gate={w.gate} "
+            if w.routing == "topk" else
+            f"expert choice T={w.T} d={w.d} h={w.h} E={w.E} {w.dtype} ")
+    return head + f"cf={w.capacity_factor:g}; x~N(0,1), weights ~N(0,1/fan_in), {bias}, {lb}"

@@ -40,7 +40,9 @@ MOE_DEVERR_TIMEOUT = 8
 # Every C symbol include/moe.h declares.
 EXPORTED = ("moe_status_str", "moe_capacity", "moe_workspace_size", "moe_stage_workspace_size",
             "moe_route", "moe_dispatch", "moe_expert_ffn", "moe_combine", "moe_forward",
-            "moe_device_error", "moe_dispatch_static", "moe_selftest_wait_timeout")
+            "moe_device_error", "moe_dispatch_static", "moe_selftest_wait_timeout",
+            "moe_expert_choice_capacity", "moe_expert_choice_workspace_size",
+            "moe_expert_choice_forward")
 
 # Table cells of moe_dispatch_static's library-held scratch (include/moe.h).
 MOE_DISPATCH_STATIC_MAX_CELLS = 262144
@@ -65,6 +67,12 @@ class MoeForwardArgs(ctypes.Structure):
         "topk_w",
         "counts", "aux_loss", "offsets", "kept_counts", "slot_row", "row_token", "dropped",
         "routing_stats")]
+
+
+class MoeExpertChoiceArgs(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in (
+        "x", "w_gate", "logit_bias", "w1", "b1", "w2", "b2", "y", "logits", "probs", "sel_token",
+        "sel_w", "token_experts", "unrouted")]
 
 
 _lib = None
@@ -93,6 +101,9 @@ def lib():
         L.moe_device_error.argtypes = [P, P, ctypes.POINTER(ctypes.c_int32)]
         L.moe_dispatch_static.argtypes = [cfg, P, P, P, P, P, P, P, P, P, P]
         L.moe_selftest_wait_timeout.argtypes = [P, ctypes.c_uint64, P]
+        L.moe_expert_choice_capacity.argtypes = [cfg, ctypes.POINTER(ctypes.c_int64)]
+        L.moe_expert_choice_workspace_size.argtypes = [cfg, ctypes.POINTER(S)]
+        L.moe_expert_choice_forward.argtypes = [cfg, ctypes.POINTER(MoeExpertChoiceArgs), P, S, P]
         for name in EXPORTED:
             if name != "moe_status_str":
                 getattr(L, name).restype = ctypes.c_int
@@ -231,3 +242,41 @@ def moe_selftest_wait_timeout(device_flags, limit_ns: int, stream=None) -> None:
     """Runs the bounded pipeline wait on a barrier nothing completes (see moe.h)."""
     _check(lib().moe_selftest_wait_timeout(_p(device_flags), int(limit_ns), _stream(stream)),
            "moe_selftest_wait_timeout")
+
+
+EC_INPUTS = ("x", "w_gate", "logit_bias", "w1", "b1", "w2", "b2")
+EC_OUTPUTS = ("y", "logits", "probs", "sel_token", "sel_w", "token_experts", "unrouted")
+
+
+def moe_expert_choice_capacity(cfg: MoeConfig) -> int:
+    v = ctypes.c_int64()
+    _check(lib().moe_expert_choice_capacity(ctypes.byref(cfg), ctypes.byref(v)),
+           "moe_expert_choice_capacity")
+    return v.value
+
+
+def moe_expert_choice_workspace_size(cfg: MoeConfig) -> int:
+    v = ctypes.c_size_t()
+    _check(lib().moe_expert_choice_workspace_size(ctypes.byref(cfg), ctypes.byref(v)),
+           "moe_expert_choice_workspace_size")
+    return v.value
+
+
+def expert_choice_args(inputs: dict, outputs: dict) -> MoeExpertChoiceArgs:
+    """Build the moe_expert_choice_args struct (missing keys -> NULL)."""
+    a = MoeExpertChoiceArgs()
+    for n in EC_INPUTS:
+        setattr(a, n, _p(inputs.get(n)))
+    for n in EC_OUTPUTS:
+        setattr(a, n, _p(outputs.get(n)))
+    return a
+
+
+def moe_expert_choice_forward(cfg, inputs: dict, outputs: dict, ws, stream=None,
+                              args: MoeExpertChoiceArgs = None):
+    """The expert-choice layer: each expert takes its C highest-probability tokens."""
+    if args is None:
+        args = expert_choice_args(inputs, outputs)
+    _check(lib().moe_expert_choice_forward(ctypes.byref(cfg), ctypes.byref(args), _p(ws),
+                                           ws.numel() * ws.element_size(), _stream(stream)),
+           "moe_expert_choice_forward")

@@ -85,7 +85,82 @@ __global__ void __launch_bounds__(kThreads)
   Vec<T>::store(y + t * d + v * V, acc);
 }
 
+// Expert-choice combine ("Expert Choice routing and capacity-factor tuning" section
+// of the same page): y[t] = sum over the experts e that took t, in ascending e, of
+// p[t,e] * y_perm[e*C + c]; a token no expert took gets 0.  One CTA per token: thread
+// e reads the [E,T] row map, the chosen experts are compacted in expert order into
+// shared memory, then the CTA's threads stride over the 16-byte column vectors.
+constexpr int kEcThreads = kMaxExperts;
+
+template <typename T>
+__global__ void __launch_bounds__(kEcThreads)
+    ec_combine_kernel(const T* __restrict__ y_perm, const int32_t* __restrict__ rowmap_et,
+                      const float* __restrict__ probs_et, int64_t ntok, int E, int64_t C, int d,
+                      T* __restrict__ y, int32_t* __restrict__ token_experts,
+                      int32_t* __restrict__ unrouted) {
+  constexpr int V = Vec<T>::N;
+  __shared__ int64_t s_row[kMaxExperts];
+  __shared__ float s_w[kMaxExperts];
+  __shared__ int s_cnt[kEcThreads / 32];
+  const int64_t t = blockIdx.x;
+  const int e = threadIdx.x, lane = e & 31, warp = e >> 5;
+  int c = -1;
+  float w = 0.f;
+  if (e < E) {
+    c = rowmap_et[static_cast<int64_t>(e) * ntok + t];
+    if (c >= 0) w = probs_et[static_cast<int64_t>(e) * ntok + t];
+  }
+  const unsigned b = __ballot_sync(0xffffffffu, c >= 0);
+  if (lane == 0) s_cnt[warp] = __popc(b);
+  __syncthreads();
+  int before = 0, n = 0;
+#pragma unroll
+  for (int i = 0; i < kEcThreads / 32; ++i) {
+    before += (i < warp) ? s_cnt[i] : 0;
+    n += s_cnt[i];
+  }
+  if (c >= 0) {
+    const int pos = before + __popc(b & ((1u << lane) - 1u));
+    s_row[pos] = static_cast<int64_t>(e) * C + c;
+    s_w[pos] = w;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    if (token_experts) token_experts[t] = n;
+    if (n == 0 && unrouted) atomicAdd(unrouted, 1);
+  }
+  const int nvec = d / V;
+  for (int v = threadIdx.x; v < nvec; v += kEcThreads) {
+    float acc[V];
+#pragma unroll
+    for (int i = 0; i < V; ++i) acc[i] = 0.f;
+    for (int j = 0; j < n; ++j) {
+      float val[V];
+      Vec<T>::load(y_perm + s_row[j] * d + v * V, val);
+#pragma unroll
+      for (int i = 0; i < V; ++i) acc[i] = fmaf(s_w[j], val[i], acc[i]);
+    }
+    Vec<T>::store(y + t * d + v * V, acc);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_ec_combine(int dtype, const void* y_perm, const int32_t* rowmap_et,
+                              const float* probs_et, int64_t T, int E, int64_t C, int d, void* y,
+                              int32_t* token_experts, int32_t* unrouted, cudaStream_t stream) {
+  if (T == 0) return cudaSuccess;
+  const dim3 grid(static_cast<unsigned>(T));
+  if (dtype == MOE_F32)
+    ec_combine_kernel<float><<<grid, kEcThreads, 0, stream>>>(
+        static_cast<const float*>(y_perm), rowmap_et, probs_et, T, E, C, d,
+        static_cast<float*>(y), token_experts, unrouted);
+  else
+    ec_combine_kernel<__nv_bfloat16><<<grid, kEcThreads, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(y_perm), rowmap_et, probs_et, T, E, C, d,
+        static_cast<__nv_bfloat16*>(y), token_experts, unrouted);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_combine(int dtype, const void* y_perm, const int32_t* slot_row,
                            const float* topk_w, int64_t T, int d, int k, void* y, int* flags,

@@ -131,8 +131,14 @@ cudaError_t launch_dispatch_place(int dtype, const int32_t* topk_idx, int64_t T,
       topk_idx, T, E, k, C, chunk_base, offsets, slot_row, row_token, flags);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  return launch_gather_rows(dtype, row_token, offsets, E, x, x_perm, d, T * k, stream);
+}
+
+cudaError_t launch_gather_rows(int dtype, const int32_t* row_token, const int32_t* offsets, int E,
+                               const void* x, void* x_perm, int d, int64_t rows,
+                               cudaStream_t stream) {
+  if (rows == 0) return cudaSuccess;
   // Enough warps for every possible row, capped; the kernel strides over the rest.
-  const int64_t rows = T * k;
   const unsigned grid =
       static_cast<unsigned>(std::min<int64_t>((rows + kThreads / 32 - 1) / (kThreads / 32), 4096));
   if (dtype == MOE_F32)

@@ -38,6 +38,30 @@ cudaError_t launch_dispatch_place(int dtype, const int32_t* topk_idx, int64_t T,
                                   int32_t* slot_row, int32_t* row_token, const void* x,
                                   void* x_perm, int d, int* flags, cudaStream_t stream);
 
+// D3 alone: x_perm[r] = x[row_token[r]] for r < offsets[E]; `rows` bounds offsets[E].
+cudaError_t launch_gather_rows(int dtype, const int32_t* row_token, const int32_t* offsets, int E,
+                               const void* x, void* x_perm, int d, int64_t rows,
+                               cudaStream_t stream);
+
+// EC1: logits l (split partials added in order, then the bias), p = softmax(l) per
+// token; writes logits_out / probs_out [T,E] when given and probs_et [E,T] always.
+cudaError_t launch_ec_softmax(const float* src, int nsplit, int64_t split_stride,
+                              const float* bias, float* logits_out, float* probs_out,
+                              float* probs_et, int64_t T, int E, int* flags, cudaStream_t stream);
+
+// EC2: per expert e, its C largest p[., e] (lower token first on equal values) in
+// ascending token order: sel_token / sel_w [E,C]; rowmap_et[e,t] = position c or -1;
+// offsets[e] = e*C.  Requires C <= T.
+cudaError_t launch_ec_select(const float* probs_et, int64_t T, int E, int64_t C,
+                             int32_t* sel_token, float* sel_w, int32_t* rowmap_et,
+                             int32_t* offsets, cudaStream_t stream);
+
+// EC3: y[t] = sum over experts e with rowmap_et[e,t] = c >= 0, ascending e, of
+// probs_et[e,t] * y_perm[e*C + c]; token_experts[t] and unrouted (both optional).
+cudaError_t launch_ec_combine(int dtype, const void* y_perm, const int32_t* rowmap_et,
+                              const float* probs_et, int64_t T, int E, int64_t C, int d, void* y,
+                              int32_t* token_experts, int32_t* unrouted, cudaStream_t stream);
+
 // C1: y[t] = sum_j w[t,j] * y_perm[slot_row[t,j]] in slot order.
 cudaError_t launch_combine(int dtype, const void* y_perm, const int32_t* slot_row,
                            const float* topk_w, int64_t T, int d, int k, void* y, int* flags,

@@ -163,13 +163,15 @@ moe_status run_router(const moe_config& c, const Layout& L, void* ws, const void
   return MOE_OK;
 }
 
-// G1 + G2 over the expert-contiguous rows.
-moe_status run_expert_ffn(const moe_config& c, const void* x_perm, const int32_t* offsets,
-                          const void* w1, const void* b1, const void* w2, const void* b2,
-                          void* h_buf, void* y_perm, int* flags, int sms, cudaStream_t st) {
+// G1 + G2 over the expert-contiguous rows: `rows_alloc` rows in the buffers, no
+// expert with more than `max_group` rows.
+moe_status run_expert_ffn_rows(const moe_config& c, int64_t rows_alloc, int64_t max_group,
+                               const void* x_perm, const int32_t* offsets, const void* w1,
+                               const void* b1, const void* w2, const void* b2, void* h_buf,
+                               void* y_perm, int* flags, int sms, cudaStream_t st) {
   GemmArgs g1{};
   g1.A = x_perm;
-  g1.rows_alloc = c.T * c.k;
+  g1.rows_alloc = rows_alloc;
   g1.B = w1;
   g1.bias = b1;
   g1.out = h_buf;
@@ -177,10 +179,7 @@ moe_status run_expert_ffn(const moe_config& c, const void* x_perm, const int32_t
   g1.G = c.E;
   g1.N = c.h;
   g1.K = c.d;
-  // A valid routing gives an expert at most T rows (one per token), and at most C
-  // with a capacity; the tile height follows this bound.
-  const int64_t C = capacity_of(c);
-  g1.max_group = static_cast<int>(C >= 0 && C < c.T ? C : c.T);
+  g1.max_group = static_cast<int>(max_group);
   g1.flags = flags;
   GemmArgs g2 = g1;
   g2.A = h_buf;
@@ -197,6 +196,66 @@ moe_status run_expert_ffn(const moe_config& c, const void* x_perm, const int32_t
     MOE_CUDA(launch_tc_gemm_bf16(g2, EPI_BIAS, sms, st));
   }
   return MOE_OK;
+}
+
+// Top-k routing: a valid routing gives an expert at most T rows (one per token), and
+// at most C with a capacity; the tile height follows this bound.
+moe_status run_expert_ffn(const moe_config& c, const void* x_perm, const int32_t* offsets,
+                          const void* w1, const void* b1, const void* w2, const void* b2,
+                          void* h_buf, void* y_perm, int* flags, int sms, cudaStream_t st) {
+  const int64_t C = capacity_of(c);
+  return run_expert_ffn_rows(c, c.T * c.k, C >= 0 && C < c.T ? C : c.T, x_perm, offsets, w1, b1,
+                             w2, b2, h_buf, y_perm, flags, sms, st);
+}
+
+// ---------------------------------------------------------------- expert choice
+// Workspace: [flags | router output | probs [E,T] | row map [E,T] | offsets |
+// sel_token | sel_w | token rows x_perm, h_buf, y_perm of E*C rows].
+struct EcLayout {
+  size_t flags, logits, probs_et, rowmap, offsets, sel_token, sel_w, x_perm, h_buf, y_perm, total;
+  int64_t C;
+};
+
+int64_t ec_capacity_of(const moe_config& c) {
+  const int64_t C = static_cast<int64_t>(
+      std::ceil(static_cast<double>(c.T) * c.capacity_factor / static_cast<double>(c.E)));
+  return C < c.T ? C : c.T;
+}
+
+moe_status check_ec_config(const moe_config* c) {
+  if (!c) return MOE_ERR_INVALID_ARGUMENT;
+  if (c->dtype != MOE_F32 && c->dtype != MOE_BF16) return MOE_ERR_INVALID_ARGUMENT;
+  if (!std::isfinite(c->capacity_factor) || !(c->capacity_factor > 0.0))
+    return MOE_ERR_INVALID_ARGUMENT;
+  if (c->noise != MOE_NOISE_NONE) return MOE_ERR_INVALID_ARGUMENT;
+  if (c->T < 0 || c->T >= (int64_t{1} << 31) || c->E < 1 || c->E > kMaxExperts)
+    return MOE_ERR_UNSUPPORTED;
+  if (c->d < 8 || c->d % 8 != 0 || c->h < 8 || c->h % 8 != 0) return MOE_ERR_UNSUPPORTED;
+  if (ec_capacity_of(*c) * c->E >= (int64_t{1} << 31)) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+EcLayout make_ec_layout(const moe_config& c) {
+  EcLayout L{};
+  const int64_t T = c.T, E = c.E;
+  const size_t s = c.dtype == MOE_F32 ? 4 : 2;
+  L.C = ec_capacity_of(c);
+  const int64_t rows = E * L.C;
+  size_t o = 0;
+  L.flags = o; o += kAlign;
+  const int64_t splits =
+      c.dtype == MOE_BF16 ? router_splits(c.T, c.E, c.d, kMaxSmsForSizing) : 1;
+  L.logits = o; o = align_up(o + splits * T * E * 4);
+  L.probs_et = o; o = align_up(o + T * E * 4);
+  L.rowmap = o; o = align_up(o + T * E * 4);
+  L.offsets = o; o = align_up(o + (E + 1) * 4);
+  L.sel_token = o; o = align_up(o + rows * 4);
+  L.sel_w = o; o = align_up(o + rows * 4);
+  L.x_perm = o; o = align_up(o + rows * c.d * s);
+  L.h_buf = o; o = align_up(o + rows * c.h * s);
+  L.y_perm = o; o = align_up(o + rows * c.d * s);
+  L.total = o;
+  return L;
 }
 
 moe_status zero_async(void* p, size_t bytes, cudaStream_t st) {
@@ -419,4 +478,90 @@ MOE_EXPORT moe_status moe_device_error(const void* ws, moe_stream_t stream, int3
   if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
   if (flags) *flags = v;
   return v ? MOE_ERR_DEVICE : MOE_OK;
+}
+
+MOE_EXPORT moe_status moe_expert_choice_capacity(const moe_config* cfg, int64_t* capacity) {
+  moe_status s = check_ec_config(cfg);
+  if (s != MOE_OK) return s;
+  if (!capacity) return MOE_ERR_INVALID_ARGUMENT;
+  *capacity = ec_capacity_of(*cfg);
+  return MOE_OK;
+}
+
+MOE_EXPORT moe_status moe_expert_choice_workspace_size(const moe_config* cfg, size_t* bytes) {
+  moe_status s = check_ec_config(cfg);
+  if (s != MOE_OK) return s;
+  if (!bytes) return MOE_ERR_INVALID_ARGUMENT;
+  *bytes = make_ec_layout(*cfg).total;
+  return MOE_OK;
+}
+
+MOE_EXPORT moe_status moe_expert_choice_forward(const moe_config* cfg,
+                                                const moe_expert_choice_args* a, void* ws,
+                                                size_t ws_bytes, moe_stream_t stream) {
+  moe_status s = check_ec_config(cfg);
+  if (s != MOE_OK) return s;
+  if (!a) return MOE_ERR_INVALID_ARGUMENT;
+  const moe_config& c = *cfg;
+  if (!tok16(c, a->x) || !need16(a->w_gate) || !opt4(a->logit_bias) || !need16(a->w1) ||
+      !opt16(a->b1) || !need16(a->w2) || !opt16(a->b2) || !tok16(c, a->y) || !opt16(a->logits) ||
+      !opt16(a->probs) || !opt4(a->sel_token) || !opt4(a->sel_w) || !opt4(a->token_experts) ||
+      !opt4(a->unrouted))
+    return MOE_ERR_INVALID_ARGUMENT;
+  const EcLayout L = make_ec_layout(c);
+  if (!ws || !al16(ws) || ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int* flags = at<int>(ws, L.flags);
+  MOE_CUDA(cudaMemsetAsync(flags, 0, sizeof(int), st));
+  if ((s = zero_async(a->unrouted, sizeof(int32_t), st)) != MOE_OK) return s;
+  if (c.T == 0) return MOE_OK;
+  const int sms = sm_count();
+  if (sms <= 0) return MOE_ERR_CUDA;
+  const int64_t C = L.C;
+  float* region = at<float>(ws, L.logits);
+  float* probs_et = at<float>(ws, L.probs_et);
+  int32_t* rowmap = at<int32_t>(ws, L.rowmap);
+  int32_t* offsets = at<int32_t>(ws, L.offsets);
+  int32_t* sel_token = a->sel_token ? a->sel_token : at<int32_t>(ws, L.sel_token);
+  float* sel_w = a->sel_w ? a->sel_w : at<float>(ws, L.sel_w);
+  void* x_perm = at<void>(ws, L.x_perm);
+  void* h_buf = at<void>(ws, L.h_buf);
+  void* y_perm = at<void>(ws, L.y_perm);
+
+  // EC1: router contraction and softmax (fp32: SIMT GEMM with the bias in its
+  // epilogue; bf16: tensor-core K-split partials, added with the bias in EC1).
+  GemmArgs g{};
+  g.A = a->x;
+  g.rows_alloc = c.T;
+  g.B = a->w_gate;
+  g.m_rows = c.T;
+  g.G = 1;
+  g.N = c.E;
+  g.K = c.d;
+  g.flags = flags;
+  if (c.dtype == MOE_F32) {
+    float* lg = a->logits ? a->logits : region;
+    g.bias = a->logit_bias;
+    g.out = lg;
+    MOE_CUDA(launch_simt_gemm_f32(g, EPI_ROUTER_F32, sms, st));
+    MOE_CUDA(launch_ec_softmax(lg, 1, 0, nullptr, nullptr, a->probs, probs_et, c.T, c.E, flags,
+                               st));
+  } else {
+    g.out = region;
+    g.ksplit = router_splits(c.T, c.E, c.d, sms < kMaxSmsForSizing ? sms : kMaxSmsForSizing);
+    g.split_stride = c.T * c.E;
+    MOE_CUDA(launch_tc_gemm_bf16(g, EPI_ROUTER_F32, sms, st));
+    MOE_CUDA(launch_ec_softmax(region, g.ksplit, g.split_stride, a->logit_bias, a->logits,
+                               a->probs, probs_et, c.T, c.E, flags, st));
+  }
+  // EC2: each expert's C tokens; then the rows in expert order and the expert FFN.
+  MOE_CUDA(launch_ec_select(probs_et, c.T, c.E, C, sel_token, sel_w, rowmap, offsets, st));
+  MOE_CUDA(launch_gather_rows(c.dtype, sel_token, offsets, c.E, a->x, x_perm, c.d, c.E * C, st));
+  if ((s = run_expert_ffn_rows(c, c.E * C, C, x_perm, offsets, a->w1, a->b1, a->w2, a->b2, h_buf,
+                               y_perm, flags, sms, st)) != MOE_OK)
+    return s;
+  // EC3: per-token combine over the experts that took the token.
+  MOE_CUDA(launch_ec_combine(c.dtype, y_perm, rowmap, probs_et, c.T, c.E, C, c.d, a->y,
+                             a->token_experts, a->unrouted, st));
+  return MOE_OK;
 }

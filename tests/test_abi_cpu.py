@@ -56,6 +56,7 @@ def test_struct_layouts_match_header():
     assert moe.MoeConfig.noise.offset == 40
     assert moe.MoeConfig.capacity_factor.offset == 32
     assert ctypes.sizeof(moe.MoeForwardArgs) == 20 * 8
+    assert ctypes.sizeof(moe.MoeExpertChoiceArgs) == 14 * 8
 
 
 def test_status_strings(L):
@@ -165,3 +166,60 @@ def test_selftest_validation_before_launch(L):
     assert L.moe_selftest_wait_timeout(FAKE_ODD + 1, 1000, None) == moe.MOE_ERR_INVALID_ARGUMENT
     assert L.moe_selftest_wait_timeout(FAKE, 0, None) == moe.MOE_ERR_INVALID_ARGUMENT
     assert L.moe_selftest_wait_timeout(FAKE, 3 * 10**9, None) == moe.MOE_ERR_INVALID_ARGUMENT
+
+
+# ---------------------------------------------------------------- expert choice
+@pytest.mark.parametrize("kw,status", [
+    (dict(capacity_factor=0.0), moe.MOE_ERR_INVALID_ARGUMENT),
+    (dict(capacity_factor=-1.0), moe.MOE_ERR_INVALID_ARGUMENT),
+    (dict(capacity_factor=float("inf")), moe.MOE_ERR_INVALID_ARGUMENT),
+    (dict(noise=1), moe.MOE_ERR_INVALID_ARGUMENT),
+    (dict(dtype=3), moe.MOE_ERR_INVALID_ARGUMENT),
+    (dict(E=0), moe.MOE_ERR_UNSUPPORTED),
+    (dict(E=257), moe.MOE_ERR_UNSUPPORTED),
+    (dict(d=4), moe.MOE_ERR_UNSUPPORTED),
+    (dict(T=-5), moe.MOE_ERR_UNSUPPORTED),
+    (dict(T=2**31), moe.MOE_ERR_UNSUPPORTED),
+    (dict(T=2**26, E=256, capacity_factor=64.0), moe.MOE_ERR_UNSUPPORTED),  # E*C >= 2^31
+    (dict(k=0, gate=9), moe.MOE_OK),      # k and gate are not read
+    (dict(E=1), moe.MOE_OK),
+])
+def test_expert_choice_config_validation(L, kw, status):
+    base = dict(T=64, d=64, h=128, E=8, k=2, dtype="bf16", gate=0, capacity_factor=1.0)
+    base.update(kw)
+    cfg = moe.config(**base)
+    n = ctypes.c_size_t()
+    assert L.moe_expert_choice_workspace_size(ctypes.byref(cfg), ctypes.byref(n)) == status
+    c = ctypes.c_int64()
+    assert L.moe_expert_choice_capacity(ctypes.byref(cfg), ctypes.byref(c)) == status
+
+
+@pytest.mark.parametrize("T,E,cf", [(4096, 8, 2.0), (777, 8, 2.0), (64, 64, 1.0), (10, 3, 0.7),
+                                    (5, 8, 100.0), (1, 1, 1.0), (0, 4, 1.0)])
+def test_expert_choice_capacity_is_clamped_capacity_rule(L, T, E, cf):
+    cfg = moe.config(T, 64, 64, E, 1, "bf16", 0, cf)
+    assert moe.moe_expert_choice_capacity(cfg) == min(T, oracle.capacity(T, E, cf))
+
+
+def test_expert_choice_pointer_and_workspace_checks(L):
+    cfg = moe.config(64, 64, 128, 8, 2, capacity_factor=2.0)
+    need = moe.moe_expert_choice_workspace_size(cfg)
+    C = moe.moe_expert_choice_capacity(cfg)
+    # the row buffers alone: E*C rows of d, h and d bf16 elements
+    assert need >= 8 * C * (64 + 128 + 64) * 2
+    INV, WS = moe.MOE_ERR_INVALID_ARGUMENT, moe.MOE_ERR_WORKSPACE
+    ok = dict(x=FAKE, w_gate=FAKE, w1=FAKE, w2=FAKE, y=FAKE)
+    f = L.moe_expert_choice_forward
+    assert f(ctypes.byref(cfg), None, FAKE, need, None) == INV
+    for drop in ok:
+        a = moe.MoeExpertChoiceArgs(**{k: v for k, v in ok.items() if k != drop})
+        assert f(ctypes.byref(cfg), ctypes.byref(a), FAKE, need, None) == INV, drop
+    for odd in ("x", "w1", "y", "b2", "probs"):
+        a = moe.MoeExpertChoiceArgs(**dict(ok, **{odd: FAKE_ODD}))
+        assert f(ctypes.byref(cfg), ctypes.byref(a), FAKE, need, None) == INV, odd
+    a = moe.MoeExpertChoiceArgs(**dict(ok, sel_token=FAKE + 2))
+    assert f(ctypes.byref(cfg), ctypes.byref(a), FAKE, need, None) == INV
+    a = moe.MoeExpertChoiceArgs(**ok)
+    assert f(ctypes.byref(cfg), ctypes.byref(a), FAKE, need - 1, None) == WS
+    assert f(ctypes.byref(cfg), ctypes.byref(a), None, need, None) == WS
+    assert f(ctypes.byref(cfg), ctypes.byref(a), FAKE_ODD, need, None) == WS
