@@ -229,8 +229,13 @@ __global__ void __launch_bounds__(kRouteWarps * 32)
   }
 }
 
-// Single CTA of 256 threads; thread e owns expert e.
-__global__ void __launch_bounds__(kMaxExperts)
+// Single CTA of kFinThreads threads.  The per-chunk tables are reduced by
+// kFinThreads / EP slices of consecutive chunks (EP = E rounded up to a power of two,
+// at least 32), each slice summing its chunks in order and the slices then added in
+// slice order; the rest of the kernel runs on thread e = expert e.
+constexpr int kFinThreads = 1024;
+
+__global__ void __launch_bounds__(kFinThreads)
     route_finalize_kernel(const int32_t* __restrict__ hist, const float* __restrict__ psum,
                           int nchunks, int E, int64_t T, int64_t C, int32_t* __restrict__ counts,
                           float* __restrict__ aux, int32_t* __restrict__ chunk_base,
@@ -239,38 +244,67 @@ __global__ void __launch_bounds__(kMaxExperts)
   __shared__ double s_red[kMaxExperts];
   __shared__ int s_scan[kMaxExperts];
   __shared__ int s_drop;
-  const int e = threadIdx.x;
-  if (e == 0) s_drop = 0;
-  int cnt = 0;
-  double ps = 0.0;
-  if (e < E) {
-    // Eight chunks at a time: the loads are issued together, then added in order.
-    constexpr int B = 8;
-    for (int c0 = 0; c0 < nchunks; c0 += B) {
-      int hv[B];
-      float pv[B];
+  __shared__ int s_cnt[kFinThreads];
+  __shared__ double s_ps[kFinThreads];
+  const int tid = threadIdx.x;
+  int EP = 32;
+  while (EP < E) EP <<= 1;
+  const int nslices = kFinThreads / EP;
+  const int per = (nchunks + nslices - 1) / nslices;
+  {
+    // Slice sl of expert ex: chunks [c_lo, c_hi), summed in order.
+    const int sl = tid / EP, ex = tid % EP;
+    const int c_lo = sl * per, c_hi = min(nchunks, c_lo + per);
+    int cnt = 0;
+    double ps = 0.0;
+    if (ex < E) {
+      // Eight chunks at a time: the loads are issued together, then added in order.
+      constexpr int B = 8;
+      for (int c0 = c_lo; c0 < c_hi; c0 += B) {
+        int hv[B];
+        float pv[B];
 #pragma unroll
-      for (int i = 0; i < B; ++i) {
-        const int c = c0 + i;
-        hv[i] = c < nchunks ? hist[static_cast<int64_t>(c) * E + e] : 0;
-        pv[i] = (psum && c < nchunks) ? psum[static_cast<int64_t>(c) * E + e] : 0.f;
-      }
+        for (int i = 0; i < B; ++i) {
+          const int c = c0 + i;
+          hv[i] = c < c_hi ? hist[static_cast<int64_t>(c) * E + ex] : 0;
+          pv[i] = (psum && c < c_hi) ? psum[static_cast<int64_t>(c) * E + ex] : 0.f;
+        }
 #pragma unroll
-      for (int i = 0; i < B; ++i) {
-        const int c = c0 + i;
-        if (c < nchunks) {
-          if (chunk_base) chunk_base[static_cast<int64_t>(c) * E + e] = cnt;
+        for (int i = 0; i < B; ++i) {
           cnt += hv[i];
           ps += static_cast<double>(pv[i]);
         }
       }
     }
+    s_cnt[tid] = cnt;
+    s_ps[tid] = ps;
+    __syncthreads();
+    // Position bases: the counts of the lower slices, then this slice's chunks in order.
+    if (chunk_base && ex < E) {
+      int base = 0;
+      for (int q = 0; q < sl; ++q) base += s_cnt[q * EP + ex];
+      for (int c = c_lo; c < c_hi; ++c) {
+        chunk_base[static_cast<int64_t>(c) * E + ex] = base;
+        base += hist[static_cast<int64_t>(c) * E + ex];
+      }
+    }
+  }
+  const int e = tid;
+  if (e == 0) s_drop = 0;
+  int cnt = 0;
+  double ps = 0.0;
+  if (e < E) {
+    for (int q = 0; q < nslices; ++q) {
+      cnt += s_cnt[q * EP + e];
+      ps += s_ps[q * EP + e];
+    }
     if (counts) counts[e] = cnt;
   }
   // balance loss: E * sum_e (psum_e / T) * (count_e / T), fixed-order tree sum
-  s_red[e] = (e < E && T > 0) ? (ps / static_cast<double>(T)) *
-                                    (static_cast<double>(cnt) / static_cast<double>(T))
-                              : 0.0;
+  if (e < kMaxExperts)
+    s_red[e] = (e < E && T > 0) ? (ps / static_cast<double>(T)) *
+                                      (static_cast<double>(cnt) / static_cast<double>(T))
+                                : 0.0;
   __syncthreads();
   for (int o = kMaxExperts / 2; o > 0; o >>= 1) {
     if (e < o) s_red[e] += s_red[e + o];
@@ -283,12 +317,12 @@ __global__ void __launch_bounds__(kMaxExperts)
   if (e < E) kp = (C < 0 || cnt < C) ? cnt : static_cast<int>(C);
   if (kept && e < E) kept[e] = kp;
   if (e < E && cnt > kp) atomicAdd(&s_drop, cnt - kp);
-  s_scan[e] = kp;
+  if (e < kMaxExperts) s_scan[e] = kp;
   __syncthreads();
   for (int o = 1; o < kMaxExperts; o <<= 1) {
-    const int add = (e >= o) ? s_scan[e - o] : 0;
+    const int add = (e >= o && e < kMaxExperts) ? s_scan[e - o] : 0;
     __syncthreads();
-    s_scan[e] += add;
+    if (e < kMaxExperts) s_scan[e] += add;
     __syncthreads();
   }
   if (offsets) {
@@ -302,7 +336,7 @@ __global__ void __launch_bounds__(kMaxExperts)
   if (stats) {
     auto block_sum = [&](double v) {
       __syncthreads();
-      s_red[e] = v;
+      if (e < kMaxExperts) s_red[e] = v;
       __syncthreads();
       for (int o = kMaxExperts / 2; o > 0; o >>= 1) {
         if (e < o) s_red[e] += s_red[e + o];
@@ -312,7 +346,7 @@ __global__ void __launch_bounds__(kMaxExperts)
     };
     auto block_max = [&](double v) {
       __syncthreads();
-      s_red[e] = v;
+      if (e < kMaxExperts) s_red[e] = v;
       __syncthreads();
       for (int o = kMaxExperts / 2; o > 0; o >>= 1) {
         if (e < o) s_red[e] = fmax(s_red[e], s_red[e + o]);
@@ -377,7 +411,7 @@ cudaError_t launch_route_finalize(const int32_t* hist, const float* psum, int nc
                                   int64_t T, int64_t C, int32_t* counts, float* aux,
                                   int32_t* chunk_base, int32_t* kept, int32_t* offsets,
                                   int32_t* dropped, float* stats, cudaStream_t stream) {
-  route_finalize_kernel<<<1, kMaxExperts, 0, stream>>>(hist, psum, nchunks, E, T, C, counts, aux,
+  route_finalize_kernel<<<1, kFinThreads, 0, stream>>>(hist, psum, nchunks, E, T, C, counts, aux,
                                                        chunk_base, kept, offsets, dropped, stats);
   return cudaGetLastError();
 }
