@@ -51,9 +51,17 @@ KERNELS_PER_FORWARD = 8   # router GEMM, softmax/top-k, finalize/scan, place, ga
 KERNELS_PER_EC_FORWARD = 7  # router GEMM, softmax, per-expert select, gather, GEMM1, GEMM2, combine
 
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the grouped GEMM pair
-# (G1 + G2), from the ncu capture summarised in profiles/traffic_ffn_mixtral_prefill.md.
-# Only workloads whose current kernels were captured appear here; others report null.
-NCU_TRAFFIC_BYTES = {"mixtral_prefill": 1010024704 + 213667328 + 1434962176 + 60748032}
+# (G1 + G2), from the ncu capture summarised in
+# profiles/traffic_expert_gemms_bf16_workloads.md.  Only workloads whose current kernels
+# were captured appear here; others report null.
+NCU_TRAFFIC_BYTES = {
+    "mixtral_prefill": 2723869696,
+    "deepseek_fine": 17675532032,
+    "mixtral_prefill_ec": 2655692032,
+    "deepseek_fine_ec": 17559433984,
+    "decode": 4480856832,
+    "switch_capacity": 156232192,
+}
 
 
 def load_peaks():
