@@ -41,6 +41,9 @@ def lib():
         L.orc_aux_loss.restype = _D
         L.orc_routing_stats.argtypes = [_I, _P, _P]
         L.orc_noisy_scores.argtypes = [_I64, _I, _I, _P, _P, _P]
+        L.orc_backward.argtypes = [_I64, _I, _I, _I, _I, _I, _I, ctypes.c_double] + [_P] * 8 + \
+            [ctypes.c_double] + [_P] * 7
+        L.orc_backward.restype = _I
         L.orc_expert_choice.argtypes = [_I64, _I, _I64, _P, _P, _P]
         L.orc_combine_expert_choice.argtypes = [_I64, _I, _I, _I64, _P, _P, _P, _P]
         L.orc_capacity.argtypes = [_I64, _I, _D]
@@ -67,8 +70,8 @@ def set_num_threads(n: int) -> None:
 def raw(a):
     """Return (contiguous numpy array of raw element bits, dtype code) for a tensor/array.
 
-    dtype code 0 = fp32, 1 = bf16.  Accepts CPU torch tensors (fp32/bf16) and numpy
-    float32 arrays."""
+    dtype code 0 = fp32, 1 = bf16, 2 = fp64.  Accepts CPU torch tensors (fp32/bf16/fp64)
+    and numpy float32/float64 arrays."""
     try:
         import torch
         if isinstance(a, torch.Tensor):
@@ -77,12 +80,16 @@ def raw(a):
                 return a.view(torch.int16).numpy(), 1
             if a.dtype == torch.float32:
                 return a.numpy(), 0
+            if a.dtype == torch.float64:
+                return a.numpy(), 2
             raise TypeError(f"unsupported tensor dtype {a.dtype}")
     except ImportError:  # pragma: no cover
         pass
     a = np.ascontiguousarray(a)
     if a.dtype == np.float32:
         return a, 0
+    if a.dtype == np.float64:
+        return a, 2
     if a.dtype in (np.int16, np.uint16):
         return a, 1
     raise TypeError(f"unsupported array dtype {a.dtype}")
@@ -205,6 +212,35 @@ def dispatch(idx, E, C):
         raise ValueError("expert index out of range")
     return dict(kept=kept, offsets=offsets, slot_row=slot_row, row_token=row_token,
                 dropped=int(dropped[0]))
+
+
+def backward(inp, dy, k, mode, capacity_factor=None, d_aux=0.0):
+    """Gradients of the layer (B1..B7 in moe_oracle.cpp) for dL/dy = dy and dL/daux =
+    d_aux: dict dx [T,d], dw_gate [E,d], dlogit_bias [E], dw1 [E,h,d], db1 [E,h],
+    dw2 [E,d,h], db2 [E,d], all float64.  dy has the dtype of x."""
+    xr, dt = raw(inp["x"])
+    wg, _ = raw(inp["w_gate"])
+    w1, _ = raw(inp["w1"])
+    w2, _ = raw(inp["w2"])
+    b1 = raw(inp["b1"])[0] if inp.get("b1") is not None else None
+    b2 = raw(inp["b2"])[0] if inp.get("b2") is not None else None
+    g, gdt = raw(dy)
+    if gdt != dt:
+        raise TypeError("dy must have the dtype of x")
+    lb = _f32(inp.get("logit_bias"))
+    T, d = xr.shape
+    E, h = w1.shape[0], w1.shape[1]
+    out = dict(dx=np.empty((T, d)), dw_gate=np.empty((E, d)), dlogit_bias=np.empty(E),
+               dw1=np.empty((E, h, d)), db1=np.empty((E, h)), dw2=np.empty((E, d, h)),
+               db2=np.empty((E, d)))
+    rc = lib().orc_backward(T, d, h, E, k, int(mode), dt, float(capacity_factor or 0.0),
+                            _ptr(xr), _ptr(wg), _ptr(lb), _ptr(w1), _ptr(b1), _ptr(w2), _ptr(b2),
+                            _ptr(g), float(d_aux), _ptr(out["dx"]), _ptr(out["dw_gate"]),
+                            _ptr(out["dlogit_bias"]), _ptr(out["dw1"]), _ptr(out["db1"]),
+                            _ptr(out["dw2"]), _ptr(out["db2"]))
+    if rc != 0:
+        raise ValueError("oracle backward failed")
+    return out
 
 
 def expert_choice(p, C):

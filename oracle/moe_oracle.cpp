@@ -22,8 +22,9 @@
 // Parity status per function (what pins it is listed in the tests):
 //   orc_logits, orc_softmax, orc_topk, orc_gate_weights, orc_aux_loss,
 //   orc_capacity, orc_dispatch, orc_expert_rows, orc_combine, orc_forward,
-//   orc_forward_dense, orc_expert_choice and orc_combine_expert_choice are each
-//   pinned by closed forms, invariants, library routines or brute force in
+//   orc_forward_dense, orc_expert_choice, orc_combine_expert_choice and
+//   orc_backward are each pinned by closed forms, invariants, library routines,
+//   brute force or (the backward) central differences of the fp64 forward in
 //   tests/test_oracle_pins.py.
 
 #include <cmath>
@@ -38,17 +39,27 @@
 
 namespace {
 
-// dtype codes: 0 = IEEE fp32, 1 = bfloat16 (upper 16 bits of an fp32).
+// dtype codes: 0 = IEEE fp32, 1 = bfloat16 (upper 16 bits of an fp32), 2 = IEEE fp64
+// (used by the tests that differentiate the layer numerically).
 double elem(const void* p, int dtype, int64_t i) {
   if (dtype == 0) return (double)static_cast<const float*>(p)[i];
+  if (dtype == 2) return static_cast<const double*>(p)[i];
   uint32_t bits = (uint32_t)static_cast<const uint16_t*>(p)[i] << 16;
   float f;
   std::memcpy(&f, &bits, sizeof f);
   return (double)f;
 }
 
+int64_t elem_size(int dtype) { return dtype == 0 ? 4 : dtype == 2 ? 8 : 2; }
+
 // SiLU(a) = a * sigmoid(a) = a / (1 + e^{-a})  ([P5] Expert.forward uses F.silu).
 double silu(double a) { return a / (1.0 + std::exp(-a)); }
+
+// d SiLU / da = sigmoid(a) * (1 + a * (1 - sigmoid(a))).
+double silu_grad(double a) {
+  const double sg = 1.0 / (1.0 + std::exp(-a));
+  return sg * (1.0 + a * (1.0 - sg));
+}
 
 }  // namespace
 
@@ -403,7 +414,7 @@ int orc_forward(int64_t T, int d, int h, int E, int k, int mode, int dtype, doub
     for (int j = 0; j < k; ++j) {
       if (slot_row[t * k + j] < 0) continue;
       int e = idx[t * k + j];
-      int64_t sz = dtype == 0 ? 4 : 2;
+      int64_t sz = elem_size(dtype);
       const char* xr = static_cast<const char*>(x) + t * d * sz;
       const char* w1e = static_cast<const char*>(w1) + (int64_t)e * h * d * sz;
       const char* w2e = static_cast<const char*>(w2) + (int64_t)e * d * h * sz;
@@ -425,6 +436,129 @@ int orc_forward(int64_t T, int d, int h, int E, int k, int mode, int dtype, doub
   return 0;
 }
 
+// B. Backward of the whole layer (the gradients that training through the pages'
+// MoELayer would take; the pages print no backward, so this is the chain rule
+// applied to O1..O7 in reverse).  Given dy = dL/dy [T,d] (dtype) and d_aux = dL/d aux:
+//   forward recomputed: l, p, TopK set S_t, w, capacity and kept slots, and for each
+//   kept slot (t,j) of expert e: a = W1[e] x_t + b1[e], s = SiLU(a), z = W2[e] s + b2[e];
+//   B7  dz = w_tj dy_t;  dw_tj = <dy_t, z>  (a dropped slot has z = 0, so dw = 0);
+//   B6  dW2[e] += dz s^T;  db2[e] += dz;  ds = W2[e]^T dz;  da = ds * SiLU'(a);
+//       dW1[e] += da x_t^T;  db1[e] += da;  dx_t += W1[e]^T da;
+//   B3  gate: both gate forms give w_j = e^{l_j} / sum_{i in S} e^{l_i} on S, so
+//       dl_j = w_j (dw_j - sum_{i in S} w_i dw_i) for j in S, 0 elsewhere;
+//   B4  balance loss E sum_e f_e P_e with f_e = mean_t p[t,e] and P_e = counts_e / T
+//       (counts do not depend on l): dl[t,c] += d_aux (E/T) p[t,c] (P_c - sum_e P_e p[t,e]);
+//   B1  dlogit_bias = sum_t dl[t,:];  dWg = dl^T x;  dx_t += Wg^T dl_t.
+// Outputs are double; dlb, db1, db2 may be NULL.  Returns 0, or 1 if routing failed.
+int orc_backward(int64_t T, int d, int h, int E, int k, int mode, int dtype,
+                 double capacity_factor, const void* x, const void* wg, const float* logit_bias,
+                 const void* w1, const void* b1, const void* w2, const void* b2, const void* dy,
+                 double d_aux, double* dx, double* dwg, double* dlb, double* dw1, double* db1,
+                 double* dw2, double* db2) {
+  std::vector<double> logits(T * E), p(T * E), w(T * k), dw(T * k, 0.0), dl(T * E, 0.0);
+  std::vector<int32_t> idx(T * k), kept(E), offsets(E + 1), slot_row(T * k), row_token(T * k);
+  std::vector<int64_t> counts(E);
+  int64_t dropped = 0;
+  orc_logits(T, d, E, dtype, x, wg, logit_bias, logits.data());
+  orc_softmax(T, E, logits.data(), p.data());
+  orc_topk(T, E, k, logits.data(), idx.data());
+  orc_gate_weights(T, E, k, mode, logits.data(), idx.data(), w.data());
+  orc_aux_loss(T, E, k, p.data(), idx.data(), counts.data(), nullptr, nullptr);
+  const int64_t C = orc_capacity(T, E, capacity_factor);
+  if (orc_dispatch(T, E, k, C, idx.data(), kept.data(), offsets.data(), slot_row.data(),
+                   row_token.data(), &dropped))
+    return 1;
+  for (int64_t i = 0; i < T * d; ++i) dx[i] = 0.0;
+  for (int64_t i = 0; i < (int64_t)E * d; ++i) dwg[i] = 0.0;
+  for (int64_t i = 0; i < (int64_t)E * h * d; ++i) dw1[i] = dw2[i] = 0.0;
+  if (db1) for (int64_t i = 0; i < (int64_t)E * h; ++i) db1[i] = 0.0;
+  if (db2) for (int64_t i = 0; i < (int64_t)E * d; ++i) db2[i] = 0.0;
+
+  // B7, B6: expert path, slot by slot.
+  std::vector<double> a(h), sv(h), z(d), dz(d), ds(h), da(h);
+  for (int64_t t = 0; t < T; ++t)
+    for (int j = 0; j < k; ++j) {
+      if (slot_row[t * k + j] < 0) continue;
+      const int e = idx[t * k + j];
+      const int64_t w1o = (int64_t)e * h * d, w2o = (int64_t)e * d * h;
+      for (int i = 0; i < h; ++i) {
+        double acc = 0.0;
+        for (int c = 0; c < d; ++c) acc += elem(w1, dtype, w1o + (int64_t)i * d + c) * elem(x, dtype, t * d + c);
+        if (b1) acc += elem(b1, dtype, (int64_t)e * h + i);
+        a[i] = acc;
+        sv[i] = silu(acc);
+      }
+      double dwt = 0.0;
+      for (int o = 0; o < d; ++o) {
+        double acc = 0.0;
+        for (int i = 0; i < h; ++i) acc += elem(w2, dtype, w2o + (int64_t)o * h + i) * sv[i];
+        if (b2) acc += elem(b2, dtype, (int64_t)e * d + o);
+        z[o] = acc;
+        const double g = elem(dy, dtype, t * d + o);
+        dz[o] = w[t * k + j] * g;
+        dwt += g * acc;
+      }
+      dw[t * k + j] = dwt;
+      for (int o = 0; o < d; ++o) {
+        for (int i = 0; i < h; ++i) dw2[w2o + (int64_t)o * h + i] += dz[o] * sv[i];
+        if (db2) db2[(int64_t)e * d + o] += dz[o];
+      }
+      for (int i = 0; i < h; ++i) {
+        double acc = 0.0;
+        for (int o = 0; o < d; ++o) acc += elem(w2, dtype, w2o + (int64_t)o * h + i) * dz[o];
+        ds[i] = acc;
+        da[i] = acc * silu_grad(a[i]);
+      }
+      for (int i = 0; i < h; ++i) {
+        for (int c = 0; c < d; ++c) dw1[w1o + (int64_t)i * d + c] += da[i] * elem(x, dtype, t * d + c);
+        if (db1) db1[(int64_t)e * h + i] += da[i];
+      }
+      for (int c = 0; c < d; ++c) {
+        double acc = 0.0;
+        for (int i = 0; i < h; ++i) acc += elem(w1, dtype, w1o + (int64_t)i * d + c) * da[i];
+        dx[t * d + c] += acc;
+      }
+    }
+
+  // B3: gate weights -> logits (softmax over the TopK set).
+  for (int64_t t = 0; t < T; ++t) {
+    double inner = 0.0;
+    for (int j = 0; j < k; ++j) inner += w[t * k + j] * dw[t * k + j];
+    for (int j = 0; j < k; ++j)
+      dl[t * E + idx[t * k + j]] += w[t * k + j] * (dw[t * k + j] - inner);
+  }
+  // B4: balance loss -> logits.
+  if (d_aux != 0.0 && T > 0) {
+    for (int64_t t = 0; t < T; ++t) {
+      double pp = 0.0;
+      for (int e = 0; e < E; ++e) pp += ((double)counts[e] / (double)T) * p[t * E + e];
+      for (int c = 0; c < E; ++c)
+        dl[t * E + c] += d_aux * ((double)E / (double)T) * p[t * E + c] *
+                         ((double)counts[c] / (double)T - pp);
+    }
+  }
+  // B1: router.
+  if (dlb)
+    for (int e = 0; e < E; ++e) {
+      double acc = 0.0;
+      for (int64_t t = 0; t < T; ++t) acc += dl[t * E + e];
+      dlb[e] = acc;
+    }
+  for (int e = 0; e < E; ++e)
+    for (int c = 0; c < d; ++c) {
+      double acc = 0.0;
+      for (int64_t t = 0; t < T; ++t) acc += dl[t * E + e] * elem(x, dtype, t * d + c);
+      dwg[(int64_t)e * d + c] = acc;
+    }
+  for (int64_t t = 0; t < T; ++t)
+    for (int c = 0; c < d; ++c) {
+      double acc = 0.0;
+      for (int e = 0; e < E; ++e) acc += dl[t * E + e] * elem(wg, dtype, (int64_t)e * d + c);
+      dx[t * d + c] += acc;
+    }
+  return 0;
+}
+
 // O-BF. Dense brute force of the same layer, for tiny inputs only.  It follows
 // the formulas literally and shares no intermediate with orc_forward:
 //  * TopK(t) is a set: e is in it iff fewer than k experts rank above e, where e'
@@ -437,7 +571,7 @@ void orc_forward_dense(int64_t T, int d, int h, int E, int k, int mode, int dtyp
                        double capacity_factor, const void* x, const void* wg,
                        const float* logit_bias, const void* w1, const void* b1, const void* w2,
                        const void* b2, double* y) {
-  int64_t sz = dtype == 0 ? 4 : 2;
+  int64_t sz = elem_size(dtype);
   std::vector<double> l(T * E), z(d), a(h);
   for (int64_t t = 0; t < T; ++t)
     for (int e = 0; e < E; ++e) {

@@ -455,3 +455,71 @@ def test_expert_choice_unchosen_tokens_get_zero():
     chosen = set(out["sel_token"].ravel().tolist())
     for t in range(40):
         assert np.any(out["y"][t] != 0.0) == (t in chosen)
+
+
+# ----------------------------------------------------------------- backward (B1..B7)
+def _tiny_f64_layer(rng, T=6, d=5, h=7, E=4):
+    return dict(x=rng.standard_normal((T, d)), w_gate=rng.standard_normal((E, d)),
+                w1=rng.standard_normal((E, h, d)) / 2, b1=rng.standard_normal((E, h)) * 0.1,
+                w2=rng.standard_normal((E, d, h)) / 2, b2=rng.standard_normal((E, d)) * 0.1,
+                logit_bias=None)
+
+
+@pytest.mark.parametrize("mode,cf,k", [(0, None, 2), (1, None, 2), (0, 1.0, 2), (1, 0.5, 3),
+                                       (1, None, 4)])
+def test_backward_matches_central_differences(mode, cf, k):
+    """Every gradient of L = <G, y> + d_aux * aux equals the central difference of the
+    oracle's own fp64 forward (step 1e-6), with and without capacity drops and with
+    k = E (softmax over every expert)."""
+    rng = np.random.default_rng(10 * mode + k)
+    inp = _tiny_f64_layer(rng)
+    G = rng.standard_normal(inp["x"].shape)
+    d_aux = 0.7
+
+    def loss():
+        o = oracle.forward(inp, k, mode, cf)
+        return float((o["y"] * G).sum() + d_aux * o["aux"])
+
+    base = oracle.forward(inp, k, mode, cf)
+    g = oracle.backward(inp, G, k, mode, cf, d_aux)
+    eps = 1e-6
+    for name, key in [("x", "dx"), ("w_gate", "dw_gate"), ("w1", "dw1"), ("b1", "db1"),
+                      ("w2", "dw2"), ("b2", "db2")]:
+        a = inp[name]
+        fd = np.zeros_like(a)
+        for ix in np.ndindex(a.shape):
+            old = a[ix]
+            a[ix] = old + eps
+            lp = loss()
+            a[ix] = old - eps
+            lm = loss()
+            a[ix] = old
+            fd[ix] = (lp - lm) / (2 * eps)
+        np.testing.assert_allclose(g[key], fd, rtol=1e-6, atol=1e-7, err_msg=name)
+    # the perturbations never crossed a routing decision
+    assert np.array_equal(oracle.forward(inp, k, mode, cf)["idx"], base["idx"])
+
+
+def test_backward_logit_bias_equals_constant_feature_router_weight():
+    """With a constant-one input feature, the router weight on that feature acts exactly
+    as a logit bias, so its gradient is the logit-bias gradient."""
+    rng = np.random.default_rng(3)
+    inp = _tiny_f64_layer(rng, T=9)
+    inp["x"][:, -1] = 1.0
+    G = rng.standard_normal(inp["x"].shape)
+    g = oracle.backward(inp, G, 2, 1, 1.0, 0.3)
+    np.testing.assert_allclose(g["dlogit_bias"], g["dw_gate"][:, -1], rtol=1e-12, atol=1e-13)
+
+
+def test_backward_without_upstream_gradient_is_the_balance_loss_gradient():
+    """dy = 0: no expert weight receives gradient, and d_aux = 0 makes every gradient 0."""
+    rng = np.random.default_rng(4)
+    inp = _tiny_f64_layer(rng)
+    zero = np.zeros_like(inp["x"])
+    g = oracle.backward(inp, zero, 2, 0, None, 1.0)
+    for key in ("dw1", "db1", "dw2", "db2"):
+        assert np.all(g[key] == 0.0), key
+    assert np.abs(g["dw_gate"]).max() > 0
+    g0 = oracle.backward(inp, zero, 2, 0, None, 0.0)
+    for key, v in g0.items():
+        assert np.all(v == 0.0), key
