@@ -157,6 +157,12 @@ typedef struct moe_forward_args {
   int32_t* row_token;       /* [T*k], or NULL */
   int32_t* dropped;         /* [1], or NULL */
   float* routing_stats;     /* [MOE_ROUTING_STATS] fp32, or NULL (see moe_route) */
+  /* Activations saved for moe_backward (each [T*k, .] dtype, or NULL to keep the
+     forward's copy inside the workspace; h_pre is only written when given): */
+  void* x_perm;             /* [T*k,d] the gathered token rows Xp */
+  void* h_act;              /* [T*k,h] H = SiLU(A), GEMM1's output */
+  void* y_perm;             /* [T*k,d] Yp, GEMM2's output */
+  void* h_pre;              /* [T*k,h] A = W1 x + b1, the pre-activation */
 } moe_forward_args;
 
 /* Human-readable name of a status code.  Never NULL. */
@@ -230,6 +236,56 @@ moe_status moe_combine(const moe_config* cfg, const void* y_perm, const int32_t*
    the four stage calls in order. */
 moe_status moe_forward(const moe_config* cfg, const moe_forward_args* args, void* ws,
                        size_t ws_bytes, moe_stream_t stream);
+
+/* ---- Backward ------------------------------------------------------------------
+   Gradients of the layer for training (the pages train the MoELayer but print no
+   backward; this is the chain rule through the forward above).  With dy = dL/dy and
+   d_aux = dL/d(aux_loss), for every kept slot (t,j) of expert e in row r:
+     dYp[r] = w_tj dy_t;  dw_tj = <dy_t, Yp[r]>;  dA[r] = (dYp[r] W2[e]) * SiLU'(A[r]);
+     dXp[r] = dA[r] W1[e];
+     dW2[e] = sum_r dYp[r]^T H[r];  db2[e] = sum_r dYp[r];
+     dW1[e] = sum_r dA[r]^T Xp[r];  db1[e] = sum_r dA[r];
+     dl_t   = w_j (dw_j - sum_i w_i dw_i) on the TopK set (both gate forms) plus the
+              balance-loss term d_aux (E/T) p_c (P_c - sum_e P_e p_e), P_e = counts_e / T;
+     dW_g   = dl^T x;  dlogit_bias = sum_t dl_t;  dx_t = dl_t W_g + sum_j dXp[slot j].
+   bf16 layers only (MOE_ERR_UNSUPPORTED for fp32), no routing noise.  GEMMs run on the
+   tensor cores with bf16 operands (dYp, dA, dXp and dl rounded to bf16) and fp32
+   accumulation; dW1, dW2 and dx are rounded to bf16 once, the other gradients are
+   fp32.  Results are deterministic.  The routing and saved-activation inputs are the
+   outputs of the moe_forward call being differentiated (same cfg). */
+typedef struct moe_backward_args {
+  const void* dy;           /* [T,d] dtype */
+  const void* x;            /* [T,d] dtype */
+  const void* w_gate;       /* [E,d] dtype */
+  const void* w1;           /* [E,h,d] dtype */
+  const void* w2;           /* [E,d,h] dtype */
+  const float* logits;      /* [T,E] fp32 forward logits */
+  const int32_t* topk_idx;  /* [T,k] */
+  const float* topk_w;      /* [T,k] fp32 */
+  const int32_t* counts;    /* [E] pre-drop assignments per expert */
+  const int32_t* offsets;   /* [E+1] */
+  const int32_t* slot_row;  /* [T,k] */
+  const void* x_perm;       /* [T*k,d] dtype, forward's Xp */
+  const void* h_pre;        /* [T*k,h] dtype, forward's A */
+  const void* h_act;        /* [T*k,h] dtype, forward's H */
+  const void* y_perm;       /* [T*k,d] dtype, forward's Yp */
+  float d_aux;              /* dL / d aux_loss */
+  void* dx;                 /* [T,d] dtype, required */
+  float* dw_gate;           /* [E,d] fp32, or NULL */
+  float* dlogit_bias;       /* [E] fp32, or NULL */
+  void* dw1;                /* [E,h,d] dtype, or NULL */
+  float* db1;               /* [E,h] fp32, or NULL */
+  void* dw2;                /* [E,d,h] dtype, or NULL */
+  float* db2;               /* [E,d] fp32, or NULL */
+} moe_backward_args;
+
+/* Workspace bytes moe_backward needs (dYp, dA, dXp row buffers and per-token
+   gradients of the gate).  Host only. */
+moe_status moe_backward_workspace_size(const moe_config* cfg, size_t* bytes);
+
+/* The layer's backward on one stream.  Device flags: MOE_DEVERR_TIMEOUT. */
+moe_status moe_backward(const moe_config* cfg, const moe_backward_args* args, void* ws,
+                        size_t ws_bytes, moe_stream_t stream);
 
 /* ---- Expert-choice routing -------------------------------------------------
    The selection direction reversed (routing-mechanism page, section "Expert Choice

@@ -42,7 +42,7 @@ def lib():
         L.orc_routing_stats.argtypes = [_I, _P, _P]
         L.orc_noisy_scores.argtypes = [_I64, _I, _I, _P, _P, _P]
         L.orc_backward.argtypes = [_I64, _I, _I, _I, _I, _I, _I, ctypes.c_double] + [_P] * 8 + \
-            [ctypes.c_double] + [_P] * 7
+            [ctypes.c_double] + [_P] * 8
         L.orc_backward.restype = _I
         L.orc_expert_choice.argtypes = [_I64, _I, _I64, _P, _P, _P]
         L.orc_combine_expert_choice.argtypes = [_I64, _I, _I, _I64, _P, _P, _P, _P]
@@ -214,10 +214,11 @@ def dispatch(idx, E, C):
                 dropped=int(dropped[0]))
 
 
-def backward(inp, dy, k, mode, capacity_factor=None, d_aux=0.0):
+def backward(inp, dy, k, mode, capacity_factor=None, d_aux=0.0, logits_in=None):
     """Gradients of the layer (B1..B7 in moe_oracle.cpp) for dL/dy = dy and dL/daux =
     d_aux: dict dx [T,d], dw_gate [E,d], dlogit_bias [E], dw1 [E,h,d], db1 [E,h],
-    dw2 [E,d,h], db2 [E,d], all float64.  dy has the dtype of x."""
+    dw2 [E,d,h], db2 [E,d], all float64.  dy has the dtype of x.  logits_in [T,E]
+    (optional) replaces the recomputed router logits downstream of O1."""
     xr, dt = raw(inp["x"])
     wg, _ = raw(inp["w_gate"])
     w1, _ = raw(inp["w1"])
@@ -233,9 +234,10 @@ def backward(inp, dy, k, mode, capacity_factor=None, d_aux=0.0):
     out = dict(dx=np.empty((T, d)), dw_gate=np.empty((E, d)), dlogit_bias=np.empty(E),
                dw1=np.empty((E, h, d)), db1=np.empty((E, h)), dw2=np.empty((E, d, h)),
                db2=np.empty((E, d)))
+    li = None if logits_in is None else np.ascontiguousarray(logits_in, np.float64)
     rc = lib().orc_backward(T, d, h, E, k, int(mode), dt, float(capacity_factor or 0.0),
                             _ptr(xr), _ptr(wg), _ptr(lb), _ptr(w1), _ptr(b1), _ptr(w2), _ptr(b2),
-                            _ptr(g), float(d_aux), _ptr(out["dx"]), _ptr(out["dw_gate"]),
+                            _ptr(g), float(d_aux), _ptr(li), _ptr(out["dx"]), _ptr(out["dw_gate"]),
                             _ptr(out["dlogit_bias"]), _ptr(out["dw1"]), _ptr(out["db1"]),
                             _ptr(out["dw2"]), _ptr(out["db2"]))
     if rc != 0:

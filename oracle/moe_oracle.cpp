@@ -449,17 +449,23 @@ int orc_forward(int64_t T, int d, int h, int E, int k, int mode, int dtype, doub
 //   B4  balance loss E sum_e f_e P_e with f_e = mean_t p[t,e] and P_e = counts_e / T
 //       (counts do not depend on l): dl[t,c] += d_aux (E/T) p[t,c] (P_c - sum_e P_e p[t,e]);
 //   B1  dlogit_bias = sum_t dl[t,:];  dWg = dl^T x;  dx_t += Wg^T dl_t.
-// Outputs are double; dlb, db1, db2 may be NULL.  Returns 0, or 1 if routing failed.
+// Outputs are double; dlb, db1, db2 may be NULL.  logits_in (may be NULL) replaces the
+// recomputed router logits l for everything downstream of O1 (routing, gate weights,
+// p), so the backward can be evaluated on another implementation's routing decisions.
+// Returns 0, or 1 if routing failed.
 int orc_backward(int64_t T, int d, int h, int E, int k, int mode, int dtype,
                  double capacity_factor, const void* x, const void* wg, const float* logit_bias,
                  const void* w1, const void* b1, const void* w2, const void* b2, const void* dy,
-                 double d_aux, double* dx, double* dwg, double* dlb, double* dw1, double* db1,
-                 double* dw2, double* db2) {
+                 double d_aux, const double* logits_in, double* dx, double* dwg, double* dlb,
+                 double* dw1, double* db1, double* dw2, double* db2) {
   std::vector<double> logits(T * E), p(T * E), w(T * k), dw(T * k, 0.0), dl(T * E, 0.0);
   std::vector<int32_t> idx(T * k), kept(E), offsets(E + 1), slot_row(T * k), row_token(T * k);
   std::vector<int64_t> counts(E);
   int64_t dropped = 0;
-  orc_logits(T, d, E, dtype, x, wg, logit_bias, logits.data());
+  if (logits_in)
+    std::memcpy(logits.data(), logits_in, sizeof(double) * T * E);
+  else
+    orc_logits(T, d, E, dtype, x, wg, logit_bias, logits.data());
   orc_softmax(T, E, logits.data(), p.data());
   orc_topk(T, E, k, logits.data(), idx.data());
   orc_gate_weights(T, E, k, mode, logits.data(), idx.data(), w.data());

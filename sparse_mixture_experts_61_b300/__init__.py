@@ -42,7 +42,7 @@ EXPORTED = ("moe_status_str", "moe_capacity", "moe_workspace_size", "moe_stage_w
             "moe_route", "moe_dispatch", "moe_expert_ffn", "moe_combine", "moe_forward",
             "moe_device_error", "moe_dispatch_static", "moe_selftest_wait_timeout",
             "moe_expert_choice_capacity", "moe_expert_choice_workspace_size",
-            "moe_expert_choice_forward")
+            "moe_expert_choice_forward", "moe_backward_workspace_size", "moe_backward")
 
 # Table cells of moe_dispatch_static's library-held scratch (include/moe.h).
 MOE_DISPATCH_STATIC_MAX_CELLS = 262144
@@ -66,7 +66,17 @@ class MoeForwardArgs(ctypes.Structure):
         "x", "w_gate", "logit_bias", "noise", "w1", "b1", "w2", "b2", "y", "logits", "topk_idx",
         "topk_w",
         "counts", "aux_loss", "offsets", "kept_counts", "slot_row", "row_token", "dropped",
-        "routing_stats")]
+        "routing_stats", "x_perm", "h_act", "y_perm", "h_pre")]
+
+
+BACKWARD_INPUTS = ("dy", "x", "w_gate", "w1", "w2", "logits", "topk_idx", "topk_w", "counts",
+                   "offsets", "slot_row", "x_perm", "h_pre", "h_act", "y_perm")
+BACKWARD_OUTPUTS = ("dx", "dw_gate", "dlogit_bias", "dw1", "db1", "dw2", "db2")
+
+
+class MoeBackwardArgs(ctypes.Structure):
+    _fields_ = ([(n, ctypes.c_void_p) for n in BACKWARD_INPUTS] + [("d_aux", ctypes.c_float)] +
+                [(n, ctypes.c_void_p) for n in BACKWARD_OUTPUTS])
 
 
 class MoeExpertChoiceArgs(ctypes.Structure):
@@ -104,6 +114,8 @@ def lib():
         L.moe_expert_choice_capacity.argtypes = [cfg, ctypes.POINTER(ctypes.c_int64)]
         L.moe_expert_choice_workspace_size.argtypes = [cfg, ctypes.POINTER(S)]
         L.moe_expert_choice_forward.argtypes = [cfg, ctypes.POINTER(MoeExpertChoiceArgs), P, S, P]
+        L.moe_backward_workspace_size.argtypes = [cfg, ctypes.POINTER(S)]
+        L.moe_backward.argtypes = [cfg, ctypes.POINTER(MoeBackwardArgs), P, S, P]
         for name in EXPORTED:
             if name != "moe_status_str":
                 getattr(L, name).restype = ctypes.c_int
@@ -192,7 +204,8 @@ def moe_combine(cfg, y_perm, slot_row, topk_w, y, ws, stream=None):
 
 FORWARD_INPUTS = ("x", "w_gate", "logit_bias", "noise", "w1", "b1", "w2", "b2")
 FORWARD_OUTPUTS = ("y", "logits", "topk_idx", "topk_w", "counts", "aux_loss", "offsets",
-                   "kept_counts", "slot_row", "row_token", "dropped", "routing_stats")
+                   "kept_counts", "slot_row", "row_token", "dropped", "routing_stats", "x_perm",
+                   "h_act", "y_perm", "h_pre")
 
 # Order of the routing statistics (include/moe.h, MOE_STAT_*).
 ROUTING_STATS = ("cv", "dead_ratio", "max_over_avg", "entropy", "effective_experts",
@@ -280,3 +293,31 @@ def moe_expert_choice_forward(cfg, inputs: dict, outputs: dict, ws, stream=None,
     _check(lib().moe_expert_choice_forward(ctypes.byref(cfg), ctypes.byref(args), _p(ws),
                                            ws.numel() * ws.element_size(), _stream(stream)),
            "moe_expert_choice_forward")
+
+
+def moe_backward_workspace_size(cfg: MoeConfig) -> int:
+    v = ctypes.c_size_t()
+    _check(lib().moe_backward_workspace_size(ctypes.byref(cfg), ctypes.byref(v)),
+           "moe_backward_workspace_size")
+    return v.value
+
+
+def backward_args(inputs: dict, outputs: dict, d_aux: float) -> MoeBackwardArgs:
+    """Build the moe_backward_args struct (missing keys -> NULL)."""
+    a = MoeBackwardArgs()
+    for n in BACKWARD_INPUTS:
+        setattr(a, n, _p(inputs.get(n)))
+    a.d_aux = float(d_aux)
+    for n in BACKWARD_OUTPUTS:
+        setattr(a, n, _p(outputs.get(n)))
+    return a
+
+
+def moe_backward(cfg, inputs: dict, outputs: dict, d_aux: float, ws, stream=None,
+                 args: MoeBackwardArgs = None):
+    """Gradients of the layer.  ``inputs``: dy and the forward's inputs / saved outputs
+    (BACKWARD_INPUTS); ``outputs``: dx and any parameter gradients wanted."""
+    if args is None:
+        args = backward_args(inputs, outputs, d_aux)
+    _check(lib().moe_backward(ctypes.byref(cfg), ctypes.byref(args), _p(ws),
+                              ws.numel() * ws.element_size(), _stream(stream)), "moe_backward")

@@ -246,6 +246,25 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t smem_addr) {
   return d;
 }
 
+// Shared-memory descriptor of an MN-major operand tile stored as 128-byte-swizzled
+// boxes of [K rows x 64 MN elements] (8 KB each for 64 K rows), one box per 64 MN
+// elements, boxes `atom_stride` bytes apart: the 8-row K groups are 1024 B apart
+// (stride byte offset) and the 64-element MN atoms `atom_stride` apart (leading
+// byte offset).  A 16-deep K step advances the start address by 2048 B.
+__device__ __forceinline__ uint64_t sw128_mnmajor_desc(uint32_t smem_addr, uint32_t atom_stride) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((atom_stride >> 4) & 0x3FFFu) << 16;  // leading byte offset
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;                      // stride byte offset
+  d |= static_cast<uint64_t>(1) << 46;                              // descriptor version
+  d |= static_cast<uint64_t>(2) << 61;                              // 128-byte swizzle
+  return d;
+}
+
+// Instruction-descriptor bits marking A / B as MN-major.
+constexpr uint32_t kIdescAMnMajor = 1u << 15;
+constexpr uint32_t kIdescBMnMajor = 1u << 16;
+
 // Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulator (bits 4-5 = 1),
 // A and B bf16 (bits 7-9 = 1, bits 10-12 = 1), both K-major (bits 15, 16 = 0),
 // N/8 in bits 17-22 and M/16 in bits 24-28.

@@ -114,7 +114,10 @@ __global__ void __launch_bounds__(256) simt_gemm_f32_kernel(GemmArgs p) {
         if (n >= p.N) continue;
         float v = acc[i][j];
         if (bias) v += (EPI == EPI_ROUTER_F32) ? bias[n] : bias[static_cast<int64_t>(g) * p.N + n];
-        if (EPI == EPI_BIAS_SILU) v = v / (1.f + expf(-v));
+        if (EPI == EPI_BIAS_SILU) {
+          if (p.pre_out) static_cast<float*>(p.pre_out)[r * p.N + n] = v;
+          v = v / (1.f + expf(-v));
+        }
         out[r * p.N + n] = v;
       }
     }

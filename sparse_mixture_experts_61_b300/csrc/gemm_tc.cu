@@ -36,223 +36,10 @@
 //
 // The router keeps tokens as M (128 rows per tile) and the E experts as N.
 
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
-#include <algorithm>
-#include <mutex>
-
-#include "common.cuh"
-#include "kernels.h"
+#include "tc_pipe.cuh"
 
 namespace moe {
 namespace {
-
-constexpr int TC_BK = 64;  // 64 bf16 = 128 bytes = one swizzle row
-constexpr int TC_THREADS = 192;
-// The row-tile expert GEMM runs two epilogue warps per TMEM lane quadrant (each takes
-// half of the tile's columns): 64 + 256 threads.
-constexpr int ROWS_EPI_WARPS = 8;
-constexpr int ROWS_THREADS = 64 + 32 * ROWS_EPI_WARPS;
-constexpr int TILE_M = 128;
-
-template <int A_BYTES, int B_BYTES, int STAGES>
-struct PipeSmem {
-  uint8_t a[STAGES][A_BYTES];
-  uint8_t b[STAGES][B_BYTES];
-  uint64_t full[STAGES];
-  uint64_t empty[STAGES];
-  uint64_t tfull[2];
-  uint64_t tempty[2];
-  uint64_t drain;
-  uint32_t tmem_base;
-  int abort;
-  int pref[kMaxExperts + 1];  // per-group prefix of tile units
-};
-
-// Wait used only while unwinding: bounded by time, ignores the abort flag.
-__device__ __forceinline__ void mbar_wait_unwind(uint32_t bar, uint32_t parity) {
-  const uint64_t t0 = global_ns();
-  while (!mbar_try_wait(bar, parity))
-    if (global_ns() - t0 > kWaitLimitNs) return;
-}
-
-// Barrier set-up, TMEM allocation and the per-group prefix of ceil(rows_g / unit)
-// (rows_g from the offsets, or m_rows for a single dense group).  All threads call.
-// CTAS = CTAs per cluster whose MMAs read (and so must release) each stage.
-template <class Smem, int STAGES, int CTAS>
-__device__ __forceinline__ void pipe_prologue(Smem& S, uint32_t tmem_cols, const GemmArgs& p,
-                                              int G, int unit, const void* tmA,
-                                              const void* tmB, uint32_t epi_threads = 128) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (threadIdx.x == 0) {
-#pragma unroll
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(smem_u32(&S.full[s]), 1);
-      mbar_init(smem_u32(&S.empty[s]), CTAS);
-    }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(smem_u32(&S.tfull[i]), 1);
-      mbar_init(smem_u32(&S.tempty[i]), epi_threads);
-    }
-    mbar_init(smem_u32(&S.drain), 1);
-    S.abort = 0;
-    fence_mbar_init();
-    tma_prefetch_desc(tmA);
-    tma_prefetch_desc(tmB);
-  }
-  if (warp == 1) {
-    tmem_alloc(smem_u32(&S.tmem_base), tmem_cols);
-    tmem_relinquish();
-  }
-  if (warp == 0) {
-    int carry = 0;
-    if (lane == 0) S.pref[0] = 0;
-    for (int base = 0; base < G; base += 32) {
-      const int g = base + lane;
-      int units = 0;
-      if (g < G) {
-        const int64_t rows = p.offsets ? (p.offsets[g + 1] - p.offsets[g]) : p.m_rows;
-        units = rows > 0 ? static_cast<int>((rows + unit - 1) / unit) : 0;
-      }
-      int v = units;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int n = __shfl_up_sync(0xffffffffu, v, o);
-        if (lane >= o) v += n;
-      }
-      if (g < G) S.pref[g + 1] = carry + v;
-      carry += __shfl_sync(0xffffffffu, v, 31);
-    }
-  }
-  tc_fence_before();
-  if (CTAS > 1)
-    cluster_sync_all();  // peers' barriers are initialised before anyone multicasts
-  else
-    __syncthreads();
-  tc_fence_after();
-}
-
-// Group of a tile: the g with pref[g]*per <= tile < pref[g+1]*per.
-__device__ __forceinline__ int find_group(const int* pref, int G, int per, int tile) {
-  int lo = 0, hi = G;
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (pref[mid] * per <= tile) lo = mid; else hi = mid;
-  }
-  return lo;
-}
-
-// Warp 0, lane 0, over tiles first, first + step, ...  decode(tile) -> coordinates
-// with the stage's byte count in .bytes and the tile's k-blocks [.kb0, .kb1);
-// load(coords, kb, smem_a, smem_b, bar).
-template <int STAGES, class Smem, class Decode, class Load>
-__device__ __forceinline__ void run_producer(Smem& S, int first, int step, int total,
-                                             Decode decode, Load load, volatile int* abort,
-                                             int* flags) {
-  int s = 0;
-  uint32_t ph = 0, issued = 0, issued_par = 0;
-  bool ok = true;
-  for (int tile = first; ok && tile < total; tile += step) {
-    const auto c = decode(tile);
-    for (int kb = c.kb0; kb < c.kb1; ++kb) {
-      if (!mbar_wait_bounded(smem_u32(&S.empty[s]), ph ^ 1u, abort, flags)) {
-        ok = false;
-        break;
-      }
-      const uint32_t fb = smem_u32(&S.full[s]);
-      mbar_arrive_expect_tx(fb, c.bytes);
-      load(c, kb, smem_u32(S.a[s]), smem_u32(S.b[s]), fb);
-      issued |= 1u << s;
-      issued_par = (issued_par & ~(1u << s)) | (ph << s);
-      if (++s == STAGES) {
-        s = 0;
-        ph ^= 1u;
-      }
-    }
-  }
-  if (!ok) {
-    // Unwinding: let this CTA's copies in flight land before it exits.
-    for (int q = 0; q < STAGES; ++q)
-      if ((issued >> q) & 1u) mbar_wait_unwind(smem_u32(&S.full[q]), (issued_par >> q) & 1u);
-  }
-}
-
-// Warp 1, lane 0.  decode(tile) -> coordinates with the k-block range [.kb0, .kb1);
-// idesc_of(coords) -> instruction descriptor of the tile's MMAs.  With CTAS = 2 each
-// stage is released on both CTAs of the cluster.
-template <int STAGES, int ACC_COLS, int CTAS, class Smem, class Decode, class Idesc>
-__device__ __forceinline__ void run_mma(Smem& S, int first, int step, int total,
-                                        uint32_t tmem_base, Decode decode, Idesc idesc_of,
-                                        volatile int* abort, int* flags) {
-  int s = 0, acc = 0;
-  uint32_t ph = 0, aph = 0;
-  bool ok = true, issued_any = false;
-  for (int tile = first; ok && tile < total; tile += step) {
-    const auto c = decode(tile);
-    const uint32_t idesc = idesc_of(c);
-    if (!mbar_wait_bounded(smem_u32(&S.tempty[acc]), aph ^ 1u, abort, flags)) {
-      ok = false;
-      break;
-    }
-    tc_fence_after();
-    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * ACC_COLS);
-    for (int kb = c.kb0; kb < c.kb1; ++kb) {
-      if (!mbar_wait_bounded(smem_u32(&S.full[s]), ph, abort, flags)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const uint32_t a0 = smem_u32(S.a[s]), b0 = smem_u32(S.b[s]);
-#pragma unroll
-      for (int kk = 0; kk < TC_BK / 16; ++kk)
-        tc_mma_bf16(d_tmem, sw128_kmajor_desc(a0 + kk * 32), sw128_kmajor_desc(b0 + kk * 32),
-                    idesc, (kb != c.kb0 || kk != 0) ? 1u : 0u);
-      issued_any = true;
-      if (CTAS > 1)
-        tc_commit_multicast(smem_u32(&S.empty[s]), static_cast<uint16_t>((1u << CTAS) - 1u));
-      else
-        tc_commit(smem_u32(&S.empty[s]));
-      if (++s == STAGES) {
-        s = 0;
-        ph ^= 1u;
-      }
-    }
-    if (!ok) break;
-    tc_commit(smem_u32(&S.tfull[acc]));
-    acc ^= 1;
-    if (acc == 0) aph ^= 1u;
-  }
-  // Unwinding: every MMA issued by this thread completes before TMEM is released.
-  // (On the normal path the epilogue has already waited for all of them.)
-  if (!ok && issued_any) {
-    tc_commit(smem_u32(&S.drain));
-    mbar_wait_unwind(smem_u32(&S.drain), 0);
-  }
-}
-
-// With CTAS > 1 no CTA leaves before its peer has stopped writing into its shared
-// memory (multicast copies, commit arrivals).
-template <int CTAS, class Smem>
-__device__ __forceinline__ void pipe_teardown(Smem& S, uint32_t tmem_cols) {
-  tc_fence_before();
-  __syncthreads();
-  if ((threadIdx.x >> 5) == 1) {
-    __syncwarp();
-    tc_fence_after();
-    tmem_dealloc(S.tmem_base, tmem_cols);
-  }
-  if (CTAS > 1) cluster_sync_all();
-}
-
-template <class Smem>
-__device__ __forceinline__ Smem& smem_aligned() {
-  extern __shared__ uint8_t smem_raw[];
-  return *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                  ~static_cast<uintptr_t>(1023));
-}
-
-__device__ __forceinline__ float silu(float x) { return x / (1.f + __expf(-x)); }
 
 // ------------------------------------------------------------- expert FFN GEMM
 // A = weight block [128 x 64] of W[g] (3-D map over [G, N, K]); B = token block of
@@ -354,7 +141,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
           for (int i = 0; i < 32; ++i) {
             if (col + i < nrows) {
               float x = v[i] + b;
-              if (EPI == EPI_BIAS_SILU) x = silu(x);
+              if (EPI == EPI_BIAS_SILU) {
+                if (p.pre_out)
+                  static_cast<__nv_bfloat16*>(p.pre_out)[(o - out) + static_cast<int64_t>(i) * p.N] =
+                      __float2bfloat16_rn(x);
+                x = silu(x);
+              }
               o[static_cast<int64_t>(i) * p.N] = __float2bfloat16_rn(x);
             }
           }
@@ -475,25 +267,35 @@ __global__ void __launch_bounds__(ROWS_THREADS, 1)
               b[i] = (bias && c.n0 + col + 8 * q + i < p.N) ? __bfloat162float(bias[col + 8 * q + i])
                                                               : 0.f;
           }
-          uint4 packed;
+          uint4 packed, pre;
           __nv_bfloat162* ph = reinterpret_cast<__nv_bfloat162*>(&packed);
+          __nv_bfloat162* pp = reinterpret_cast<__nv_bfloat162*>(&pre);
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             float x0 = v[8 * q + 2 * i] + b[2 * i];
             float x1 = v[8 * q + 2 * i + 1] + b[2 * i + 1];
             if (EPI == EPI_BIAS_SILU) {
+              pp[i] = __floats2bfloat162_rn(x0, x1);
               x0 = silu(x0);
               x1 = silu(x1);
             }
             ph[i] = __floats2bfloat162_rn(x0, x1);
           }
+          __nv_bfloat16* op = (EPI == EPI_BIAS_SILU && p.pre_out)
+                                  ? static_cast<__nv_bfloat16*>(p.pre_out) + (o - out)
+                                  : nullptr;
           if (whole) {
             *reinterpret_cast<uint4*>(o + 8 * q) = packed;
+            if (op) *reinterpret_cast<uint4*>(op + 8 * q) = pre;
           } else {
             const __nv_bfloat16* pv = reinterpret_cast<const __nv_bfloat16*>(&packed);
+            const __nv_bfloat16* pr = reinterpret_cast<const __nv_bfloat16*>(&pre);
 #pragma unroll
             for (int i = 0; i < 8; ++i)
-              if (c.n0 + col + 8 * q + i < p.N) o[8 * q + i] = pv[i];
+              if (c.n0 + col + 8 * q + i < p.N) {
+                o[8 * q + i] = pv[i];
+                if (op) op[8 * q + i] = pr[i];
+              }
           }
         }
       }
@@ -601,83 +403,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     }
   }
   pipe_teardown<1>(S, kTmemCols);
-}
-
-// ------------------------------------------------------------------ host side
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  });
-  return fn;
-}
-
-bool encode_bf16_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
-                     const cuuint64_t* strides_bytes, const cuuint32_t* box) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  cuuint32_t estr[3] = {1, 1, 1};
-  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims,
-                        strides_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
-// 2-D map over a row-major [rows, K] bf16 matrix, box [box_rows x box_cols].
-bool rows_map(CUtensorMap* m, const void* base, int64_t rows, int K, int box_rows,
-              int box_cols = TC_BK) {
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
-  const cuuint64_t str[1] = {static_cast<cuuint64_t>(K) * 2};
-  const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
-  return encode_bf16_map(m, base, 2, dims, str, box);
-}
-
-// 3-D map over stacked [G, N, K] bf16 weights, box [box_rows x 64] of one group.
-bool stacked_map(CUtensorMap* m, const void* base, int G, int N, int K, int box_rows) {
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(N),
-                              static_cast<cuuint64_t>(G)};
-  const cuuint64_t str[2] = {static_cast<cuuint64_t>(K) * 2, static_cast<cuuint64_t>(N) * K * 2};
-  const cuuint32_t box[3] = {TC_BK, static_cast<cuuint32_t>(box_rows), 1};
-  return encode_bf16_map(m, base, 3, dims, str, box);
-}
-
-template <class Kern>
-cudaError_t launch_pipe(Kern kern, size_t smem, int grid, const CUtensorMap& a,
-                        const CUtensorMap& b, const GemmArgs& args, cudaStream_t stream,
-                        int threads = TC_THREADS) {
-  if (grid <= 0) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
-  if (e != cudaSuccess) return e;
-  kern<<<grid, threads, smem, stream>>>(a, b, args);
-  return cudaGetLastError();
-}
-
-// Clusters of two that can be resident at once (one CTA per SM), per device.
-template <class Kern>
-int resident_clusters(Kern kern, size_t smem, int sm_count) {
-  static int cached[64] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return sm_count / 2;
-  if (cached[dev] > 0) return cached[dev];
-  int n = 0;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(sm_count / 2 * 2));
-  cfg.blockDim = dim3(TC_THREADS);
-  cfg.dynamicSmemBytes = smem;
-  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
-    (void)cudaGetLastError();
-    n = sm_count / 2;
-  }
-  cached[dev] = n;
-  return n;
 }
 
 template <int TB, int STAGES, int EPI>

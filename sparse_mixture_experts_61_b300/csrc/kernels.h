@@ -83,6 +83,14 @@ struct GemmArgs {
   int ksplit;             // router: K splits; split s writes out + s * split_stride
   int64_t split_stride;
   int* flags;
+  void* pre_out;          // EPI_BIAS_SILU: also writes the pre-activation (before SiLU), or nullptr
+  // Backward epilogues: EPI_DSILU multiplies by SiLU'(aux_in[row, n]) (the saved
+  // pre-activation); EPI_DX adds aux_in[slots[row, j], n] for j < nslots (slot < 0
+  // skipped).
+  const void* aux_in;
+  const int32_t* slots;
+  int nslots;
+  int64_t b_rows;  // backward B [G][b_rows][N] when b_rows differs from K (rows past it read 0)
 };
 
 // K splits of the bf16 router contraction for T tokens, E experts, model width d on a
@@ -92,7 +100,61 @@ struct GemmArgs {
 int router_splits(int64_t T, int E, int d, int sms);
 constexpr int kMaxSmsForSizing = 160;
 
-enum Epilogue { EPI_BIAS_SILU = 0, EPI_BIAS = 1, EPI_ROUTER_F32 = 2 };
+enum Epilogue {
+  EPI_BIAS_SILU = 0,
+  EPI_BIAS = 1,
+  EPI_ROUTER_F32 = 2,
+  EPI_DSILU = 3,  // out = acc * SiLU'(pre)
+  EPI_PLAIN = 4,  // out = acc
+  EPI_DX = 5      // out = acc + sum_j rows[slots[row, j]]
+};
+
+// Backward GEMMs on row tiles (bf16): A [rows, K] K-major as in the forward, B stored
+// [G][K][N] (N contiguous: the forward weights read transposed, MN-major), epilogue
+// EPI_DSILU, EPI_PLAIN or EPI_DX, bf16 output [rows, N].  offsets == nullptr: one
+// dense group of m_rows rows.
+cudaError_t launch_tc_bwd_rows(const GemmArgs& a, int epi, int sm_count, cudaStream_t stream);
+
+// Weight gradients: for each group g with rows [offsets[g], offsets[g+1]) (or one
+// group of m_rows rows when offsets == nullptr):
+//   out[g][m][n] = sum_{r in g} A[r][m] * B[r][n],  m < Mdim, n < Ndim,
+// A [rows, Mdim] and B [rows, Ndim] bf16 row-major (both read MN-major), fp32
+// accumulation, out bf16 or fp32; a group without rows gets zeros.
+struct WgradArgs {
+  const void* A;
+  int Mdim;
+  const void* B;
+  int Ndim;
+  const int32_t* offsets;
+  int64_t m_rows;
+  int64_t rows_alloc;  // rows of the A and B buffers
+  int G;
+  void* out;
+  bool out_f32;
+  int* flags;
+};
+cudaError_t launch_tc_wgrad(const WgradArgs& a, int sm_count, cudaStream_t stream);
+
+// Backward of the combine: for kept slot (t,j) in row r = slot_row[t,j]:
+//   dy_perm[r] = topk_w[t,j] * dy[t] (bf16),  dw[t,j] = <dy[t], y_perm[r]> (fp32);
+// a dropped slot gets dw = 0.
+cudaError_t launch_bwd_combine(const void* dy, const void* y_perm, const int32_t* slot_row,
+                               const float* topk_w, int64_t T, int d, int k, void* dy_perm,
+                               float* dw, cudaStream_t stream);
+
+// Backward of the gate and the balance loss to the logits: dl [T,E] fp32 and its bf16
+// copy dl16 [T,Epad] (columns E..Epad-1 zero, Epad <= 256).
+cudaError_t launch_bwd_gate(const float* logits, const int32_t* topk_idx, const float* topk_w,
+                            const float* dw, const int32_t* counts, float d_aux, int64_t T,
+                            int E, int Epad, int k, float* dl, void* dl16, cudaStream_t stream);
+
+// Column sums per group: out[g][c] = sum over rows r of group g of A[r][c] (rows in
+// order within 64-row slices, slices in order), A bf16 (a_f32 = false) or fp32.
+// partial: workspace of colsum_partial_floats(...) floats.
+int64_t colsum_partial_floats(int64_t rows_alloc, int G, int C);
+cudaError_t launch_colsum(const void* A, bool a_f32, int C, const int32_t* offsets, int64_t m_rows,
+                          int64_t rows_alloc, int G, float* partial, float* out,
+                          cudaStream_t stream);
 
 // fp32 SIMT grouped GEMM (fp32 operands, fp32 bias and output).
 cudaError_t launch_simt_gemm_f32(const GemmArgs& a, int epi, int sm_count, cudaStream_t stream);

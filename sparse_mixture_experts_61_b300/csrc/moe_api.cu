@@ -4,6 +4,7 @@
 
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdint>
@@ -168,9 +169,11 @@ moe_status run_router(const moe_config& c, const Layout& L, void* ws, const void
 moe_status run_expert_ffn_rows(const moe_config& c, int64_t rows_alloc, int64_t max_group,
                                const void* x_perm, const int32_t* offsets, const void* w1,
                                const void* b1, const void* w2, const void* b2, void* h_buf,
-                               void* y_perm, int* flags, int sms, cudaStream_t st) {
+                               void* y_perm, int* flags, int sms, cudaStream_t st,
+                               void* h_pre = nullptr) {
   GemmArgs g1{};
   g1.A = x_perm;
+  g1.pre_out = h_pre;
   g1.rows_alloc = rows_alloc;
   g1.B = w1;
   g1.bias = b1;
@@ -183,6 +186,7 @@ moe_status run_expert_ffn_rows(const moe_config& c, int64_t rows_alloc, int64_t 
   g1.flags = flags;
   GemmArgs g2 = g1;
   g2.A = h_buf;
+  g2.pre_out = nullptr;
   g2.B = w2;
   g2.bias = b2;
   g2.out = y_perm;
@@ -202,10 +206,11 @@ moe_status run_expert_ffn_rows(const moe_config& c, int64_t rows_alloc, int64_t 
 // at most C with a capacity; the tile height follows this bound.
 moe_status run_expert_ffn(const moe_config& c, const void* x_perm, const int32_t* offsets,
                           const void* w1, const void* b1, const void* w2, const void* b2,
-                          void* h_buf, void* y_perm, int* flags, int sms, cudaStream_t st) {
+                          void* h_buf, void* y_perm, int* flags, int sms, cudaStream_t st,
+                          void* h_pre = nullptr) {
   const int64_t C = capacity_of(c);
   return run_expert_ffn_rows(c, c.T * c.k, C >= 0 && C < c.T ? C : c.T, x_perm, offsets, w1, b1,
-                             w2, b2, h_buf, y_perm, flags, sms, st);
+                             w2, b2, h_buf, y_perm, flags, sms, st, h_pre);
 }
 
 // ---------------------------------------------------------------- expert choice
@@ -419,7 +424,8 @@ MOE_EXPORT moe_status moe_forward(const moe_config* cfg, const moe_forward_args*
       !opt16(a->b1) || !need16(a->w2) || !opt16(a->b2) || !tok16(c, a->y) || !opt16(a->logits) ||
       !opt4(a->topk_idx) || !opt4(a->topk_w) || !opt4(a->counts) || !opt4(a->aux_loss) ||
       !opt4(a->offsets) || !opt4(a->kept_counts) || !opt4(a->slot_row) || !opt4(a->row_token) ||
-      !opt4(a->dropped) || !opt4(a->routing_stats) ||
+      !opt4(a->dropped) || !opt4(a->routing_stats) || !opt16(a->x_perm) || !opt16(a->h_act) ||
+      !opt16(a->y_perm) || !opt16(a->h_pre) ||
       (c.noise != MOE_NOISE_NONE ? !tok4(c, a->noise) : !opt4(a->noise)))
     return MOE_ERR_INVALID_ARGUMENT;
   const Layout L = make_layout(c);
@@ -450,9 +456,9 @@ MOE_EXPORT moe_status moe_forward(const moe_config* cfg, const moe_forward_args*
   int32_t* hist = at<int32_t>(ws, L.hist);
   int32_t* chunk_base = at<int32_t>(ws, L.chunk_base);
   float* psum = at<float>(ws, L.psum);
-  void* x_perm = at<void>(ws, L.x_perm);
-  void* h_buf = at<void>(ws, L.h_buf);
-  void* y_perm = at<void>(ws, L.y_perm);
+  void* x_perm = a->x_perm ? a->x_perm : at<void>(ws, L.x_perm);
+  void* h_buf = a->h_act ? a->h_act : at<void>(ws, L.h_buf);
+  void* y_perm = a->y_perm ? a->y_perm : at<void>(ws, L.y_perm);
   const int64_t C = capacity_of(c);
 
   if ((s = run_router(c, L, ws, a->x, a->w_gate, a->logit_bias, a->noise, a->logits, idx, w,
@@ -463,7 +469,7 @@ MOE_EXPORT moe_status moe_forward(const moe_config* cfg, const moe_forward_args*
   MOE_CUDA(launch_dispatch_place(c.dtype, idx, c.T, c.E, c.k, C, chunk_base, offsets, slot_row,
                                  row_token, a->x, x_perm, c.d, flags, st));
   if ((s = run_expert_ffn(c, x_perm, offsets, a->w1, a->b1, a->w2, a->b2, h_buf, y_perm, flags,
-                          sms, st)) != MOE_OK)
+                          sms, st, a->h_pre)) != MOE_OK)
     return s;
   MOE_CUDA(launch_combine(c.dtype, y_perm, slot_row, w, c.T, c.d, c.k, a->y, flags, st));
   return MOE_OK;
@@ -563,5 +569,178 @@ MOE_EXPORT moe_status moe_expert_choice_forward(const moe_config* cfg,
   // EC3: per-token combine over the experts that took the token.
   MOE_CUDA(launch_ec_combine(c.dtype, y_perm, rowmap, probs_et, c.T, c.E, C, c.d, a->y,
                              a->token_experts, a->unrouted, st));
+  return MOE_OK;
+}
+
+// ---------------------------------------------------------------- backward
+namespace moe {
+namespace {
+
+struct BwdLayout {
+  size_t flags, dyp, da, dxp, dw, dl, dl16, dwg, partial, total;
+  int Epad;
+};
+
+BwdLayout make_bwd_layout(const moe_config& c) {
+  BwdLayout L{};
+  const int64_t T = c.T, E = c.E, k = c.k, rows = T * k;
+  L.Epad = (c.E + 63) & ~63;  // dl16 rows span whole 64-column boxes
+  int64_t pf = colsum_partial_floats(rows, c.E, c.d);
+  pf = std::max<int64_t>(pf, colsum_partial_floats(rows, c.E, c.h));
+  pf = std::max<int64_t>(pf, colsum_partial_floats(T, 1, c.E));
+  size_t o = 0;
+  L.flags = o; o += kAlign;
+  L.dyp = o; o = align_up(o + rows * c.d * 2);
+  L.da = o; o = align_up(o + rows * c.h * 2);
+  L.dxp = o; o = align_up(o + rows * c.d * 2);
+  L.dw = o; o = align_up(o + T * k * 4);
+  L.dl = o; o = align_up(o + T * E * 4);
+  L.dl16 = o; o = align_up(o + T * L.Epad * 2);
+  L.dwg = o; o = align_up(o + static_cast<int64_t>(L.Epad) * c.d * 4);
+  L.partial = o; o = align_up(o + pf * 4);
+  L.total = o;
+  return L;
+}
+
+moe_status check_bwd_config(const moe_config* c) {
+  moe_status s = check_config(c);
+  if (s != MOE_OK) return s;
+  if (c->dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  if (c->noise != MOE_NOISE_NONE) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
+MOE_EXPORT moe_status moe_backward_workspace_size(const moe_config* cfg, size_t* bytes) {
+  moe_status s = check_bwd_config(cfg);
+  if (s != MOE_OK) return s;
+  if (!bytes) return MOE_ERR_INVALID_ARGUMENT;
+  *bytes = make_bwd_layout(*cfg).total;
+  return MOE_OK;
+}
+
+MOE_EXPORT moe_status moe_backward(const moe_config* cfg, const moe_backward_args* a, void* ws,
+                                   size_t ws_bytes, moe_stream_t stream) {
+  moe_status s = check_bwd_config(cfg);
+  if (s != MOE_OK) return s;
+  if (!a) return MOE_ERR_INVALID_ARGUMENT;
+  const moe_config& c = *cfg;
+  if (!tok16(c, a->dy) || !tok16(c, a->x) || !need16(a->w_gate) || !need16(a->w1) ||
+      !need16(a->w2) || !tok4(c, a->logits) || !tok4(c, a->topk_idx) || !tok4(c, a->topk_w) ||
+      !need4(a->counts) || !need4(a->offsets) || !tok4(c, a->slot_row) || !tok16(c, a->x_perm) ||
+      !tok16(c, a->h_pre) || !tok16(c, a->h_act) || !tok16(c, a->y_perm) || !tok16(c, a->dx) ||
+      !opt4(a->dw_gate) || !opt4(a->dlogit_bias) || !opt16(a->dw1) || !opt4(a->db1) ||
+      !opt16(a->dw2) || !opt4(a->db2) || !std::isfinite(a->d_aux))
+    return MOE_ERR_INVALID_ARGUMENT;
+  const BwdLayout L = make_bwd_layout(c);
+  if (!ws || !al16(ws) || ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int* flags = at<int>(ws, L.flags);
+  MOE_CUDA(cudaMemsetAsync(flags, 0, sizeof(int), st));
+  const int64_t rows = c.T * c.k;
+  if (c.T == 0) {
+    // No tokens: every parameter gradient is zero.
+    if ((s = zero_async(a->dw_gate, sizeof(float) * c.E * c.d, st)) != MOE_OK) return s;
+    if ((s = zero_async(a->dlogit_bias, sizeof(float) * c.E, st)) != MOE_OK) return s;
+    if ((s = zero_async(a->dw1, size_t{2} * c.E * c.h * c.d, st)) != MOE_OK) return s;
+    if ((s = zero_async(a->db1, sizeof(float) * c.E * c.h, st)) != MOE_OK) return s;
+    if ((s = zero_async(a->dw2, size_t{2} * c.E * c.d * c.h, st)) != MOE_OK) return s;
+    return zero_async(a->db2, sizeof(float) * c.E * c.d, st);
+  }
+  const int sms = sm_count();
+  if (sms <= 0) return MOE_ERR_CUDA;
+  void* dyp = at<void>(ws, L.dyp);
+  void* da = at<void>(ws, L.da);
+  void* dxp = at<void>(ws, L.dxp);
+  float* dw = at<float>(ws, L.dw);
+  float* dl = at<float>(ws, L.dl);
+  void* dl16 = at<void>(ws, L.dl16);
+  float* partial = at<float>(ws, L.partial);
+
+  // Combine and gate backward: dYp, dw, then dl (gate + balance loss).
+  MOE_CUDA(launch_bwd_combine(a->dy, a->y_perm, a->slot_row, a->topk_w, c.T, c.d, c.k, dyp, dw, st));
+  MOE_CUDA(launch_bwd_gate(a->logits, a->topk_idx, a->topk_w, dw, a->counts, a->d_aux, c.T, c.E,
+                           L.Epad, c.k, dl, dl16, st));
+  // Data gradients: dA = (dYp W2) * SiLU'(A), dXp = dA W1, dx = dl W_g + sum_j dXp.
+  GemmArgs g{};
+  g.A = dyp;
+  g.rows_alloc = rows;
+  g.B = a->w2;
+  g.offsets = a->offsets;
+  g.G = c.E;
+  g.N = c.h;
+  g.K = c.d;
+  g.out = da;
+  g.aux_in = a->h_pre;
+  g.flags = flags;
+  MOE_CUDA(launch_tc_bwd_rows(g, EPI_DSILU, sms, st));
+  g.A = da;
+  g.B = a->w1;
+  g.N = c.d;
+  g.K = c.h;
+  g.out = dxp;
+  g.aux_in = nullptr;
+  MOE_CUDA(launch_tc_bwd_rows(g, EPI_PLAIN, sms, st));
+  GemmArgs r{};
+  r.A = dl16;
+  r.m_rows = c.T;
+  r.B = a->w_gate;
+  r.G = 1;
+  r.N = c.d;
+  r.K = L.Epad;
+  r.b_rows = c.E;
+  r.out = a->dx;
+  r.aux_in = dxp;
+  r.slots = a->slot_row;
+  r.nslots = c.k;
+  r.flags = flags;
+  MOE_CUDA(launch_tc_bwd_rows(r, EPI_DX, sms, st));
+  // Weight gradients.
+  WgradArgs wg{};
+  wg.offsets = a->offsets;
+  wg.rows_alloc = rows;
+  wg.G = c.E;
+  wg.flags = flags;
+  if (a->dw2) {
+    wg.A = dyp;
+    wg.Mdim = c.d;
+    wg.B = a->h_act;
+    wg.Ndim = c.h;
+    wg.out = a->dw2;
+    MOE_CUDA(launch_tc_wgrad(wg, sms, st));
+  }
+  if (a->dw1) {
+    wg.A = da;
+    wg.Mdim = c.h;
+    wg.B = a->x_perm;
+    wg.Ndim = c.d;
+    wg.out = a->dw1;
+    MOE_CUDA(launch_tc_wgrad(wg, sms, st));
+  }
+  if (a->dw_gate) {
+    WgradArgs rg{};
+    rg.A = dl16;
+    rg.Mdim = L.Epad;
+    rg.B = a->x;
+    rg.Ndim = c.d;
+    rg.m_rows = c.T;
+    rg.rows_alloc = c.T;
+    rg.G = 1;
+    rg.out = at<float>(ws, L.dwg);
+    rg.out_f32 = true;
+    rg.flags = flags;
+    MOE_CUDA(launch_tc_wgrad(rg, sms, st));
+    MOE_CUDA(cudaMemcpyAsync(a->dw_gate, at<float>(ws, L.dwg), sizeof(float) * c.E * c.d,
+                             cudaMemcpyDeviceToDevice, st));
+  }
+  // Bias gradients: column sums per expert (fixed order).
+  if (a->db2)
+    MOE_CUDA(launch_colsum(dyp, false, c.d, a->offsets, 0, rows, c.E, partial, a->db2, st));
+  if (a->db1)
+    MOE_CUDA(launch_colsum(da, false, c.h, a->offsets, 0, rows, c.E, partial, a->db1, st));
+  if (a->dlogit_bias)
+    MOE_CUDA(launch_colsum(dl, true, c.E, nullptr, c.T, c.T, 1, partial, a->dlogit_bias, st));
   return MOE_OK;
 }

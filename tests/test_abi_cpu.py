@@ -55,7 +55,10 @@ def test_struct_layouts_match_header():
     assert ctypes.sizeof(moe.MoeConfig) == 48
     assert moe.MoeConfig.noise.offset == 40
     assert moe.MoeConfig.capacity_factor.offset == 32
-    assert ctypes.sizeof(moe.MoeForwardArgs) == 20 * 8
+    assert ctypes.sizeof(moe.MoeForwardArgs) == 24 * 8
+    assert ctypes.sizeof(moe.MoeBackwardArgs) == 15 * 8 + 8 + 7 * 8
+    assert moe.MoeBackwardArgs.d_aux.offset == 15 * 8
+    assert moe.MoeBackwardArgs.dx.offset == 16 * 8
     assert ctypes.sizeof(moe.MoeExpertChoiceArgs) == 14 * 8
 
 
@@ -223,3 +226,47 @@ def test_expert_choice_pointer_and_workspace_checks(L):
     assert f(ctypes.byref(cfg), ctypes.byref(a), FAKE, need - 1, None) == WS
     assert f(ctypes.byref(cfg), ctypes.byref(a), None, need, None) == WS
     assert f(ctypes.byref(cfg), ctypes.byref(a), FAKE_ODD, need, None) == WS
+
+
+# ---------------------------------------------------------------- backward
+@pytest.mark.parametrize("kw,status", [
+    (dict(dtype="f32"), moe.MOE_ERR_UNSUPPORTED),
+    (dict(noise=1), moe.MOE_ERR_UNSUPPORTED),
+    (dict(k=9), moe.MOE_ERR_UNSUPPORTED),
+    (dict(gate=5), moe.MOE_ERR_INVALID_ARGUMENT),
+    (dict(), moe.MOE_OK),
+])
+def test_backward_config_validation(L, kw, status):
+    base = dict(T=64, d=64, h=128, E=8, k=2, dtype="bf16", gate=0, capacity_factor=0.0)
+    base.update(kw)
+    cfg = moe.config(**base)
+    n = ctypes.c_size_t()
+    assert L.moe_backward_workspace_size(ctypes.byref(cfg), ctypes.byref(n)) == status
+
+
+def test_backward_pointer_and_workspace_checks(L):
+    cfg = moe.config(64, 64, 128, 8, 2)
+    need = moe.moe_backward_workspace_size(cfg)
+    assert need >= 64 * 2 * (64 + 128 + 64) * 2  # dYp, dA, dXp row buffers
+    INV, WS = moe.MOE_ERR_INVALID_ARGUMENT, moe.MOE_ERR_WORKSPACE
+    ok = {n: FAKE for n in moe.BACKWARD_INPUTS}
+    ok["dx"] = FAKE
+    f = L.moe_backward
+
+    def args(**kw):
+        d = dict(ok, **kw)
+        a = moe.MoeBackwardArgs()
+        for n, v in d.items():
+            setattr(a, n, v)
+        return a
+
+    assert f(ctypes.byref(cfg), None, FAKE, need, None) == INV
+    for drop in list(ok):
+        a = args(**{drop: None})
+        assert f(ctypes.byref(cfg), ctypes.byref(a), FAKE, need, None) == INV, drop
+    a = args(dw1=FAKE_ODD)
+    assert f(ctypes.byref(cfg), ctypes.byref(a), FAKE, need, None) == INV
+    a = args(d_aux=float("nan"))
+    assert f(ctypes.byref(cfg), ctypes.byref(a), FAKE, need, None) == INV
+    a = args()
+    assert f(ctypes.byref(cfg), ctypes.byref(a), FAKE, need - 1, None) == WS

@@ -523,3 +523,15 @@ def test_backward_without_upstream_gradient_is_the_balance_loss_gradient():
     g0 = oracle.backward(inp, zero, 2, 0, None, 0.0)
     for key, v in g0.items():
         assert np.all(v == 0.0), key
+
+
+def test_backward_on_given_logits_equals_recomputed():
+    """Passing the layer's own logits in reproduces the self-contained backward exactly."""
+    rng = np.random.default_rng(5)
+    inp = _tiny_f64_layer(rng)
+    G = rng.standard_normal(inp["x"].shape)
+    lg = oracle.forward(inp, 2, 1, 1.0)["logits"]
+    a = oracle.backward(inp, G, 2, 1, 1.0, 0.2)
+    b = oracle.backward(inp, G, 2, 1, 1.0, 0.2, logits_in=lg)
+    for key in a:
+        np.testing.assert_array_equal(a[key], b[key], err_msg=key)
