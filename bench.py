@@ -49,6 +49,11 @@ DEFAULT_WORKLOAD = "mixtral_prefill"
 L2_FLUSH_BYTES = 256 << 20
 KERNELS_PER_FORWARD = 8   # router GEMM, softmax/top-k, finalize/scan, place, gather, GEMM1, GEMM2, combine
 KERNELS_PER_EC_FORWARD = 7  # router GEMM, softmax, per-expert select, gather, GEMM1, GEMM2, combine
+# moe_backward: combine and gate backward, dA / dXp / dx GEMMs, dW2 / dW1 / dW_g GEMMs, three
+# two-kernel column sums
+KERNELS_PER_BACKWARD = 14
+TRAIN_METRIC = "MoE-layer fwd+bwd (training step) tokens/s at 1 B300; backward GEMMs % BF16 peak"
+D_AUX = 0.01
 
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the grouped GEMM pair
 # (G1 + G2), from the ncu capture summarised in
@@ -448,6 +453,121 @@ def run_ours(args, world, rank, local):
     return line
 
 
+# ------------------------------------------------------------------ training step
+def run_train(args, world, rank, local):
+    """Forward (keeping its activations) + backward of the layer per step."""
+    import sparse_mixture_experts_61_b300 as moe
+
+    moe.lib()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = WORKLOADS[args.workload]
+    if w.routing != "topk" or w.dtype != "bf16":
+        raise SystemExit("--pass train needs a bf16 top-k workload")
+    inp = make_inputs(w, seed=rank, device=str(dev))
+    cfg = moe.config_from_workload(w)
+    T, d, h, E, k = w.T, w.d, w.h, w.E, w.k
+    rows = T * k
+    i32 = dict(dtype=torch.int32, device=dev)
+    f32 = dict(dtype=torch.float32, device=dev)
+    bf = dict(dtype=torch.bfloat16, device=dev)
+    outs = dict(y=torch.empty((T, d), **bf), logits=torch.empty((T, E), **f32),
+                topk_idx=torch.empty((T, k), **i32), topk_w=torch.empty((T, k), **f32),
+                counts=torch.empty((E,), **i32), aux_loss=torch.empty((1,), **f32),
+                offsets=torch.empty((E + 1,), **i32), kept_counts=torch.empty((E,), **i32),
+                slot_row=torch.empty((T, k), **i32), x_perm=torch.empty((rows, d), **bf),
+                h_act=torch.empty((rows, h), **bf), y_perm=torch.empty((rows, d), **bf),
+                h_pre=torch.empty((rows, h), **bf))
+    grads = dict(dx=torch.empty((T, d), **bf), dw_gate=torch.empty((E, d), **f32),
+                 dlogit_bias=torch.empty((E,), **f32), dw1=torch.empty((E, h, d), **bf),
+                 db1=torch.empty((E, h), **f32), dw2=torch.empty((E, d, h), **bf),
+                 db2=torch.empty((E, d), **f32))
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1000 + rank)
+    dy = torch.randn((T, d), generator=gen, device=dev).to(torch.bfloat16)
+    ws = torch.empty(moe.moe_workspace_size(cfg), dtype=torch.uint8, device=dev)
+    bws = torch.empty(moe.moe_backward_workspace_size(cfg), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    fwd_args = moe.forward_args(inp, outs)
+    bin_ = dict(dy=dy, x=inp["x"], w_gate=inp["w_gate"], w1=inp["w1"], w2=inp["w2"])
+    for n in ("logits", "topk_idx", "topk_w", "counts", "offsets", "slot_row", "x_perm", "h_pre",
+              "h_act", "y_perm"):
+        bin_[n] = outs[n]
+    bwd_args = moe.backward_args(bin_, grads, D_AUX)
+
+    def fwd():
+        moe.moe_forward(cfg, inp, outs, ws, stream, args=fwd_args)
+
+    def bwd():
+        moe.moe_backward(cfg, bin_, grads, D_AUX, bws, stream, args=bwd_args)
+
+    for _ in range(args.warmup):
+        fwd()
+        bwd()
+    assert moe.moe_device_error(ws) == 0 and moe.moe_device_error(bws) == 0
+    M = int(outs["offsets"][-1])
+    nonempty = int((outs["kept_counts"] > 0).sum())
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    clocks = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    if clocks:
+        clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    for i in range(args.steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        fwd()
+        ev[i][1].record(stream)
+        bwd()
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    t1 = time.time()
+    if clocks:
+        clocks.stop()
+    step_ms = allreduce_max(statistics.fmean(e[0].elapsed_time(e[2]) for e in ev), world)
+    bwd_ms = statistics.fmean(e[1].elapsed_time(e[2]) for e in ev)
+    assert moe.moe_device_error(bws) == 0
+    if rank != 0:
+        return None
+    peaks = load_peaks()
+    # Backward tensor-core work: four expert GEMMs of 2*M*d*h flops each, plus the router's
+    # data and weight gradients (2 * 2*T*E*d).
+    flops = 4 * 2.0 * M * d * h + 2 * 2.0 * T * E * d
+    achieved = flops / (bwd_ms / 1e3) / 1e12
+    return {
+        "metric": TRAIN_METRIC,
+        "value": round(world * T / (step_ms / 1e3), 1),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(step_ms, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": w.dtype,
+        "data": "synthetic",
+        "config": {"workload": w.name, "T": T, "d": d, "h": h, "E": E, "k": k,
+                   "gate": ["topk_softmax", "softmax_topk_renorm"][w.gate],
+                   "capacity_factor": w.capacity_factor, "kept_rows": M,
+                   "nonempty_experts": nonempty, "d_aux": D_AUX, "inputs": input_recipe(w),
+                   "l2": "flushed before every timed step (256 MB write outside the event pair)",
+                   "parallelism": f"replicas x{world} (token-parallel, no collective)"},
+        "backward_ms": round(bwd_ms, 4),
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 1),
+                     "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": round(achieved / peaks["bf16_tflops"], 4), "traffic": None,
+                     "kernel": "moe_backward (all backward kernels; GEMM flops only)",
+                     "algorithmic_flops": flops, "peak_source": peaks["source"],
+                     "ms": round(bwd_ms, 4)},
+        "gpu_launches": (KERNELS_PER_FORWARD + KERNELS_PER_BACKWARD) * args.steps,
+        "clocks": clocks.summary(t0, t1) if clocks else None,
+    }
+
+
 # ------------------------------------------------------------------ reference arm
 def run_reference(args, world, rank, local):
     if rank != 0:
@@ -509,6 +629,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip the timed CPU-oracle sample (for quick runs)")
+    ap.add_argument("--pass", dest="pass_", default="forward", choices=["forward", "train"],
+                    help="forward (default) or train: forward + backward of the layer per step")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -517,7 +639,7 @@ def main():
         line = run_reference(args, world, rank, local)
     else:
         dist_init(world, local)
-        line = run_ours(args, world, rank, local)
+        line = (run_train if args.pass_ == "train" else run_ours)(args, world, rank, local)
         if world > 1:
             import torch.distributed as dist
             dist.destroy_process_group()
