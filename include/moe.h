@@ -250,8 +250,8 @@ moe_status moe_forward(const moe_config* cfg, const moe_forward_args* args, void
      dW_g   = dl^T x;  dlogit_bias = sum_t dl_t;  dx_t = dl_t W_g + sum_j dXp[slot j].
    bf16 layers only (MOE_ERR_UNSUPPORTED for fp32), no routing noise.  GEMMs run on the
    tensor cores with bf16 operands (dYp, dA, dXp and dl rounded to bf16) and fp32
-   accumulation; dW1, dW2 and dx are rounded to bf16 once, the other gradients are
-   fp32.  Results are deterministic.  The routing and saved-activation inputs are the
+   accumulation; dW1, dW2 and the router's part of dx are rounded to bf16 once, dx once
+   more after the slot sum; the other gradients are fp32.  Results are deterministic.  The routing and saved-activation inputs are the
    outputs of the moe_forward call being differentiated (same cfg). */
 typedef struct moe_backward_args {
   const void* dy;           /* [T,d] dtype */
@@ -279,8 +279,8 @@ typedef struct moe_backward_args {
   float* db2;               /* [E,d] fp32, or NULL */
 } moe_backward_args;
 
-/* Workspace bytes moe_backward needs (dYp, dA, dXp row buffers and per-token
-   gradients of the gate).  Host only. */
+/* Workspace bytes moe_backward needs (dYp, dA, dXp row buffers, the router's part of
+   dx and per-token gradients of the gate).  Host only. */
 moe_status moe_backward_workspace_size(const moe_config* cfg, size_t* bytes);
 
 /* The layer's backward on one stream.  Device flags: MOE_DEVERR_TIMEOUT. */

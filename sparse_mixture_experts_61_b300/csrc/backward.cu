@@ -133,6 +133,49 @@ __global__ void __launch_bounds__(kGateWarps * 32)
   }
 }
 
+// dx: one thread per 16-byte vector of a token; the router term, then the slots in order.
+constexpr int kDxThreads = 128;
+
+__global__ void __launch_bounds__(kDxThreads)
+    bwd_dx_kernel(const __nv_bfloat16* __restrict__ dxr, const __nv_bfloat16* __restrict__ dxp,
+                  const int32_t* __restrict__ slot_row, int d, int k,
+                  __nv_bfloat16* __restrict__ dx) {
+  __shared__ int s_row[kMaxK];
+  const int64_t t = blockIdx.x;
+  if (threadIdx.x < k) s_row[threadIdx.x] = slot_row[t * k + threadIdx.x];
+  __syncthreads();
+  const int v = blockIdx.y * kDxThreads + threadIdx.x;
+  if (v >= d / 8) return;
+  float acc[8], a[8];
+  const uint4 q0 = __ldg(reinterpret_cast<const uint4*>(dxr + t * d) + v);
+  const __nv_bfloat162* h0 = reinterpret_cast<const __nv_bfloat162*>(&q0);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __bfloat1622float2(h0[i]);
+    acc[2 * i] = f.x;
+    acc[2 * i + 1] = f.y;
+  }
+  for (int j = 0; j < k; ++j) {
+    const int r = s_row[j];
+    if (r < 0) continue;
+    const uint4 q = __ldg(reinterpret_cast<const uint4*>(dxp + static_cast<int64_t>(r) * d) + v);
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&q);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __bfloat1622float2(h[i]);
+      a[2 * i] = f.x;
+      a[2 * i + 1] = f.y;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] += a[i];
+  }
+  uint4 o;
+  __nv_bfloat162* oh = reinterpret_cast<__nv_bfloat162*>(&o);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) oh[i] = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+  reinterpret_cast<uint4*>(dx + t * d)[v] = o;
+}
+
 // Per-group prefix of 64-row slices; thread 0..31 of the block compute it.
 constexpr int kSlice = 64;
 constexpr int kColThreads = 256;
@@ -230,6 +273,16 @@ cudaError_t launch_bwd_gate(const float* logits, const int32_t* topk_idx, const 
   else
     MOE_GATE_BWD(8);
 #undef MOE_GATE_BWD
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_dx(const void* dxr, const void* dxp, const int32_t* slot_row, int64_t T,
+                          int d, int k, void* dx, cudaStream_t stream) {
+  if (T == 0) return cudaSuccess;
+  const dim3 grid(static_cast<unsigned>(T), static_cast<unsigned>((d / 8 + kDxThreads - 1) / kDxThreads));
+  bwd_dx_kernel<<<grid, kDxThreads, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(dxr), static_cast<const __nv_bfloat16*>(dxp), slot_row, d,
+      k, static_cast<__nv_bfloat16*>(dx));
   return cudaGetLastError();
 }
 

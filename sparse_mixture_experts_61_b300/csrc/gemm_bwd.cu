@@ -7,7 +7,8 @@
 //   transposed, i.e. as MN-major B operands):
 //     dA  = (dYp . W2[g]) * SiLU'(pre)     per expert, K = d, N = h   (EPI_DSILU)
 //     dXp = dA . W1[g]                     per expert, K = h, N = d   (EPI_PLAIN)
-//     dx  = dl . W_g + sum_j dXp[slot j]   dense, K = E, N = d        (EPI_DX)
+//     dxr = dl . W_g                       dense, K = E, N = d        (EPI_PLAIN)
+//   (dx = dxr + sum_j dXp[slot j] is summed per token in backward.cu)
 //   weight gradients (both operands MN-major, K = the expert's rows):
 //     dW2[g] = dYp_g^T . H_g,  dW1[g] = dA_g^T . Xp_g,  dW_g = dl^T . x.
 //
@@ -48,7 +49,7 @@ template <int EPI>
 __global__ void __launch_bounds__(ROWS_THREADS, 1)
     tc_bwd_rows_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB, const GemmArgs p) {
-  static_assert(EPI == EPI_DSILU || EPI == EPI_PLAIN || EPI == EPI_DX, "backward epilogues");
+  static_assert(EPI == EPI_DSILU || EPI == EPI_PLAIN, "backward epilogues");
   constexpr int BN = 256, STAGES = 4;
   constexpr uint32_t kTmemCols = 2 * BN;
   constexpr uint32_t kIdesc = bf16_idesc(TILE_M, BN) | kIdescBMnMajor;
@@ -115,12 +116,6 @@ __global__ void __launch_bounds__(ROWS_THREADS, 1)
       tc_fence_after();
       const int64_t row = c.row0 + quad * 32 + lane;
       const bool valid = row < c.row_end;
-      int32_t slot[kMaxK];
-      if (EPI == EPI_DX) {
-#pragma unroll
-        for (int j = 0; j < kMaxK; ++j)
-          slot[j] = (valid && j < p.nslots) ? p.slots[row * p.nslots + j] : -1;
-      }
       const uint32_t t_row = S.tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
                              static_cast<uint32_t>(acc * BN);
 #pragma unroll 1
@@ -148,23 +143,6 @@ __global__ void __launch_bounds__(ROWS_THREADS, 1)
 #pragma unroll
             for (int i = 0; i < 8; ++i) x[i] *= silu_grad(a[i]);
           }
-          if (EPI == EPI_DX) {
-#pragma unroll
-            for (int j = 0; j < kMaxK; ++j) {
-              if (slot[j] < 0) continue;
-              const int64_t so = static_cast<int64_t>(slot[j]) * p.N + c.n0 + col + 8 * q;
-              float a[8];
-              if (whole) {
-                unpack8(__ldg(reinterpret_cast<const uint4*>(aux + so)), a);
-              } else {
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                  a[i] = (c.n0 + col + 8 * q + i < p.N) ? __bfloat162float(aux[so + i]) : 0.f;
-              }
-#pragma unroll
-              for (int i = 0; i < 8; ++i) x[i] += a[i];
-            }
-          }
           uint4 packed;
           __nv_bfloat162* ph = reinterpret_cast<__nv_bfloat162*>(&packed);
 #pragma unroll
@@ -189,12 +167,18 @@ __global__ void __launch_bounds__(ROWS_THREADS, 1)
 }
 
 // ------------------------------------------------------------- weight gradients
-constexpr int WG_STAGES = 4;
 constexpr int WG_BM = 128, WG_BN = 256, WG_BK = 64;  // output tile; rows per k-block
+constexpr int WG_STAGES = 4;
+constexpr int WG_THREADS = 224;        // producer, MMA, 4 epilogue warps, tail-fixup warp
+constexpr int WG_STG_BOX = 32 * 128;   // one staged store box: 32 rows x 64 bf16
 
+// bf16 outputs leave through shared memory and TMA stores (whole 128-byte lines of the
+// gradient, which is as large as the weights and the bulk of this kernel's traffic), a
+// half tile at a time: each epilogue warp stages its 32 rows x 128 columns (two boxes).
 struct WgradSmem {
   uint8_t a[WG_STAGES][WG_BM * WG_BK * 2];  // two MN-major boxes [64 rows x 64 m]
   uint8_t b[WG_STAGES][WG_BN * WG_BK * 2];  // four MN-major boxes [64 rows x 64 n]
+  uint8_t stg[4][2][WG_STG_BOX];            // [epilogue warp][box]
   uint64_t full[WG_STAGES];
   uint64_t empty[WG_STAGES];
   uint64_t fixed[WG_STAGES];  // tail k-block: rows past the group zeroed
@@ -216,10 +200,17 @@ __device__ __forceinline__ void zero_box_rows(uint8_t* base, int nbox, int valid
   }
 }
 
+// Warps: 0 = TMA producer, 1 = MMA issuer (and TMEM owner), 2-5 = epilogue, 6 = fixup of
+// each group's last k-block (waits for its copies, zeroes the rows past the group,
+// then releases the stage to the MMA warp), so the producer never waits on it.  The
+// fixup warp observes every stage fill in order and a stage is refilled only after both
+// the MMA warp and the fixup warp have released it (two arrivals on `empty`), so the
+// fixup warp is never more than one phase behind a stage's `full` barrier.
 template <bool OUT_F32>
-__global__ void __launch_bounds__(TC_THREADS, 1)
+__global__ void __launch_bounds__(WG_THREADS, 1)
     tc_wgrad_kernel(const __grid_constant__ CUtensorMap tmA,
-                    const __grid_constant__ CUtensorMap tmB, const WgradArgs p) {
+                    const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmO, const WgradArgs p) {
   constexpr uint32_t kTmemCols = 2 * WG_BN;
   constexpr uint32_t kIdesc = bf16_idesc(WG_BM, WG_BN) | kIdescAMnMajor | kIdescBMnMajor;
   constexpr uint32_t kStageBytes = (WG_BM + WG_BN) * WG_BK * 2;
@@ -228,7 +219,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < WG_STAGES; ++s) {
       mbar_init(smem_u32(&S.full[s]), 1);
-      mbar_init(smem_u32(&S.empty[s]), 1);
+      mbar_init(smem_u32(&S.empty[s]), 2);  // MMA commit + fixup warp
       mbar_init(smem_u32(&S.fixed[s]), 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -240,6 +231,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    if (!OUT_F32) tma_prefetch_desc(&tmO);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(&S.tmem_base), kTmemCols);
@@ -252,6 +244,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   const int G = p.offsets ? p.G : 1;
   const int MB = (p.Mdim + WG_BM - 1) / WG_BM, NB = (p.Ndim + WG_BN - 1) / WG_BN;
   const int total = G * MB * NB;
+  const int first = static_cast<int>(blockIdx.x), step = static_cast<int>(gridDim.x);
   volatile int* abort = &S.abort;
 
   struct Coord {
@@ -272,23 +265,19 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   };
 
   if (warp == 0) {
-    // Producer warp (all lanes; lane 0 issues the copies).
-    int s = 0;
-    uint32_t ph = 0, fph = 0, issued = 0, issued_par = 0;
-    bool ok = true;
-    for (int tile = static_cast<int>(blockIdx.x); ok && tile < total;
-         tile += static_cast<int>(gridDim.x)) {
-      const Coord c = decode(tile);
-      for (int kb = 0; kb < c.nkb; ++kb) {
-        bool got = true;
-        if (lane == 0) got = mbar_wait_bounded(smem_u32(&S.empty[s]), ph ^ 1u, abort, p.flags);
-        if (!__shfl_sync(0xffffffffu, got, 0)) {
-          ok = false;
-          break;
-        }
-        const uint32_t fb = smem_u32(&S.full[s]);
-        const int row = static_cast<int>(c.row0) + kb * WG_BK;
-        if (lane == 0) {
+    if (lane == 0) {
+      int s = 0;
+      uint32_t ph = 0, issued = 0, issued_par = 0;
+      bool ok = true;
+      for (int tile = first; ok && tile < total; tile += step) {
+        const Coord c = decode(tile);
+        for (int kb = 0; kb < c.nkb; ++kb) {
+          if (!mbar_wait_bounded(smem_u32(&S.empty[s]), ph ^ 1u, abort, p.flags)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = smem_u32(&S.full[s]);
+          const int row = static_cast<int>(c.row0) + kb * WG_BK;
           mbar_arrive_expect_tx(fb, kStageBytes);
 #pragma unroll
           for (int j = 0; j < WG_BM / 64; ++j)
@@ -296,41 +285,52 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 #pragma unroll
           for (int j = 0; j < WG_BN / 64; ++j)
             tma_load_2d(smem_u32(S.b[s]) + j * kBoxBytes, &tmB, fb, c.n0 + 64 * j, row);
-        }
-        issued |= 1u << s;
-        issued_par = (issued_par & ~(1u << s)) | (ph << s);
-        if (kb == c.nkb - 1 && c.tail < WG_BK) {
-          // Tail: wait for the copies, zero the rows past the group, hand over.
-          bool landed = true;
-          if (lane == 0) landed = mbar_wait_bounded(fb, ph, abort, p.flags);
-          if (!__shfl_sync(0xffffffffu, landed, 0)) {
-            ok = false;
-            break;
+          issued |= 1u << s;
+          issued_par = (issued_par & ~(1u << s)) | (ph << s);
+          if (++s == WG_STAGES) {
+            s = 0;
+            ph ^= 1u;
           }
+        }
+      }
+      if (!ok) {
+        for (int q = 0; q < WG_STAGES; ++q)
+          if ((issued >> q) & 1u) mbar_wait_unwind(smem_u32(&S.full[q]), (issued_par >> q) & 1u);
+      }
+    }
+  } else if (warp == 6) {
+    int s = 0;
+    uint32_t ph = 0;
+    bool ok = true;
+    for (int tile = first; ok && tile < total; tile += step) {
+      const Coord c = decode(tile);
+      for (int kb = 0; kb < c.nkb; ++kb) {
+        bool landed = true;
+        if (lane == 0) landed = mbar_wait_bounded(smem_u32(&S.full[s]), ph, abort, p.flags);
+        if (!__shfl_sync(0xffffffffu, landed, 0)) {
+          ok = false;
+          break;
+        }
+        if (kb == c.nkb - 1 && c.tail < WG_BK) {
           zero_box_rows(S.a[s], WG_BM / 64, c.tail);
           zero_box_rows(S.b[s], WG_BN / 64, c.tail);
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(&S.fixed[s]));
-          fph ^= 1u << s;
         }
+        if (lane == 0) mbar_arrive(smem_u32(&S.empty[s]));
         if (++s == WG_STAGES) {
           s = 0;
           ph ^= 1u;
         }
       }
     }
-    if (!ok && lane == 0) {
-      for (int q = 0; q < WG_STAGES; ++q)
-        if ((issued >> q) & 1u) mbar_wait_unwind(smem_u32(&S.full[q]), (issued_par >> q) & 1u);
-    }
   } else if (warp == 1) {
     if (lane == 0) {
       int s = 0, acc = 0;
       uint32_t ph = 0, fph = 0, aph = 0;
       bool ok = true, issued_any = false;
-      for (int tile = static_cast<int>(blockIdx.x); ok && tile < total;
-           tile += static_cast<int>(gridDim.x)) {
+      for (int tile = first; ok && tile < total; tile += step) {
         const Coord c = decode(tile);
         if (!mbar_wait_bounded(smem_u32(&S.tempty[acc]), aph ^ 1u, abort, p.flags)) {
           ok = false;
@@ -374,33 +374,32 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       }
     }
   } else {
-    const int quad = warp & 3;
+    const int quad = warp & 3;  // TMEM lanes 32*quad .. 32*quad+31 = output rows of the tile
     int acc = 0;
     uint32_t aph = 0;
-    for (int tile = static_cast<int>(blockIdx.x); tile < total; tile += static_cast<int>(gridDim.x)) {
+    for (int tile = first; tile < total; tile += step) {
       const Coord c = decode(tile);
       const bool got = mbar_wait_bounded(smem_u32(&S.tfull[acc]), aph, abort, p.flags);
       if (!__all_sync(0xffffffffu, got)) break;
       tc_fence_after();
       const int m = c.m0 + quad * 32 + lane;
-      const bool valid = m < p.Mdim;
-      const int64_t o = (static_cast<int64_t>(c.g) * p.Mdim + m) * p.Ndim + c.n0;
       const uint32_t t_row = S.tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
                              static_cast<uint32_t>(acc * WG_BN);
+      if (OUT_F32) {
+        const bool valid = m < p.Mdim;
+        const int64_t o = (static_cast<int64_t>(c.g) * p.Mdim + m) * p.Ndim + c.n0;
 #pragma unroll 1
-      for (int col = 0; col < WG_BN; col += 32) {
-        float v[32];
-        tmem_ld_32cols(t_row + col, v);
-        tc_wait_ld();
-        if (!valid || c.n0 + col >= p.Ndim) continue;
-        if (c.nkb == 0) {
+        for (int col = 0; col < WG_BN; col += 32) {
+          float v[32];
+          tmem_ld_32cols(t_row + col, v);
+          tc_wait_ld();
+          if (!valid || c.n0 + col >= p.Ndim) continue;
+          if (c.nkb == 0) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = 0.f;
-        }
-        const bool whole = c.n0 + col + 32 <= p.Ndim;
-        if (OUT_F32) {
+            for (int i = 0; i < 32; ++i) v[i] = 0.f;
+          }
           float* out = static_cast<float*>(p.out) + o + col;
-          if (whole) {
+          if (c.n0 + col + 32 <= p.Ndim) {
 #pragma unroll
             for (int q = 0; q < 8; ++q)
               *reinterpret_cast<float4*>(out + 4 * q) =
@@ -410,31 +409,53 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             for (int i = 0; i < 32; ++i)
               if (c.n0 + col + i < p.Ndim) out[i] = v[i];
           }
-        } else {
-          __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + o + col;
+        }
+      } else {
+#pragma unroll 1
+        for (int half = 0; half < 2; ++half) {
+          // The previous stores must have finished reading this warp's staging.
+          if (lane == 0) bulk_wait_group_read0();
+          __syncwarp();
+#pragma unroll 1
+          for (int col = half * 128; col < half * 128 + 128; col += 32) {
+            float v[32];
+            tmem_ld_32cols(t_row + col, v);
+            tc_wait_ld();
+            if (c.nkb == 0) {
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint4 packed;
-            __nv_bfloat162* ph2 = reinterpret_cast<__nv_bfloat162*>(&packed);
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              ph2[i] = __floats2bfloat162_rn(v[8 * q + 2 * i], v[8 * q + 2 * i + 1]);
-            if (whole) {
-              *reinterpret_cast<uint4*>(out + 8 * q) = packed;
-            } else {
-              const __nv_bfloat16* pv = reinterpret_cast<const __nv_bfloat16*>(&packed);
-#pragma unroll
-              for (int i = 0; i < 8; ++i)
-                if (c.n0 + col + 8 * q + i < p.Ndim) out[8 * q + i] = pv[i];
+              for (int i = 0; i < 32; ++i) v[i] = 0.f;
             }
+            // Box (col%128)/64, row lane; 16-byte chunk (col%64)/8 + q, 128-byte swizzled.
+            uint8_t* box = S.stg[quad][(col % 128) / 64] + lane * 128;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              uint4 packed;
+              __nv_bfloat162* ph2 = reinterpret_cast<__nv_bfloat162*>(&packed);
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                ph2[i] = __floats2bfloat162_rn(v[8 * q + 2 * i], v[8 * q + 2 * i + 1]);
+              const int chunk = ((col % 64) / 8 + q) ^ (lane & 7);
+              *reinterpret_cast<uint4*>(box + chunk * 16) = packed;
+            }
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+              tma_store_3d(&tmO, smem_u32(S.stg[quad][j]), c.n0 + half * 128 + 64 * j,
+                           c.m0 + quad * 32, c.g);
+            bulk_commit_group();
           }
         }
       }
+      // TMEM drained: the accumulator can take the next tile while the stores run.
       tc_fence_before();
       mbar_arrive(smem_u32(&S.tempty[acc]));
       acc ^= 1;
       if (acc == 0) aph ^= 1u;
     }
+    if (!OUT_F32 && lane == 0) bulk_wait_group0();
   }
   tc_fence_before();
   __syncthreads();
@@ -468,17 +489,18 @@ cudaError_t launch_tc_bwd_rows(const GemmArgs& a, int epi, int sm_count, cudaStr
   switch (epi) {
     case EPI_DSILU: return launch_bwd_rows_epi<EPI_DSILU>(a, sm_count, stream);
     case EPI_PLAIN: return launch_bwd_rows_epi<EPI_PLAIN>(a, sm_count, stream);
-    case EPI_DX: return launch_bwd_rows_epi<EPI_DX>(a, sm_count, stream);
     default: return cudaErrorInvalidValue;
   }
 }
 
 cudaError_t launch_tc_wgrad(const WgradArgs& a, int sm_count, cudaStream_t stream) {
-  CUtensorMap tmA, tmB;
-  // [rows, Mdim] and [rows, Ndim] row-major, read as 64-column x 64-row boxes.
+  CUtensorMap tmA, tmB, tmO{};
+  // [rows, Mdim] and [rows, Ndim] row-major, read as 64-column x 64-row boxes; a bf16
+  // output [G, Mdim, Ndim] is written as 64-column x 32-row boxes.
+  const int G = a.offsets ? a.G : 1;
   if (!rows_map(&tmA, a.A, a.rows_alloc, a.Mdim, 64) || !rows_map(&tmB, a.B, a.rows_alloc, a.Ndim, 64))
     return cudaErrorInvalidValue;
-  const int G = a.offsets ? a.G : 1;
+  if (!a.out_f32 && !stacked_map(&tmO, a.out, G, a.Mdim, a.Ndim, 32)) return cudaErrorInvalidValue;
   const int64_t tiles = static_cast<int64_t>(G) * ((a.Mdim + WG_BM - 1) / WG_BM) *
                         ((a.Ndim + WG_BN - 1) / WG_BN);
   const int grid = static_cast<int>(std::min<int64_t>(tiles, sm_count));
@@ -488,7 +510,7 @@ cudaError_t launch_tc_wgrad(const WgradArgs& a, int sm_count, cudaStream_t strea
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  kern<<<grid, TC_THREADS, smem, stream>>>(tmA, tmB, a);
+  kern<<<grid, WG_THREADS, smem, stream>>>(tmA, tmB, tmO, a);
   return cudaGetLastError();
 }
 

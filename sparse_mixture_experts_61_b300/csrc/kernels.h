@@ -84,12 +84,8 @@ struct GemmArgs {
   int64_t split_stride;
   int* flags;
   void* pre_out;          // EPI_BIAS_SILU: also writes the pre-activation (before SiLU), or nullptr
-  // Backward epilogues: EPI_DSILU multiplies by SiLU'(aux_in[row, n]) (the saved
-  // pre-activation); EPI_DX adds aux_in[slots[row, j], n] for j < nslots (slot < 0
-  // skipped).
+  // Backward: EPI_DSILU multiplies by SiLU'(aux_in[row, n]) (the saved pre-activation).
   const void* aux_in;
-  const int32_t* slots;
-  int nslots;
   int64_t b_rows;  // backward B [G][b_rows][N] when b_rows differs from K (rows past it read 0)
 };
 
@@ -105,14 +101,13 @@ enum Epilogue {
   EPI_BIAS = 1,
   EPI_ROUTER_F32 = 2,
   EPI_DSILU = 3,  // out = acc * SiLU'(pre)
-  EPI_PLAIN = 4,  // out = acc
-  EPI_DX = 5      // out = acc + sum_j rows[slots[row, j]]
+  EPI_PLAIN = 4   // out = acc
 };
 
 // Backward GEMMs on row tiles (bf16): A [rows, K] K-major as in the forward, B stored
 // [G][K][N] (N contiguous: the forward weights read transposed, MN-major), epilogue
-// EPI_DSILU, EPI_PLAIN or EPI_DX, bf16 output [rows, N].  offsets == nullptr: one
-// dense group of m_rows rows.
+// EPI_DSILU or EPI_PLAIN, bf16 output [rows, N].  offsets == nullptr: one dense group
+// of m_rows rows.
 cudaError_t launch_tc_bwd_rows(const GemmArgs& a, int epi, int sm_count, cudaStream_t stream);
 
 // Weight gradients: for each group g with rows [offsets[g], offsets[g+1]) (or one
@@ -147,6 +142,11 @@ cudaError_t launch_bwd_combine(const void* dy, const void* y_perm, const int32_t
 cudaError_t launch_bwd_gate(const float* logits, const int32_t* topk_idx, const float* topk_w,
                             const float* dw, const int32_t* counts, float d_aux, int64_t T,
                             int E, int Epad, int k, float* dl, void* dl16, cudaStream_t stream);
+
+// dx[t] = dxr[t] + sum_j dXp[slot_row[t,j]] (slots in order, dropped slots skipped),
+// fp32 sums rounded once to bf16.
+cudaError_t launch_bwd_dx(const void* dxr, const void* dxp, const int32_t* slot_row, int64_t T,
+                          int d, int k, void* dx, cudaStream_t stream);
 
 // Column sums per group: out[g][c] = sum over rows r of group g of A[r][c] (rows in
 // order within 64-row slices, slices in order), A bf16 (a_f32 = false) or fp32.

@@ -577,7 +577,7 @@ namespace moe {
 namespace {
 
 struct BwdLayout {
-  size_t flags, dyp, da, dxp, dw, dl, dl16, dwg, partial, total;
+  size_t flags, dyp, da, dxp, dxr, dw, dl, dl16, dwg, partial, total;
   int Epad;
 };
 
@@ -593,6 +593,7 @@ BwdLayout make_bwd_layout(const moe_config& c) {
   L.dyp = o; o = align_up(o + rows * c.d * 2);
   L.da = o; o = align_up(o + rows * c.h * 2);
   L.dxp = o; o = align_up(o + rows * c.d * 2);
+  L.dxr = o; o = align_up(o + T * c.d * 2);
   L.dw = o; o = align_up(o + T * k * 4);
   L.dl = o; o = align_up(o + T * E * 4);
   L.dl16 = o; o = align_up(o + T * L.Epad * 2);
@@ -691,12 +692,10 @@ MOE_EXPORT moe_status moe_backward(const moe_config* cfg, const moe_backward_arg
   r.N = c.d;
   r.K = L.Epad;
   r.b_rows = c.E;
-  r.out = a->dx;
-  r.aux_in = dxp;
-  r.slots = a->slot_row;
-  r.nslots = c.k;
+  r.out = at<void>(ws, L.dxr);
   r.flags = flags;
-  MOE_CUDA(launch_tc_bwd_rows(r, EPI_DX, sms, st));
+  MOE_CUDA(launch_tc_bwd_rows(r, EPI_PLAIN, sms, st));
+  MOE_CUDA(launch_bwd_dx(at<void>(ws, L.dxr), dxp, a->slot_row, c.T, c.d, c.k, a->dx, st));
   // Weight gradients.
   WgradArgs wg{};
   wg.offsets = a->offsets;
