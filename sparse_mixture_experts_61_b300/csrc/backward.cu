@@ -22,6 +22,7 @@ __global__ void __launch_bounds__(kCbThreads)
     bwd_combine_kernel(const __nv_bfloat16* __restrict__ dy, const __nv_bfloat16* __restrict__ y_perm,
                        const int32_t* __restrict__ slot_row, const float* __restrict__ topk_w, int d,
                        int k, __nv_bfloat16* __restrict__ dy_perm, float* __restrict__ dw) {
+  pdl_enter();
   __shared__ float s_red[kCbThreads / 32];
   const int64_t t = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -73,6 +74,7 @@ __global__ void __launch_bounds__(kGateWarps * 32)
                     const float* __restrict__ topk_w, const float* __restrict__ dw,
                     const int32_t* __restrict__ counts, float d_aux, int64_t T, int E, int Epad,
                     int k, float* __restrict__ dl, __nv_bfloat16* __restrict__ dl16) {
+  pdl_enter();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t t = static_cast<int64_t>(blockIdx.x) * kGateWarps + warp;
   if (t >= T) return;
@@ -140,6 +142,7 @@ __global__ void __launch_bounds__(kDxThreads)
     bwd_dx_kernel(const __nv_bfloat16* __restrict__ dxr, const __nv_bfloat16* __restrict__ dxp,
                   const int32_t* __restrict__ slot_row, int d, int k,
                   __nv_bfloat16* __restrict__ dx) {
+  pdl_enter();
   __shared__ int s_row[kMaxK];
   const int64_t t = blockIdx.x;
   if (threadIdx.x < k) s_row[threadIdx.x] = slot_row[t * k + threadIdx.x];
@@ -209,6 +212,7 @@ template <typename Tin>
 __global__ void __launch_bounds__(kColThreads)
     colsum_partial_kernel(const Tin* __restrict__ A, int C, const int32_t* __restrict__ offsets,
                           int64_t m_rows, int G, float* __restrict__ partial) {
+  pdl_enter();
   __shared__ int pref[kMaxExperts + 1];
   slice_prefix(offsets, m_rows, G, pref);
   const int sl = blockIdx.y;
@@ -233,6 +237,7 @@ __global__ void __launch_bounds__(kColThreads)
 __global__ void __launch_bounds__(kColThreads)
     colsum_final_kernel(const float* __restrict__ partial, int C, const int32_t* __restrict__ offsets,
                         int64_t m_rows, int G, float* __restrict__ out) {
+  pdl_enter();
   __shared__ int pref[kMaxExperts + 1];
   slice_prefix(offsets, m_rows, G, pref);
   const int g = blockIdx.y;
@@ -249,7 +254,7 @@ cudaError_t launch_bwd_combine(const void* dy, const void* y_perm, const int32_t
                                const float* topk_w, int64_t T, int d, int k, void* dy_perm,
                                float* dw, cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
-  bwd_combine_kernel<<<static_cast<unsigned>(T), kCbThreads, 0, stream>>>(
+  launch_pdl(bwd_combine_kernel, static_cast<unsigned>(T), kCbThreads, 0, stream, 
       static_cast<const __nv_bfloat16*>(dy), static_cast<const __nv_bfloat16*>(y_perm), slot_row,
       topk_w, d, k, static_cast<__nv_bfloat16*>(dy_perm), dw);
   return cudaGetLastError();
@@ -262,7 +267,7 @@ cudaError_t launch_bwd_gate(const float* logits, const int32_t* topk_idx, const 
   const unsigned grid = static_cast<unsigned>((T + kGateWarps - 1) / kGateWarps);
   __nv_bfloat16* d16 = static_cast<__nv_bfloat16*>(dl16);
 #define MOE_GATE_BWD(EPL)                                                                       \
-  bwd_gate_kernel<EPL><<<grid, kGateWarps * 32, 0, stream>>>(logits, topk_idx, topk_w, dw, counts, \
+  launch_pdl(bwd_gate_kernel<EPL>, grid, kGateWarps * 32, 0, stream, logits, topk_idx, topk_w, dw, counts, \
                                                              d_aux, T, E, Epad, k, dl, d16)
   if (Epad <= 32)
     MOE_GATE_BWD(1);
@@ -280,7 +285,7 @@ cudaError_t launch_bwd_dx(const void* dxr, const void* dxp, const int32_t* slot_
                           int d, int k, void* dx, cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
   const dim3 grid(static_cast<unsigned>(T), static_cast<unsigned>((d / 8 + kDxThreads - 1) / kDxThreads));
-  bwd_dx_kernel<<<grid, kDxThreads, 0, stream>>>(
+  launch_pdl(bwd_dx_kernel, grid, kDxThreads, 0, stream, 
       static_cast<const __nv_bfloat16*>(dxr), static_cast<const __nv_bfloat16*>(dxp), slot_row, d,
       k, static_cast<__nv_bfloat16*>(dx));
   return cudaGetLastError();
@@ -298,14 +303,14 @@ cudaError_t launch_colsum(const void* A, bool a_f32, int C, const int32_t* offse
   const int64_t slices = rows_alloc / kSlice + G + 1;
   const dim3 g1(cb, static_cast<unsigned>(slices)), g2(cb, static_cast<unsigned>(G));
   if (a_f32)
-    colsum_partial_kernel<float><<<g1, kColThreads, 0, stream>>>(static_cast<const float*>(A), C,
+    launch_pdl(colsum_partial_kernel<float>, g1, kColThreads, 0, stream, static_cast<const float*>(A), C,
                                                                  offsets, m_rows, G, partial);
   else
-    colsum_partial_kernel<__nv_bfloat16><<<g1, kColThreads, 0, stream>>>(
+    launch_pdl(colsum_partial_kernel<__nv_bfloat16>, g1, kColThreads, 0, stream, 
         static_cast<const __nv_bfloat16*>(A), C, offsets, m_rows, G, partial);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  colsum_final_kernel<<<g2, kColThreads, 0, stream>>>(partial, C, offsets, m_rows, G, out);
+  launch_pdl(colsum_final_kernel, g2, kColThreads, 0, stream, partial, C, offsets, m_rows, G, out);
   return cudaGetLastError();
 }
 

@@ -54,6 +54,7 @@ __global__ void __launch_bounds__(kThreads)
     combine_kernel(const T* __restrict__ y_perm, const int32_t* __restrict__ slot_row,
                    const float* __restrict__ topk_w, int d, int k, int64_t rows,
                    T* __restrict__ y, int* flags) {
+  pdl_enter();
   constexpr int V = Vec<T>::N;
   __shared__ int s_row[kMaxK];
   __shared__ float s_w[kMaxK];
@@ -98,6 +99,7 @@ __global__ void __launch_bounds__(kEcThreads)
                       const float* __restrict__ probs_et, int64_t ntok, int E, int64_t C, int d,
                       T* __restrict__ y, int32_t* __restrict__ token_experts,
                       int32_t* __restrict__ unrouted) {
+  pdl_enter();
   constexpr int V = Vec<T>::N;
   __shared__ int64_t s_row[kMaxExperts];
   __shared__ float s_w[kMaxExperts];
@@ -152,11 +154,11 @@ cudaError_t launch_ec_combine(int dtype, const void* y_perm, const int32_t* rowm
   if (T == 0) return cudaSuccess;
   const dim3 grid(static_cast<unsigned>(T));
   if (dtype == MOE_F32)
-    ec_combine_kernel<float><<<grid, kEcThreads, 0, stream>>>(
+    launch_pdl(ec_combine_kernel<float>, grid, kEcThreads, 0, stream, 
         static_cast<const float*>(y_perm), rowmap_et, probs_et, T, E, C, d,
         static_cast<float*>(y), token_experts, unrouted);
   else
-    ec_combine_kernel<__nv_bfloat16><<<grid, kEcThreads, 0, stream>>>(
+    launch_pdl(ec_combine_kernel<__nv_bfloat16>, grid, kEcThreads, 0, stream, 
         static_cast<const __nv_bfloat16*>(y_perm), rowmap_et, probs_et, T, E, C, d,
         static_cast<__nv_bfloat16*>(y), token_experts, unrouted);
   return cudaGetLastError();
@@ -170,11 +172,11 @@ cudaError_t launch_combine(int dtype, const void* y_perm, const int32_t* slot_ro
   const dim3 grid(static_cast<unsigned>(T), static_cast<unsigned>((d / vec + kThreads - 1) / kThreads));
   const int64_t rows = T * k;
   if (dtype == MOE_F32)
-    combine_kernel<float><<<grid, kThreads, 0, stream>>>(static_cast<const float*>(y_perm),
+    launch_pdl(combine_kernel<float>, grid, kThreads, 0, stream, static_cast<const float*>(y_perm),
                                                          slot_row, topk_w, d, k, rows,
                                                          static_cast<float*>(y), flags);
   else
-    combine_kernel<__nv_bfloat16><<<grid, kThreads, 0, stream>>>(
+    launch_pdl(combine_kernel<__nv_bfloat16>, grid, kThreads, 0, stream, 
         static_cast<const __nv_bfloat16*>(y_perm), slot_row, topk_w, d, k, rows,
         static_cast<__nv_bfloat16*>(y), flags);
   return cudaGetLastError();

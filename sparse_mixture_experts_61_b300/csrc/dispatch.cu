@@ -29,6 +29,7 @@ constexpr int kThreads = 256;
 __global__ void __launch_bounds__(kThreads)
     dispatch_hist_kernel(const int32_t* __restrict__ topk_idx, int64_t T, int E, int k,
                          int32_t* __restrict__ hist, int* flags) {
+  pdl_enter();
   __shared__ int s_hist[kMaxExperts];
   for (int e = threadIdx.x; e < E; e += blockDim.x) s_hist[e] = 0;
   __syncthreads();
@@ -52,6 +53,7 @@ __global__ void __launch_bounds__(kThreads)
                           const int32_t* __restrict__ chunk_base,
                           const int32_t* __restrict__ offsets, int32_t* __restrict__ slot_row,
                           int32_t* __restrict__ row_token, int* flags) {
+  pdl_enter();
   __shared__ int s_idx[kChunk * kMaxK];
   const int c = blockIdx.x;
   const int64_t t0 = static_cast<int64_t>(c) * kChunk;
@@ -89,6 +91,7 @@ template <typename Tin>
 __global__ void __launch_bounds__(kThreads)
     gather_rows_kernel(const int32_t* __restrict__ row_token, const int32_t* __restrict__ offsets,
                        int E, const Tin* __restrict__ x, Tin* __restrict__ x_perm, int d) {
+  pdl_enter();
   const int64_t M = offsets[E];
   const int nvec = d * static_cast<int>(sizeof(Tin)) / 16;
   const int lane = threadIdx.x & 31;
@@ -116,7 +119,7 @@ cudaError_t launch_dispatch_hist(const int32_t* topk_idx, int64_t T, int E, int 
                                  int* flags, cudaStream_t stream) {
   const int64_t nchunks = (T + kChunk - 1) / kChunk;
   if (nchunks == 0) return cudaSuccess;
-  dispatch_hist_kernel<<<static_cast<unsigned>(nchunks), kThreads, 0, stream>>>(topk_idx, T, E, k,
+  launch_pdl(dispatch_hist_kernel, static_cast<unsigned>(nchunks), kThreads, 0, stream, topk_idx, T, E, k,
                                                                                hist, flags);
   return cudaGetLastError();
 }
@@ -127,7 +130,7 @@ cudaError_t launch_dispatch_place(int dtype, const int32_t* topk_idx, int64_t T,
                                   void* x_perm, int d, int* flags, cudaStream_t stream) {
   const int64_t nchunks = (T + kChunk - 1) / kChunk;
   if (nchunks == 0) return cudaSuccess;
-  dispatch_place_kernel<<<static_cast<unsigned>(nchunks), kThreads, 0, stream>>>(
+  launch_pdl(dispatch_place_kernel, static_cast<unsigned>(nchunks), kThreads, 0, stream, 
       topk_idx, T, E, k, C, chunk_base, offsets, slot_row, row_token, flags);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -142,10 +145,10 @@ cudaError_t launch_gather_rows(int dtype, const int32_t* row_token, const int32_
   const unsigned grid =
       static_cast<unsigned>(std::min<int64_t>((rows + kThreads / 32 - 1) / (kThreads / 32), 4096));
   if (dtype == MOE_F32)
-    gather_rows_kernel<float><<<grid, kThreads, 0, stream>>>(
+    launch_pdl(gather_rows_kernel<float>, grid, kThreads, 0, stream, 
         row_token, offsets, E, static_cast<const float*>(x), static_cast<float*>(x_perm), d);
   else
-    gather_rows_kernel<__nv_bfloat16><<<grid, kThreads, 0, stream>>>(
+    launch_pdl(gather_rows_kernel<__nv_bfloat16>, grid, kThreads, 0, stream, 
         row_token, offsets, E, static_cast<const __nv_bfloat16*>(x),
         static_cast<__nv_bfloat16*>(x_perm), d);
   return cudaGetLastError();

@@ -35,6 +35,7 @@ __global__ void __launch_bounds__(kSmWarps * 32)
                       const float* __restrict__ bias, float* __restrict__ logits_out,
                       float* __restrict__ probs_out, float* __restrict__ probs_et, int64_t T,
                       int E, int* flags) {
+  pdl_enter();
   __shared__ float s_p[kMaxExperts][kSmTokens + 1];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kSmTokens;
@@ -132,6 +133,7 @@ __global__ void __launch_bounds__(kSelThreads)
     ec_select_kernel(const float* __restrict__ probs_et, int64_t T, int E, int64_t C,
                      int32_t* __restrict__ sel_token, float* __restrict__ sel_w,
                      int32_t* __restrict__ rowmap_et, int32_t* __restrict__ offsets) {
+  pdl_enter();
   __shared__ int s_hist[256];
   __shared__ int s_scan[kSelWarps + 1];
   __shared__ int s_bin, s_before;
@@ -233,7 +235,7 @@ cudaError_t launch_ec_softmax(const float* src, int nsplit, int64_t split_stride
   if (T == 0) return cudaSuccess;
   const dim3 grid(static_cast<unsigned>((T + kSmTokens - 1) / kSmTokens)), block(kSmWarps * 32);
 #define MOE_EC_SOFTMAX(EPL)                                                                  \
-  ec_softmax_kernel<EPL><<<grid, block, 0, stream>>>(src, nsplit, split_stride, bias,        \
+  launch_pdl(ec_softmax_kernel<EPL>, grid, block, 0, stream, src, nsplit, split_stride, bias,        \
                                                      logits_out, probs_out, probs_et, T, E, \
                                                      flags)
   if (E <= 32)
@@ -252,7 +254,7 @@ cudaError_t launch_ec_select(const float* probs_et, int64_t T, int E, int64_t C,
                              int32_t* sel_token, float* sel_w, int32_t* rowmap_et,
                              int32_t* offsets, cudaStream_t stream) {
   if (T == 0 || C <= 0) return cudaSuccess;
-  ec_select_kernel<<<static_cast<unsigned>(E), kSelThreads, 0, stream>>>(
+  launch_pdl(ec_select_kernel, static_cast<unsigned>(E), kSelThreads, 0, stream, 
       probs_et, T, E, C, sel_token, sel_w, rowmap_et, offsets);
   return cudaGetLastError();
 }

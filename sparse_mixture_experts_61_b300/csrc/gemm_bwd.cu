@@ -49,6 +49,7 @@ template <int EPI>
 __global__ void __launch_bounds__(ROWS_THREADS, 1)
     tc_bwd_rows_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB, const GemmArgs p) {
+  pdl_enter();
   static_assert(EPI == EPI_DSILU || EPI == EPI_PLAIN, "backward epilogues");
   constexpr int BN = 256, STAGES = 4;
   constexpr uint32_t kTmemCols = 2 * BN;
@@ -211,6 +212,7 @@ __global__ void __launch_bounds__(WG_THREADS, 1)
     tc_wgrad_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmO, const WgradArgs p) {
+  pdl_enter();
   constexpr uint32_t kTmemCols = 2 * WG_BN;
   constexpr uint32_t kIdesc = bf16_idesc(WG_BM, WG_BN) | kIdescAMnMajor | kIdescBMnMajor;
   constexpr uint32_t kStageBytes = (WG_BM + WG_BN) * WG_BK * 2;
@@ -510,7 +512,7 @@ cudaError_t launch_tc_wgrad(const WgradArgs& a, int sm_count, cudaStream_t strea
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  kern<<<grid, WG_THREADS, smem, stream>>>(tmA, tmB, tmO, a);
+  launch_pdl(kern, grid, WG_THREADS, smem, stream, tmA, tmB, tmO, a);
   return cudaGetLastError();
 }
 

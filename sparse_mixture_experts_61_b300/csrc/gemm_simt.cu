@@ -21,6 +21,7 @@ constexpr int BM = 64, BN = 64, BK = 16;
 
 template <int EPI>
 __global__ void __launch_bounds__(256) simt_gemm_f32_kernel(GemmArgs p) {
+  pdl_enter();
   __shared__ float As[BK][BM + 4];
   __shared__ float Bs[BK][BN + 4];
   __shared__ int s_mpref[kMaxExperts + 1];
@@ -134,13 +135,13 @@ cudaError_t launch_simt_gemm_f32(const GemmArgs& a, int epi, int sm_count, cudaS
   if (grid <= 0) return cudaSuccess;
   switch (epi) {
     case EPI_BIAS_SILU:
-      simt_gemm_f32_kernel<EPI_BIAS_SILU><<<static_cast<unsigned>(grid), 256, 0, stream>>>(a);
+      launch_pdl(simt_gemm_f32_kernel<EPI_BIAS_SILU>, static_cast<unsigned>(grid), 256, 0, stream, a);
       break;
     case EPI_BIAS:
-      simt_gemm_f32_kernel<EPI_BIAS><<<static_cast<unsigned>(grid), 256, 0, stream>>>(a);
+      launch_pdl(simt_gemm_f32_kernel<EPI_BIAS>, static_cast<unsigned>(grid), 256, 0, stream, a);
       break;
     default:
-      simt_gemm_f32_kernel<EPI_ROUTER_F32><<<static_cast<unsigned>(grid), 256, 0, stream>>>(a);
+      launch_pdl(simt_gemm_f32_kernel<EPI_ROUTER_F32>, static_cast<unsigned>(grid), 256, 0, stream, a);
       break;
   }
   return cudaGetLastError();

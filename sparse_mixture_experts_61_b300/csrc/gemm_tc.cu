@@ -52,6 +52,7 @@ template <int TB, int STAGES, int EPI>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
     tc_ffn_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                   const GemmArgs p) {
+  pdl_enter();
   static_assert(TB >= TOK_BOX && TB <= 256 && (TB & (TB - 1)) == 0,
                 "TB: power of two in [32, 256]");
   static_assert(EPI == EPI_BIAS_SILU || EPI == EPI_BIAS, "expert epilogues only");
@@ -179,6 +180,7 @@ __global__ void __launch_bounds__(ROWS_THREADS, 1)
     tc_rows_ffn_kernel(const __grid_constant__ CUtensorMap tmX,
                        const __grid_constant__ CUtensorMap tmW,
                        const __grid_constant__ CUtensorMap tmO, const GemmArgs p) {
+  pdl_enter();
   static_assert(BN % 32 == 0 && BN <= 256 && (BN & (BN - 1)) == 0, "BN: power of two, <= 256");
   static_assert(EPI == EPI_BIAS_SILU || EPI == EPI_BIAS, "expert epilogues only");
   constexpr uint32_t kTmemCols = 2 * BN;
@@ -375,6 +377,7 @@ template <int BN, int STAGES>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     tc_router_kernel(const __grid_constant__ CUtensorMap tmX,
                      const __grid_constant__ CUtensorMap tmW, const GemmArgs p) {
+  pdl_enter();
   static_assert(BN >= 16 && BN <= 256 && (BN & (BN - 1)) == 0, "BN: power of two in [16, 256]");
   constexpr uint32_t kTmemCols = (2 * BN < 32) ? 32 : 2 * BN;
   constexpr uint32_t kIdesc = bf16_idesc(TILE_M, BN);
@@ -480,7 +483,7 @@ cudaError_t launch_ffn(const GemmArgs& a, int sm_count, cudaStream_t stream) {
   const int64_t clusters =
       std::min<int64_t>(bound, resident_clusters(kern, smem, sm_count));
   if (clusters <= 0) return cudaSuccess;
-  kern<<<static_cast<unsigned>(2 * clusters), TC_THREADS, smem, stream>>>(tmW, tmX, a);
+  launch_pdl(kern, static_cast<unsigned>(2 * clusters), TC_THREADS, smem, stream, tmW, tmX, a);
   return cudaGetLastError();
 }
 
@@ -501,7 +504,7 @@ cudaError_t launch_rows_ffn(const GemmArgs& a, int sm_count, cudaStream_t stream
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   if (grid <= 0) return cudaSuccess;
-  kern<<<grid, ROWS_THREADS, smem, stream>>>(tmX, tmW, tmO, a);
+  launch_pdl(kern, grid, ROWS_THREADS, smem, stream, tmX, tmW, tmO, a);
   return cudaGetLastError();
 }
 

@@ -36,6 +36,7 @@ __global__ void __launch_bounds__(kRouteWarps * 32)
                       int gate, int32_t* __restrict__ topk_idx,
                       float* __restrict__ topk_w, int32_t* __restrict__ hist,
                       float* __restrict__ psum, int* flags) {
+  pdl_enter();
   __shared__ int s_hist[kMaxExperts];
   __shared__ float s_ps[kRouteWarps][kMaxExperts];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -241,6 +242,7 @@ __global__ void __launch_bounds__(kFinThreads)
                           float* __restrict__ aux, int32_t* __restrict__ chunk_base,
                           int32_t* __restrict__ kept, int32_t* __restrict__ offsets,
                           int32_t* __restrict__ dropped, float* __restrict__ stats) {
+  pdl_enter();
   __shared__ double s_red[kMaxExperts];
   __shared__ int s_scan[kMaxExperts];
   __shared__ int s_drop;
@@ -392,7 +394,7 @@ cudaError_t launch_route_topk(const float* src, int nsplit, int64_t split_stride
   if (nchunks == 0) return cudaSuccess;
   const dim3 grid(static_cast<unsigned>(nchunks)), block(kRouteWarps * 32);
 #define MOE_TOPK_LAUNCH(EPL)                                                                   \
-  route_topk_kernel<EPL><<<grid, block, 0, stream>>>(src, nsplit, split_stride, bias, noise,   \
+  launch_pdl(route_topk_kernel<EPL>, grid, block, 0, stream, src, nsplit, split_stride, bias, noise,   \
                                                      noise_mode, logits_out, T, E, k, gate,    \
                                                      topk_idx, topk_w, hist, psum, flags)
   if (E <= 32)
@@ -411,7 +413,7 @@ cudaError_t launch_route_finalize(const int32_t* hist, const float* psum, int nc
                                   int64_t T, int64_t C, int32_t* counts, float* aux,
                                   int32_t* chunk_base, int32_t* kept, int32_t* offsets,
                                   int32_t* dropped, float* stats, cudaStream_t stream) {
-  route_finalize_kernel<<<1, kFinThreads, 0, stream>>>(hist, psum, nchunks, E, T, C, counts, aux,
+  launch_pdl(route_finalize_kernel, 1, kFinThreads, 0, stream, hist, psum, nchunks, E, T, C, counts, aux,
                                                        chunk_base, kept, offsets, dropped, stats);
   return cudaGetLastError();
 }

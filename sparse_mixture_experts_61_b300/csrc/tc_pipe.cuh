@@ -280,7 +280,7 @@ cudaError_t launch_pipe(Kern kern, size_t smem, int grid, const CUtensorMap& a,
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  kern<<<grid, threads, smem, stream>>>(a, b, args);
+  launch_pdl(kern, grid, threads, smem, stream, a, b, args);
   return cudaGetLastError();
 }
 
