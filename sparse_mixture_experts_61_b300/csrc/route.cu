@@ -281,13 +281,22 @@ __global__ void __launch_bounds__(kFinThreads)
     s_cnt[tid] = cnt;
     s_ps[tid] = ps;
     __syncthreads();
-    // Position bases: the counts of the lower slices, then this slice's chunks in order.
+    // Position bases: the counts of the lower slices, then this slice's chunks in order
+    // (loads issued eight at a time).
     if (chunk_base && ex < E) {
       int base = 0;
       for (int q = 0; q < sl; ++q) base += s_cnt[q * EP + ex];
-      for (int c = c_lo; c < c_hi; ++c) {
-        chunk_base[static_cast<int64_t>(c) * E + ex] = base;
-        base += hist[static_cast<int64_t>(c) * E + ex];
+      constexpr int B = 8;
+      for (int c0 = c_lo; c0 < c_hi; c0 += B) {
+        int hv[B];
+#pragma unroll
+        for (int i = 0; i < B; ++i)
+          hv[i] = c0 + i < c_hi ? hist[static_cast<int64_t>(c0 + i) * E + ex] : 0;
+#pragma unroll
+        for (int i = 0; i < B; ++i) {
+          if (c0 + i < c_hi) chunk_base[static_cast<int64_t>(c0 + i) * E + ex] = base;
+          base += hv[i];
+        }
       }
     }
   }
