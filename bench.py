@@ -86,11 +86,15 @@ def dist_env():
     return world, rank, local
 
 
-def dist_init(world, local):
+def dist_init(world, local, backend="nccl"):
+    """One process per GPU (NCCL); the gloo backend runs the same rendezvous on CPU."""
     if world > 1:
         import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        else:
+            dist.init_process_group(backend)
 
 
 def barrier(world):
@@ -99,13 +103,19 @@ def barrier(world):
         dist.barrier()
 
 
-def allreduce_max(v: float, world: int) -> float:
+def allreduce_max(v: float, world: int, device: str = "cuda") -> float:
+    """The slowest rank's value (timings are taken as the max over ranks)."""
     if world == 1:
         return v
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    t = torch.tensor([v], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def replica_throughput(world: int, tokens_per_rank: int, slowest_ms: float) -> float:
+    """Weak scaling: every rank runs its own batch; tokens of all ranks / slowest rank's time."""
+    return world * tokens_per_rank / (slowest_ms / 1e3)
 
 
 # ------------------------------------------------------------------ clocks
@@ -423,7 +433,7 @@ def run_ours(args, world, rank, local):
     peaks = load_peaks()
     line = {
         "metric": METRIC,
-        "value": round(world * w.T / (mean_ms / 1e3), 1),
+        "value": round(replica_throughput(world, w.T, mean_ms), 1),
         "unit": UNIT,
         "n_gpus": world,
         "steps": args.steps,
@@ -442,7 +452,7 @@ def run_ours(args, world, rank, local):
                    "l2": "flushed before every timed step (256 MB write outside the event pair)",
                    "parallelism": f"replicas x{world} (token-parallel, no collective)"},
         "roofline": roofline(w, M, nonempty, t_ffn, peaks),
-        "e2e": {"value": round(world * w.T / (e2e_ms / 1e3), 1), "unit": UNIT,
+        "e2e": {"value": round(replica_throughput(world, w.T, e2e_ms), 1), "unit": UNIT,
                 "h2d_bytes_per_step": x_host.numel() * x_host.element_size(),
                 "d2h_bytes_per_step": y_host.numel() * y_host.element_size()},
         "gpu_launches": (KERNELS_PER_EC_FORWARD if ec else KERNELS_PER_FORWARD) * args.steps,
@@ -539,7 +549,7 @@ def run_train(args, world, rank, local):
     achieved = flops / (bwd_ms / 1e3) / 1e12
     return {
         "metric": TRAIN_METRIC,
-        "value": round(world * T / (step_ms / 1e3), 1),
+        "value": round(replica_throughput(world, T, step_ms), 1),
         "unit": UNIT,
         "n_gpus": world,
         "steps": args.steps,
