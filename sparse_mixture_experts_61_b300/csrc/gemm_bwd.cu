@@ -190,11 +190,11 @@ struct WgradSmem {
   int abort;
 };
 
-// Zero rows [valid, 64) of the nbox 8 KB boxes at `base` (each row 128 bytes); all 32
+// Zero rows [valid, end) of the nbox 8 KB boxes at `base` (each row 128 bytes); all 32
 // lanes of the calling warp take part.
-__device__ __forceinline__ void zero_box_rows(uint8_t* base, int nbox, int valid) {
+__device__ __forceinline__ void zero_box_rows(uint8_t* base, int nbox, int valid, int end) {
   const int lane = threadIdx.x & 31;
-  const int chunks = (64 - valid) * 8;  // 16-byte chunks per box
+  const int chunks = (end - valid) * 8;  // 16-byte chunks per box
   for (int b = 0; b < nbox; ++b) {
     uint4* p = reinterpret_cast<uint4*>(base + b * kBoxBytes + valid * 128);
     for (int i = lane; i < chunks; i += 32) p[i] = make_uint4(0u, 0u, 0u, 0u);
@@ -202,8 +202,10 @@ __device__ __forceinline__ void zero_box_rows(uint8_t* base, int nbox, int valid
 }
 
 // Warps: 0 = TMA producer, 1 = MMA issuer (and TMEM owner), 2-5 = epilogue, 6 = fixup of
-// each group's last k-block (waits for its copies, zeroes the rows past the group,
-// then releases the stage to the MMA warp), so the producer never waits on it.  The
+// each group's last k-block.  The MMA warp runs only the 16-row K steps that hold rows
+// of the group; when the last of them is partial, the fixup warp waits for the copies,
+// zeroes that step's rows past the group (at most 15 rows per box) and then releases
+// the stage to the MMA warp, so the producer never waits on it.  The
 // fixup warp observes every stage fill in order and a stage is refilled only after both
 // the MMA warp and the fixup warp have released it (two arrivals on `empty`), so the
 // fixup warp is never more than one phase behind a stage's `full` barrier.
@@ -313,9 +315,10 @@ __global__ void __launch_bounds__(WG_THREADS, 1)
           ok = false;
           break;
         }
-        if (kb == c.nkb - 1 && c.tail < WG_BK) {
-          zero_box_rows(S.a[s], WG_BM / 64, c.tail);
-          zero_box_rows(S.b[s], WG_BN / 64, c.tail);
+        if (kb == c.nkb - 1 && (c.tail & 15) != 0) {
+          const int end = (c.tail + 15) & ~15;
+          zero_box_rows(S.a[s], WG_BM / 64, c.tail, end);
+          zero_box_rows(S.b[s], WG_BN / 64, c.tail, end);
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(&S.fixed[s]));
@@ -341,7 +344,9 @@ __global__ void __launch_bounds__(WG_THREADS, 1)
         tc_fence_after();
         const uint32_t d_tmem = S.tmem_base + static_cast<uint32_t>(acc * WG_BN);
         for (int kb = 0; kb < c.nkb; ++kb) {
-          const bool is_tail = kb == c.nkb - 1 && c.tail < WG_BK;
+          const bool last = kb == c.nkb - 1;
+          const bool is_tail = last && (c.tail & 15) != 0;  // partial 16-row step: wait for fixup
+          const int ksteps = last ? (c.tail + 15) / 16 : WG_BK / 16;
           const bool got = is_tail
                                ? mbar_wait_bounded(smem_u32(&S.fixed[s]), (fph >> s) & 1u, abort,
                                                    p.flags)
@@ -353,8 +358,7 @@ __global__ void __launch_bounds__(WG_THREADS, 1)
           if (is_tail) fph ^= 1u << s;
           tc_fence_after();
           const uint32_t a0 = smem_u32(S.a[s]), b0 = smem_u32(S.b[s]);
-#pragma unroll
-          for (int kk = 0; kk < WG_BK / 16; ++kk)
+          for (int kk = 0; kk < ksteps; ++kk)
             tc_mma_bf16(d_tmem, sw128_mnmajor_desc(a0 + kk * 2048, kBoxBytes),
                         sw128_mnmajor_desc(b0 + kk * 2048, kBoxBytes), kIdesc,
                         (kb != 0 || kk != 0) ? 1u : 0u);
