@@ -179,6 +179,25 @@ __global__ void __launch_bounds__(kDxThreads)
   reinterpret_cast<uint4*>(dx + t * d)[v] = o;
 }
 
+// Tail packing: CTA (g, r) writes row r of group g's zero-padded last k-block.
+constexpr int kPackThreads = 128;
+
+__global__ void __launch_bounds__(kPackThreads)
+    pack_tails_kernel(const __nv_bfloat16* __restrict__ A, int cols,
+                      const int32_t* __restrict__ offsets, __nv_bfloat16* __restrict__ tail) {
+  pdl_enter();
+  const int g = blockIdx.x, r = blockIdx.y;
+  const int64_t base = offsets[g], n = offsets[g + 1] - base;
+  if (n <= 0) return;
+  const int64_t nkb = (n + 63) / 64;
+  const int valid = static_cast<int>(n - (nkb - 1) * 64);
+  if (valid == 64) return;  // the group's last k-block is whole: read in place
+  uint4* dst = reinterpret_cast<uint4*>(tail + (static_cast<int64_t>(g) * 64 + r) * cols);
+  const uint4* src = reinterpret_cast<const uint4*>(A + (base + (nkb - 1) * 64 + r) * cols);
+  for (int v = threadIdx.x; v < cols / 8; v += kPackThreads)
+    dst[v] = r < valid ? __ldg(src + v) : make_uint4(0u, 0u, 0u, 0u);
+}
+
 // Per-group prefix of 64-row slices; thread 0..31 of the block compute it.
 constexpr int kSlice = 64;
 constexpr int kColThreads = 256;
@@ -288,6 +307,15 @@ cudaError_t launch_bwd_dx(const void* dxr, const void* dxp, const int32_t* slot_
   launch_pdl(bwd_dx_kernel, grid, kDxThreads, 0, stream, 
       static_cast<const __nv_bfloat16*>(dxr), static_cast<const __nv_bfloat16*>(dxp), slot_row, d,
       k, static_cast<__nv_bfloat16*>(dx));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pack_tails(const void* A, int cols, const int32_t* offsets, int G, void* tail,
+                              cudaStream_t stream) {
+  if (G <= 0) return cudaSuccess;
+  launch_pdl(pack_tails_kernel, dim3(static_cast<unsigned>(G), 64), kPackThreads, 0, stream,
+             static_cast<const __nv_bfloat16*>(A), cols, offsets,
+             static_cast<__nv_bfloat16*>(tail));
   return cudaGetLastError();
 }
 

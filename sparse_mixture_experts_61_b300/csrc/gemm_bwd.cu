@@ -16,9 +16,8 @@
 // loaded as four 64-column boxes of the [G][K][N] weights.  The weight-gradient kernel
 // tiles each expert's output [Mdim x Ndim] in 128 x 256 blocks and walks the expert's
 // rows in 64-row k-blocks; the last k-block of an expert usually runs into the next
-// expert's rows, so once its copies have landed the producer warp zeroes the rows past
-// the expert's end in shared memory (whole 128-byte rows, so the swizzle does not
-// matter) and only then releases the stage to the MMA warp.
+// expert's rows, so it is read from zero-padded copies of each expert's last rows
+// (backward.cu packs them before the launch).
 
 #include "tc_pipe.cuh"
 
@@ -170,7 +169,7 @@ __global__ void __launch_bounds__(ROWS_THREADS, 1)
 // ------------------------------------------------------------- weight gradients
 constexpr int WG_BM = 128, WG_BN = 256, WG_BK = 64;  // output tile; rows per k-block
 constexpr int WG_STAGES = 4;
-constexpr int WG_THREADS = 224;        // producer, MMA, 4 epilogue warps, tail-fixup warp
+constexpr int WG_THREADS = 192;        // producer, MMA, 4 epilogue warps
 constexpr int WG_STG_BOX = 32 * 128;   // one staged store box: 32 rows x 64 bf16
 
 // bf16 outputs leave through shared memory and TMA stores (whole 128-byte lines of the
@@ -182,7 +181,6 @@ struct WgradSmem {
   uint8_t stg[4][2][WG_STG_BOX];            // [epilogue warp][box]
   uint64_t full[WG_STAGES];
   uint64_t empty[WG_STAGES];
-  uint64_t fixed[WG_STAGES];  // tail k-block: rows past the group zeroed
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t drain;
@@ -190,29 +188,18 @@ struct WgradSmem {
   int abort;
 };
 
-// Zero rows [valid, end) of the nbox 8 KB boxes at `base` (each row 128 bytes); all 32
-// lanes of the calling warp take part.
-__device__ __forceinline__ void zero_box_rows(uint8_t* base, int nbox, int valid, int end) {
-  const int lane = threadIdx.x & 31;
-  const int chunks = (end - valid) * 8;  // 16-byte chunks per box
-  for (int b = 0; b < nbox; ++b) {
-    uint4* p = reinterpret_cast<uint4*>(base + b * kBoxBytes + valid * 128);
-    for (int i = lane; i < chunks; i += 32) p[i] = make_uint4(0u, 0u, 0u, 0u);
-  }
-}
-
-// Warps: 0 = TMA producer, 1 = MMA issuer (and TMEM owner), 2-5 = epilogue, 6 = fixup of
-// each group's last k-block.  The MMA warp runs only the 16-row K steps that hold rows
-// of the group; when the last of them is partial, the fixup warp waits for the copies,
-// zeroes that step's rows past the group (at most 15 rows per box) and then releases
-// the stage to the MMA warp, so the producer never waits on it.  The
-// fixup warp observes every stage fill in order and a stage is refilled only after both
-// the MMA warp and the fixup warp have released it (two arrivals on `empty`), so the
-// fixup warp is never more than one phase behind a stage's `full` barrier.
+// Warps: 0 = TMA producer, 1 = MMA issuer (and TMEM owner), 2-5 = epilogue.  The K loop
+// of group g covers its rows in 64-row k-blocks.  A last k-block that would run into the
+// next group's rows is read instead from the zero-padded copies of each group's last
+// rows (tmAt / tmBt, [G, 64, cols], filled by the tail-packing kernel), and only its K
+// steps holding rows of the group are issued.  Without offsets (one dense group), rows
+// past the end lie outside the tensor and TMA fills them with zeros.
 template <bool OUT_F32>
 __global__ void __launch_bounds__(WG_THREADS, 1)
     tc_wgrad_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmAt,
+                    const __grid_constant__ CUtensorMap tmBt,
                     const __grid_constant__ CUtensorMap tmO, const WgradArgs p) {
   pdl_enter();
   constexpr uint32_t kTmemCols = 2 * WG_BN;
@@ -223,8 +210,7 @@ __global__ void __launch_bounds__(WG_THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < WG_STAGES; ++s) {
       mbar_init(smem_u32(&S.full[s]), 1);
-      mbar_init(smem_u32(&S.empty[s]), 2);  // MMA commit + fixup warp
-      mbar_init(smem_u32(&S.fixed[s]), 1);
+      mbar_init(smem_u32(&S.empty[s]), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&S.tfull[i]), 1);
@@ -235,6 +221,10 @@ __global__ void __launch_bounds__(WG_THREADS, 1)
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    if (p.offsets) {
+      tma_prefetch_desc(&tmAt);
+      tma_prefetch_desc(&tmBt);
+    }
     if (!OUT_F32) tma_prefetch_desc(&tmO);
   }
   if (warp == 1) {
@@ -281,14 +271,23 @@ __global__ void __launch_bounds__(WG_THREADS, 1)
             break;
           }
           const uint32_t fb = smem_u32(&S.full[s]);
-          const int row = static_cast<int>(c.row0) + kb * WG_BK;
           mbar_arrive_expect_tx(fb, kStageBytes);
+          if (p.offsets && kb == c.nkb - 1 && c.tail < WG_BK) {
 #pragma unroll
-          for (int j = 0; j < WG_BM / 64; ++j)
-            tma_load_2d(smem_u32(S.a[s]) + j * kBoxBytes, &tmA, fb, c.m0 + 64 * j, row);
+            for (int j = 0; j < WG_BM / 64; ++j)
+              tma_load_3d(smem_u32(S.a[s]) + j * kBoxBytes, &tmAt, fb, c.m0 + 64 * j, 0, c.g);
 #pragma unroll
-          for (int j = 0; j < WG_BN / 64; ++j)
-            tma_load_2d(smem_u32(S.b[s]) + j * kBoxBytes, &tmB, fb, c.n0 + 64 * j, row);
+            for (int j = 0; j < WG_BN / 64; ++j)
+              tma_load_3d(smem_u32(S.b[s]) + j * kBoxBytes, &tmBt, fb, c.n0 + 64 * j, 0, c.g);
+          } else {
+            const int row = static_cast<int>(c.row0) + kb * WG_BK;
+#pragma unroll
+            for (int j = 0; j < WG_BM / 64; ++j)
+              tma_load_2d(smem_u32(S.a[s]) + j * kBoxBytes, &tmA, fb, c.m0 + 64 * j, row);
+#pragma unroll
+            for (int j = 0; j < WG_BN / 64; ++j)
+              tma_load_2d(smem_u32(S.b[s]) + j * kBoxBytes, &tmB, fb, c.n0 + 64 * j, row);
+          }
           issued |= 1u << s;
           issued_par = (issued_par & ~(1u << s)) | (ph << s);
           if (++s == WG_STAGES) {
@@ -302,38 +301,10 @@ __global__ void __launch_bounds__(WG_THREADS, 1)
           if ((issued >> q) & 1u) mbar_wait_unwind(smem_u32(&S.full[q]), (issued_par >> q) & 1u);
       }
     }
-  } else if (warp == 6) {
-    int s = 0;
-    uint32_t ph = 0;
-    bool ok = true;
-    for (int tile = first; ok && tile < total; tile += step) {
-      const Coord c = decode(tile);
-      for (int kb = 0; kb < c.nkb; ++kb) {
-        bool landed = true;
-        if (lane == 0) landed = mbar_wait_bounded(smem_u32(&S.full[s]), ph, abort, p.flags);
-        if (!__shfl_sync(0xffffffffu, landed, 0)) {
-          ok = false;
-          break;
-        }
-        if (kb == c.nkb - 1 && (c.tail & 15) != 0) {
-          const int end = (c.tail + 15) & ~15;
-          zero_box_rows(S.a[s], WG_BM / 64, c.tail, end);
-          zero_box_rows(S.b[s], WG_BN / 64, c.tail, end);
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&S.fixed[s]));
-        }
-        if (lane == 0) mbar_arrive(smem_u32(&S.empty[s]));
-        if (++s == WG_STAGES) {
-          s = 0;
-          ph ^= 1u;
-        }
-      }
-    }
   } else if (warp == 1) {
     if (lane == 0) {
       int s = 0, acc = 0;
-      uint32_t ph = 0, fph = 0, aph = 0;
+      uint32_t ph = 0, aph = 0;
       bool ok = true, issued_any = false;
       for (int tile = first; ok && tile < total; tile += step) {
         const Coord c = decode(tile);
@@ -344,19 +315,13 @@ __global__ void __launch_bounds__(WG_THREADS, 1)
         tc_fence_after();
         const uint32_t d_tmem = S.tmem_base + static_cast<uint32_t>(acc * WG_BN);
         for (int kb = 0; kb < c.nkb; ++kb) {
-          const bool last = kb == c.nkb - 1;
-          const bool is_tail = last && (c.tail & 15) != 0;  // partial 16-row step: wait for fixup
-          const int ksteps = last ? (c.tail + 15) / 16 : WG_BK / 16;
-          const bool got = is_tail
-                               ? mbar_wait_bounded(smem_u32(&S.fixed[s]), (fph >> s) & 1u, abort,
-                                                   p.flags)
-                               : mbar_wait_bounded(smem_u32(&S.full[s]), ph, abort, p.flags);
-          if (!got) {
+          if (!mbar_wait_bounded(smem_u32(&S.full[s]), ph, abort, p.flags)) {
             ok = false;
             break;
           }
-          if (is_tail) fph ^= 1u << s;
           tc_fence_after();
+          // K steps of 16 rows that hold rows of the group (the rest are zero).
+          const int ksteps = kb == c.nkb - 1 ? (c.tail + 15) / 16 : WG_BK / 16;
           const uint32_t a0 = smem_u32(S.a[s]), b0 = smem_u32(S.b[s]);
           for (int kk = 0; kk < ksteps; ++kk)
             tc_mma_bf16(d_tmem, sw128_mnmajor_desc(a0 + kk * 2048, kBoxBytes),
@@ -500,11 +465,15 @@ cudaError_t launch_tc_bwd_rows(const GemmArgs& a, int epi, int sm_count, cudaStr
 }
 
 cudaError_t launch_tc_wgrad(const WgradArgs& a, int sm_count, cudaStream_t stream) {
-  CUtensorMap tmA, tmB, tmO{};
-  // [rows, Mdim] and [rows, Ndim] row-major, read as 64-column x 64-row boxes; a bf16
-  // output [G, Mdim, Ndim] is written as 64-column x 32-row boxes.
+  CUtensorMap tmA, tmB, tmAt{}, tmBt{}, tmO{};
+  // [rows, Mdim] and [rows, Ndim] row-major, read as 64-column x 64-row boxes (the tail
+  // copies [G, 64, cols] likewise); a bf16 output [G, Mdim, Ndim] is written as
+  // 64-column x 32-row boxes.
   const int G = a.offsets ? a.G : 1;
   if (!rows_map(&tmA, a.A, a.rows_alloc, a.Mdim, 64) || !rows_map(&tmB, a.B, a.rows_alloc, a.Ndim, 64))
+    return cudaErrorInvalidValue;
+  if (a.offsets && (!a.tailA || !a.tailB || !stacked_map(&tmAt, a.tailA, G, 64, a.Mdim, 64) ||
+                    !stacked_map(&tmBt, a.tailB, G, 64, a.Ndim, 64)))
     return cudaErrorInvalidValue;
   if (!a.out_f32 && !stacked_map(&tmO, a.out, G, a.Mdim, a.Ndim, 32)) return cudaErrorInvalidValue;
   const int64_t tiles = static_cast<int64_t>(G) * ((a.Mdim + WG_BM - 1) / WG_BM) *
@@ -516,7 +485,7 @@ cudaError_t launch_tc_wgrad(const WgradArgs& a, int sm_count, cudaStream_t strea
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  launch_pdl(kern, grid, WG_THREADS, smem, stream, tmA, tmB, tmO, a);
+  launch_pdl(kern, grid, WG_THREADS, smem, stream, tmA, tmB, tmAt, tmBt, tmO, a);
   return cudaGetLastError();
 }
 

@@ -127,8 +127,18 @@ struct WgradArgs {
   void* out;
   bool out_f32;
   int* flags;
+  // With offsets: each group's last k-block when it is partial, zero-padded to 64 rows
+  // ([G, 64, Mdim] and [G, 64, Ndim], see launch_pack_tails).
+  const void* tailA;
+  const void* tailB;
 };
 cudaError_t launch_tc_wgrad(const WgradArgs& a, int sm_count, cudaStream_t stream);
+
+// For every group with rows [offsets[g], offsets[g+1]) whose last 64-row block is partial:
+// tail[g][r] = A[offsets[g] + 64*(nkb-1) + r] for r < the block's rows, 0 up to 64 rows
+// (bf16, [G, 64, cols]); other groups' slots are not written.
+cudaError_t launch_pack_tails(const void* A, int cols, const int32_t* offsets, int G, void* tail,
+                              cudaStream_t stream);
 
 // Backward of the combine: for kept slot (t,j) in row r = slot_row[t,j]:
 //   dy_perm[r] = topk_w[t,j] * dy[t] (bf16),  dw[t,j] = <dy[t], y_perm[r]> (fp32);

@@ -577,7 +577,7 @@ namespace moe {
 namespace {
 
 struct BwdLayout {
-  size_t flags, dyp, da, dxp, dxr, dw, dl, dl16, dwg, partial, total;
+  size_t flags, dyp, da, dxp, dxr, dw, dl, dl16, dwg, tail_a, tail_b, partial, total;
   int Epad;
 };
 
@@ -598,6 +598,9 @@ BwdLayout make_bwd_layout(const moe_config& c) {
   L.dl = o; o = align_up(o + T * E * 4);
   L.dl16 = o; o = align_up(o + T * L.Epad * 2);
   L.dwg = o; o = align_up(o + static_cast<int64_t>(L.Epad) * c.d * 4);
+  const int64_t tail_bytes = E * 64 * std::max(c.d, c.h) * 2;
+  L.tail_a = o; o = align_up(o + tail_bytes);
+  L.tail_b = o; o = align_up(o + tail_bytes);
   L.partial = o; o = align_up(o + pf * 4);
   L.total = o;
   return L;
@@ -702,12 +705,16 @@ MOE_EXPORT moe_status moe_backward(const moe_config* cfg, const moe_backward_arg
   wg.rows_alloc = rows;
   wg.G = c.E;
   wg.flags = flags;
+  wg.tailA = at<void>(ws, L.tail_a);
+  wg.tailB = at<void>(ws, L.tail_b);
   if (a->dw2) {
     wg.A = dyp;
     wg.Mdim = c.d;
     wg.B = a->h_act;
     wg.Ndim = c.h;
     wg.out = a->dw2;
+    MOE_CUDA(launch_pack_tails(wg.A, wg.Mdim, a->offsets, c.E, at<void>(ws, L.tail_a), st));
+    MOE_CUDA(launch_pack_tails(wg.B, wg.Ndim, a->offsets, c.E, at<void>(ws, L.tail_b), st));
     MOE_CUDA(launch_tc_wgrad(wg, sms, st));
   }
   if (a->dw1) {
@@ -716,6 +723,8 @@ MOE_EXPORT moe_status moe_backward(const moe_config* cfg, const moe_backward_arg
     wg.B = a->x_perm;
     wg.Ndim = c.d;
     wg.out = a->dw1;
+    MOE_CUDA(launch_pack_tails(wg.A, wg.Mdim, a->offsets, c.E, at<void>(ws, L.tail_a), st));
+    MOE_CUDA(launch_pack_tails(wg.B, wg.Ndim, a->offsets, c.E, at<void>(ws, L.tail_b), st));
     MOE_CUDA(launch_tc_wgrad(wg, sms, st));
   }
   if (a->dw_gate) {
