@@ -21,12 +21,15 @@
  *
  * Conventions for every entry point:
  *  - Pointers are DEVICE pointers owned by the caller (CUDA allocations on the
- *    current device), contiguous and row-major.  Activations, weights, expert
+ *    current device; the batches of moe_forward_host are host pointers),
+ *    contiguous and row-major.  Activations, weights, expert
  *    biases, row buffers and the workspace are 16-byte aligned; int32 and fp32
  *    arrays 4-byte aligned; misalignment is MOE_ERR_INVALID_ARGUMENT.  With an
  *    empty batch (T = 0) the token-indexed buffers may be NULL.  The library
- *    allocates no memory, keeps no per-call state and may be called from
- *    several host threads on different streams with different workspaces.
+ *    allocates no memory (moe_forward_host creates two copy streams and some
+ *    events per call and releases them), keeps no per-call state and may be
+ *    called from several host threads on different streams with different
+ *    workspaces.
  *  - Calls enqueue work on `stream` and return after host-side validation; no
  *    call waits for the GPU except moe_device_error.  The number of kept rows M
  *    never travels to the host: row buffers are sized for the worst case T*k.
@@ -334,6 +337,59 @@ moe_status moe_expert_choice_workspace_size(const moe_config* cfg, size_t* bytes
    logit), MOE_DEVERR_TIMEOUT (a GEMM wait gave up). */
 moe_status moe_expert_choice_forward(const moe_config* cfg, const moe_expert_choice_args* args,
                                      void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* ---- Batches in host memory --------------------------------------------------
+   A pipelined forward over a sequence of independent batches whose token rows x
+   and outputs y live in HOST memory, for a caller that streams batches through one
+   resident copy of the weights.  The pages have no counterpart; the layer itself is
+   the one above.  Batch i's x is copied to the device, the layer runs on it (exactly
+   the kernels of moe_forward, or of moe_expert_choice_forward, so its y is bitwise
+   the y of that call on the same x), and its y is copied back.  The copies run on
+   two streams the call creates (and releases before returning; CUDA frees them when
+   their work completes), each batch's x and y double-buffered in the workspace, so
+   batch i+1's host-to-device copy and batch i-1's device-to-host copy overlap batch
+   i's layer.  Ordering: all of it starts after the work already enqueued on
+   `stream`, and work enqueued on `stream` afterwards starts after all of it,
+   including the last copy back; synchronise `stream` before reading y.
+   Host buffers are the caller's and must stay valid (x unmodified) until then; they
+   should be page-locked (cudaHostAlloc / cudaHostRegister): pageable memory gives the
+   same results but the copies then do not overlap the layer.  Device flags
+   accumulate over the batches (cleared once at the start; moe_device_error(ws)). */
+typedef enum { MOE_ROUTING_TOPK = 0, MOE_ROUTING_EXPERT_CHOICE = 1 } moe_routing;
+
+/* Device-resident weights shared by every batch (same shapes, dtype and rules as
+   the fields of moe_forward_args of the same names). */
+typedef struct moe_weights {
+  const void* w_gate;       /* [E,d] dtype */
+  const float* logit_bias;  /* [E] fp32, or NULL */
+  const void* w1;           /* [E,h,d] dtype */
+  const void* b1;           /* [E,h] dtype, or NULL for zero */
+  const void* w2;           /* [E,d,h] dtype */
+  const void* b2;           /* [E,d] dtype, or NULL for zero */
+} moe_weights;
+
+typedef struct moe_host_batches {
+  int64_t n;                /* number of batches, >= 1 */
+  const void* const* x;     /* [n] HOST pointers, each to a [T,d] dtype batch (NULL only if T = 0) */
+  void* const* y;           /* [n] HOST pointers, each to [T,d] dtype outputs (NULL only if T = 0) */
+  float* aux_loss;          /* [n] HOST fp32: batch i's balance statistic (top-k routing
+                               only; must be NULL for expert choice), or NULL */
+} moe_host_batches;
+
+/* Workspace bytes moe_forward_host needs: the routing's forward workspace followed
+   by two device copies of a batch's x and two of its y.  routing: moe_routing.
+   Host only. */
+moe_status moe_forward_host_workspace_size(const moe_config* cfg, int32_t routing,
+                                           size_t* bytes);
+
+/* The pipelined forward over host batches (above).  cfg->noise must be
+   MOE_NOISE_NONE (the draws are per-batch device inputs): otherwise
+   MOE_ERR_UNSUPPORTED.  Every argument, and the layer's own validation, is checked
+   before anything is enqueued.  With T = 0 nothing is copied and aux_loss, when
+   given, is set to 0 on the host before the call returns. */
+moe_status moe_forward_host(const moe_config* cfg, int32_t routing, const moe_weights* weights,
+                            const moe_host_batches* batches, void* ws, size_t ws_bytes,
+                            moe_stream_t stream);
 
 /* Waits for `stream`, then reads the device flag word at the start of `ws` into
    *flags (may be NULL).  Returns MOE_ERR_DEVICE when any bit is set, MOE_OK

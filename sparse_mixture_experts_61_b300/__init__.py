@@ -32,6 +32,9 @@ MOE_NOISE_GUMBEL = 1
 MOE_NOISE_PROB_GAUSS = 2
 MOE_NOISE_LOGIT_SOFTMAX = 3
 
+MOE_ROUTING_TOPK = 0
+MOE_ROUTING_EXPERT_CHOICE = 1
+
 MOE_DEVERR_BAD_INDEX = 1
 MOE_DEVERR_BAD_ROW = 2
 MOE_DEVERR_NONFINITE = 4
@@ -42,7 +45,8 @@ EXPORTED = ("moe_status_str", "moe_capacity", "moe_workspace_size", "moe_stage_w
             "moe_route", "moe_dispatch", "moe_expert_ffn", "moe_combine", "moe_forward",
             "moe_device_error", "moe_dispatch_static", "moe_selftest_wait_timeout",
             "moe_expert_choice_capacity", "moe_expert_choice_workspace_size",
-            "moe_expert_choice_forward", "moe_backward_workspace_size", "moe_backward")
+            "moe_expert_choice_forward", "moe_backward_workspace_size", "moe_backward",
+            "moe_forward_host_workspace_size", "moe_forward_host")
 
 # Table cells of moe_dispatch_static's library-held scratch (include/moe.h).
 MOE_DISPATCH_STATIC_MAX_CELLS = 262144
@@ -85,6 +89,18 @@ class MoeExpertChoiceArgs(ctypes.Structure):
         "sel_w", "token_experts", "unrouted")]
 
 
+WEIGHTS = ("w_gate", "logit_bias", "w1", "b1", "w2", "b2")
+
+
+class MoeWeights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in WEIGHTS]
+
+
+class MoeHostBatches(ctypes.Structure):
+    _fields_ = [("n", ctypes.c_int64), ("x", ctypes.POINTER(ctypes.c_void_p)),
+                ("y", ctypes.POINTER(ctypes.c_void_p)), ("aux_loss", ctypes.c_void_p)]
+
+
 _lib = None
 
 
@@ -116,6 +132,9 @@ def lib():
         L.moe_expert_choice_forward.argtypes = [cfg, ctypes.POINTER(MoeExpertChoiceArgs), P, S, P]
         L.moe_backward_workspace_size.argtypes = [cfg, ctypes.POINTER(S)]
         L.moe_backward.argtypes = [cfg, ctypes.POINTER(MoeBackwardArgs), P, S, P]
+        L.moe_forward_host_workspace_size.argtypes = [cfg, ctypes.c_int32, ctypes.POINTER(S)]
+        L.moe_forward_host.argtypes = [cfg, ctypes.c_int32, ctypes.POINTER(MoeWeights),
+                                       ctypes.POINTER(MoeHostBatches), P, S, P]
         for name in EXPORTED:
             if name != "moe_status_str":
                 getattr(L, name).restype = ctypes.c_int
@@ -321,3 +340,35 @@ def moe_backward(cfg, inputs: dict, outputs: dict, d_aux: float, ws, stream=None
         args = backward_args(inputs, outputs, d_aux)
     _check(lib().moe_backward(ctypes.byref(cfg), ctypes.byref(args), _p(ws),
                               ws.numel() * ws.element_size(), _stream(stream)), "moe_backward")
+
+
+_ROUTING = {"topk": MOE_ROUTING_TOPK, "expert_choice": MOE_ROUTING_EXPERT_CHOICE}
+
+
+def moe_forward_host_workspace_size(cfg: MoeConfig, routing: str = "topk") -> int:
+    v = ctypes.c_size_t()
+    _check(lib().moe_forward_host_workspace_size(ctypes.byref(cfg), _ROUTING[routing],
+                                                 ctypes.byref(v)),
+           "moe_forward_host_workspace_size")
+    return v.value
+
+
+def moe_forward_host(cfg, weights: dict, xs, ys, ws, stream=None, routing: str = "topk",
+                     aux_loss=None):
+    """The layer over the host batches ``xs[i]`` -> ``ys[i]`` (CPU tensors, page-locked
+    for the copies to overlap the layer), weights on the device.  ``aux_loss``: an
+    optional CPU fp32 tensor of len(xs) for each batch's balance statistic.  Enqueued
+    on ``stream``; synchronise it before reading ``ys``."""
+    n = len(xs)
+    if len(ys) != n:
+        raise ValueError("xs and ys differ in length")
+    w = MoeWeights()
+    for name in WEIGHTS:
+        setattr(w, name, _p(weights.get(name)))
+    xa = (ctypes.c_void_p * max(n, 1))(*[_p(t) for t in xs])
+    ya = (ctypes.c_void_p * max(n, 1))(*[_p(t) for t in ys])
+    b = MoeHostBatches(n, ctypes.cast(xa, ctypes.POINTER(ctypes.c_void_p)),
+                       ctypes.cast(ya, ctypes.POINTER(ctypes.c_void_p)), _p(aux_loss))
+    _check(lib().moe_forward_host(ctypes.byref(cfg), _ROUTING[routing], ctypes.byref(w),
+                                  ctypes.byref(b), _p(ws), ws.numel() * ws.element_size(),
+                                  _stream(stream)), "moe_forward_host")

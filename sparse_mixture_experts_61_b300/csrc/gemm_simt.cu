@@ -5,9 +5,12 @@
 // for the first expert GEMM ("MoE mixture-of-experts routing mechanism",
 // Expert.forward = w2(silu(w1(x)))).
 //
-// 64x64 output tiles, 16-deep K slices staged in shared memory, 4x4 outputs per
-// thread.  Tiles never straddle two groups: group g owns ceil(rows_g/64) row
-// tiles, ordered (group, column block, row block) and walked grid-stride.
+// Output tiles of (16*TM) x (16*TN), TM x TN outputs per thread of 256; 32-deep K
+// slices staged in shared memory, double-buffered: the next slice is loaded into
+// registers while the current one is multiplied.  64x64 tiles when they fill the
+// GPU, 32x32 otherwise (small layers are latency-bound: more CTAs, fewer slices in
+// flight per CTA).  Tiles never straddle two groups: group g owns ceil(rows_g/BM)
+// row tiles, ordered (group, column block, row block) and walked grid-stride.
 
 #include <algorithm>
 
@@ -17,13 +20,18 @@
 namespace moe {
 namespace {
 
-constexpr int BM = 64, BN = 64, BK = 16;
+constexpr int BK = 32;
+constexpr int kSimtThreads = 256;
 
-template <int EPI>
-__global__ void __launch_bounds__(256) simt_gemm_f32_kernel(GemmArgs p) {
+template <int EPI, int TM, int TN>
+__global__ void __launch_bounds__(kSimtThreads) simt_gemm_f32_kernel(GemmArgs p) {
+  constexpr int BM = 16 * TM, BN = 16 * TN;
+  constexpr int KV = BK / 4;                      // float4 per row of a slice
+  constexpr int VA = (BM * KV + kSimtThreads - 1) / kSimtThreads;  // A vectors per thread
+  constexpr int VB = (BN * KV + kSimtThreads - 1) / kSimtThreads;
   pdl_enter();
-  __shared__ float As[BK][BM + 4];
-  __shared__ float Bs[BK][BN + 4];
+  __shared__ float As[2][BK][BM + 4];
+  __shared__ float Bs[2][BK][BN + 4];
   __shared__ int s_mpref[kMaxExperts + 1];
   const int tid = threadIdx.x;
   const int G = p.offsets ? p.G : 1;
@@ -55,7 +63,7 @@ __global__ void __launch_bounds__(256) simt_gemm_f32_kernel(GemmArgs p) {
   const float* bias = static_cast<const float*>(p.bias);
   float* out = static_cast<float*>(p.out);
   const int ty = tid >> 4, tx = tid & 15;
-  const int lr = tid >> 2, lk = (tid & 3) * 4;
+  const int nslices = (p.K + BK - 1) / BK;
 
   for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
     int lo = 0, hi = G;
@@ -73,45 +81,84 @@ __global__ void __launch_bounds__(256) simt_gemm_f32_kernel(GemmArgs p) {
     const int n0 = nb * BN;
     const float* Bg = B + static_cast<int64_t>(g) * p.N * p.K;
 
-    float acc[4][4];
+    // Slice loads: vector v of A covers row v / KV, columns 4 * (v % KV) .. +3.
+    float4 ra[VA], rb[VB];
+    auto load = [&](int k0) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+      for (int i = 0; i < VA; ++i) {
+        const int v = tid + i * kSimtThreads;
+        const int r = v / KV, kq = 4 * (v % KV);
+        ra[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (v < BM * KV && row0 + r < row_end && k0 + kq < p.K)
+          ra[i] = *reinterpret_cast<const float4*>(A + (row0 + r) * p.K + k0 + kq);
+      }
 #pragma unroll
-      for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+      for (int i = 0; i < VB; ++i) {
+        const int v = tid + i * kSimtThreads;
+        const int r = v / KV, kq = 4 * (v % KV);
+        rb[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (v < BN * KV && n0 + r < p.N && k0 + kq < p.K)
+          rb[i] = *reinterpret_cast<const float4*>(Bg + static_cast<int64_t>(n0 + r) * p.K + k0 +
+                                                   kq);
+      }
+    };
+    auto stage = [&](int buf) {
+#pragma unroll
+      for (int i = 0; i < VA; ++i) {
+        const int v = tid + i * kSimtThreads;
+        if (v < BM * KV) {
+          const int r = v / KV, kq = 4 * (v % KV);
+          As[buf][kq + 0][r] = ra[i].x; As[buf][kq + 1][r] = ra[i].y;
+          As[buf][kq + 2][r] = ra[i].z; As[buf][kq + 3][r] = ra[i].w;
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < VB; ++i) {
+        const int v = tid + i * kSimtThreads;
+        if (v < BN * KV) {
+          const int r = v / KV, kq = 4 * (v % KV);
+          Bs[buf][kq + 0][r] = rb[i].x; Bs[buf][kq + 1][r] = rb[i].y;
+          Bs[buf][kq + 2][r] = rb[i].z; Bs[buf][kq + 3][r] = rb[i].w;
+        }
+      }
+    };
 
-    for (int k0 = 0; k0 < p.K; k0 += BK) {
-      float4 va = make_float4(0.f, 0.f, 0.f, 0.f), vb = va;
-      const int64_t ar = row0 + lr;
-      if (ar < row_end && k0 + lk < p.K)
-        va = *reinterpret_cast<const float4*>(A + ar * p.K + k0 + lk);
-      const int bn = n0 + lr;
-      if (bn < p.N && k0 + lk < p.K)
-        vb = *reinterpret_cast<const float4*>(Bg + static_cast<int64_t>(bn) * p.K + k0 + lk);
-      As[lk + 0][lr] = va.x; As[lk + 1][lr] = va.y; As[lk + 2][lr] = va.z; As[lk + 3][lr] = va.w;
-      Bs[lk + 0][lr] = vb.x; Bs[lk + 1][lr] = vb.y; Bs[lk + 2][lr] = vb.z; Bs[lk + 3][lr] = vb.w;
-      __syncthreads();
+    float acc[TM][TN];
+#pragma unroll
+    for (int i = 0; i < TM; ++i)
+#pragma unroll
+      for (int j = 0; j < TN; ++j) acc[i][j] = 0.f;
+
+    load(0);
+    stage(0);
+    __syncthreads();
+    for (int s = 0; s < nslices; ++s) {
+      const int buf = s & 1;
+      if (s + 1 < nslices) load((s + 1) * BK);  // in flight during this slice's FMAs
 #pragma unroll
       for (int kk = 0; kk < BK; ++kk) {
-        float a4[4], b4[4];
+        float a[TM], b[TN];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) a4[i] = As[kk][ty * 4 + i];
+        for (int i = 0; i < TM; ++i) a[i] = As[buf][kk][ty * TM + i];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) b4[j] = Bs[kk][tx * 4 + j];
+        for (int j = 0; j < TN; ++j) b[j] = Bs[buf][kk][tx * TN + j];
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+        for (int i = 0; i < TM; ++i)
 #pragma unroll
-          for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a4[i], b4[j], acc[i][j]);
+          for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
       }
+      // The other buffer was last read in slice s-1, before the barrier that ended it.
+      if (s + 1 < nslices) stage(buf ^ 1);
       __syncthreads();
     }
 
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int64_t r = row0 + ty * 4 + i;
+    for (int i = 0; i < TM; ++i) {
+      const int64_t r = row0 + ty * TM + i;
       if (r >= row_end) continue;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int n = n0 + tx * 4 + j;
+      for (int j = 0; j < TN; ++j) {
+        const int n = n0 + tx * TN + j;
         if (n >= p.N) continue;
         float v = acc[i][j];
         if (bias) v += (EPI == EPI_ROUTER_F32) ? bias[n] : bias[static_cast<int64_t>(g) * p.N + n];
@@ -127,23 +174,37 @@ __global__ void __launch_bounds__(256) simt_gemm_f32_kernel(GemmArgs p) {
 
 }  // namespace
 
+template <int TM, int TN>
+void launch_simt_tiles(const GemmArgs& a, int epi, int64_t bound, int sm_count,
+                       cudaStream_t stream) {
+  const unsigned grid =
+      static_cast<unsigned>(std::min<int64_t>(bound, static_cast<int64_t>(sm_count) * 8));
+  switch (epi) {
+    case EPI_BIAS_SILU:
+      launch_pdl(simt_gemm_f32_kernel<EPI_BIAS_SILU, TM, TN>, grid, kSimtThreads, 0, stream, a);
+      break;
+    case EPI_BIAS:
+      launch_pdl(simt_gemm_f32_kernel<EPI_BIAS, TM, TN>, grid, kSimtThreads, 0, stream, a);
+      break;
+    default:
+      launch_pdl(simt_gemm_f32_kernel<EPI_ROUTER_F32, TM, TN>, grid, kSimtThreads, 0, stream, a);
+      break;
+  }
+}
+
 cudaError_t launch_simt_gemm_f32(const GemmArgs& a, int epi, int sm_count, cudaStream_t stream) {
   const int G = a.offsets ? a.G : 1;
   const int64_t rows = a.offsets ? a.rows_alloc : a.m_rows;
-  const int64_t bound = ((rows + BM - 1) / BM + (a.offsets ? G : 0)) * ((a.N + BN - 1) / BN);
-  const int64_t grid = std::min<int64_t>(bound, static_cast<int64_t>(sm_count) * 8);
-  if (grid <= 0) return cudaSuccess;
-  switch (epi) {
-    case EPI_BIAS_SILU:
-      launch_pdl(simt_gemm_f32_kernel<EPI_BIAS_SILU>, static_cast<unsigned>(grid), 256, 0, stream, a);
-      break;
-    case EPI_BIAS:
-      launch_pdl(simt_gemm_f32_kernel<EPI_BIAS>, static_cast<unsigned>(grid), 256, 0, stream, a);
-      break;
-    default:
-      launch_pdl(simt_gemm_f32_kernel<EPI_ROUTER_F32>, static_cast<unsigned>(grid), 256, 0, stream, a);
-      break;
-  }
+  // Upper bound on the tiles of a tile shape (each group adds at most one partial tile).
+  auto bound = [&](int bm, int bn) {
+    return ((rows + bm - 1) / bm + (a.offsets ? G : 0)) * ((a.N + bn - 1) / bn);
+  };
+  const int64_t b64 = bound(64, 64);
+  if (b64 <= 0) return cudaSuccess;
+  if (b64 >= sm_count)
+    launch_simt_tiles<4, 4>(a, epi, b64, sm_count, stream);
+  else
+    launch_simt_tiles<2, 2>(a, epi, bound(32, 32), sm_count, stream);
   return cudaGetLastError();
 }
 

@@ -11,6 +11,7 @@
 
 #include "../../include/moe.h"
 #include "common.cuh"
+#include "entry.h"
 #include "kernels.h"
 
 #define MOE_EXPORT extern "C" __attribute__((visibility("default")))
@@ -414,8 +415,8 @@ MOE_EXPORT moe_status moe_combine(const moe_config* cfg, const void* y_perm,
   return MOE_OK;
 }
 
-MOE_EXPORT moe_status moe_forward(const moe_config* cfg, const moe_forward_args* a, void* ws,
-                                  size_t ws_bytes, moe_stream_t stream) {
+moe_status moe::forward_entry(const moe_config* cfg, const moe_forward_args* a, void* ws,
+                              size_t ws_bytes, cudaStream_t st, EntryMode mode) {
   moe_status s = check_config(cfg);
   if (s != MOE_OK) return s;
   if (!a) return MOE_ERR_INVALID_ARGUMENT;
@@ -430,9 +431,9 @@ MOE_EXPORT moe_status moe_forward(const moe_config* cfg, const moe_forward_args*
     return MOE_ERR_INVALID_ARGUMENT;
   const Layout L = make_layout(c);
   if (!ws || !al16(ws) || ws_bytes < L.total) return MOE_ERR_WORKSPACE;
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (mode == EntryMode::kValidate) return MOE_OK;
   int* flags = at<int>(ws, L.flags);
-  MOE_CUDA(cudaMemsetAsync(flags, 0, sizeof(int), st));
+  if (mode == EntryMode::kRun) MOE_CUDA(cudaMemsetAsync(flags, 0, sizeof(int), st));
   int32_t* idx = a->topk_idx ? a->topk_idx : at<int32_t>(ws, L.idx);
   float* w = a->topk_w ? a->topk_w : at<float>(ws, L.w);
   int32_t* counts = a->counts ? a->counts : at<int32_t>(ws, L.counts);
@@ -475,6 +476,12 @@ MOE_EXPORT moe_status moe_forward(const moe_config* cfg, const moe_forward_args*
   return MOE_OK;
 }
 
+MOE_EXPORT moe_status moe_forward(const moe_config* cfg, const moe_forward_args* a, void* ws,
+                                  size_t ws_bytes, moe_stream_t stream) {
+  return forward_entry(cfg, a, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream),
+                       EntryMode::kRun);
+}
+
 MOE_EXPORT moe_status moe_device_error(const void* ws, moe_stream_t stream, int32_t* flags) {
   if (!ws) return MOE_ERR_WORKSPACE;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -502,9 +509,8 @@ MOE_EXPORT moe_status moe_expert_choice_workspace_size(const moe_config* cfg, si
   return MOE_OK;
 }
 
-MOE_EXPORT moe_status moe_expert_choice_forward(const moe_config* cfg,
-                                                const moe_expert_choice_args* a, void* ws,
-                                                size_t ws_bytes, moe_stream_t stream) {
+moe_status moe::ec_forward_entry(const moe_config* cfg, const moe_expert_choice_args* a,
+                                 void* ws, size_t ws_bytes, cudaStream_t st, EntryMode mode) {
   moe_status s = check_ec_config(cfg);
   if (s != MOE_OK) return s;
   if (!a) return MOE_ERR_INVALID_ARGUMENT;
@@ -516,9 +522,9 @@ MOE_EXPORT moe_status moe_expert_choice_forward(const moe_config* cfg,
     return MOE_ERR_INVALID_ARGUMENT;
   const EcLayout L = make_ec_layout(c);
   if (!ws || !al16(ws) || ws_bytes < L.total) return MOE_ERR_WORKSPACE;
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (mode == EntryMode::kValidate) return MOE_OK;
   int* flags = at<int>(ws, L.flags);
-  MOE_CUDA(cudaMemsetAsync(flags, 0, sizeof(int), st));
+  if (mode == EntryMode::kRun) MOE_CUDA(cudaMemsetAsync(flags, 0, sizeof(int), st));
   if ((s = zero_async(a->unrouted, sizeof(int32_t), st)) != MOE_OK) return s;
   if (c.T == 0) return MOE_OK;
   const int sms = sm_count();
@@ -570,6 +576,13 @@ MOE_EXPORT moe_status moe_expert_choice_forward(const moe_config* cfg,
   MOE_CUDA(launch_ec_combine(c.dtype, y_perm, rowmap, probs_et, c.T, c.E, C, c.d, a->y,
                              a->token_experts, a->unrouted, st));
   return MOE_OK;
+}
+
+MOE_EXPORT moe_status moe_expert_choice_forward(const moe_config* cfg,
+                                                const moe_expert_choice_args* a, void* ws,
+                                                size_t ws_bytes, moe_stream_t stream) {
+  return ec_forward_entry(cfg, a, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream),
+                          EntryMode::kRun);
 }
 
 // ---------------------------------------------------------------- backward

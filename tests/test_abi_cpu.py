@@ -270,3 +270,61 @@ def test_backward_pointer_and_workspace_checks(L):
     assert f(ctypes.byref(cfg), ctypes.byref(a), FAKE, need, None) == INV
     a = args()
     assert f(ctypes.byref(cfg), ctypes.byref(a), FAKE, need - 1, None) == WS
+
+
+# ---------------------------------------------------------------- host batches
+def test_host_batch_struct_layouts():
+    assert ctypes.sizeof(moe.MoeWeights) == 6 * 8
+    assert ctypes.sizeof(moe.MoeHostBatches) == 4 * 8
+    assert moe.MoeHostBatches.aux_loss.offset == 3 * 8
+
+
+@pytest.mark.parametrize("routing,cf", [("topk", 0.0), ("topk", 1.25), ("expert_choice", 2.0)])
+def test_host_workspace_holds_layer_and_two_slots(L, routing, cf):
+    for dt, s in (("bf16", 2), ("f32", 4)):
+        cfg = moe.config(300, 64, 128, 8, 2, dt, 0, cf)
+        fwd = (moe.moe_workspace_size(cfg) if routing == "topk"
+               else moe.moe_expert_choice_workspace_size(cfg))
+        need = moe.moe_forward_host_workspace_size(cfg, routing)
+        assert need >= fwd + 4 * 300 * 64 * s
+        assert need % 256 == 0
+
+
+def test_host_forward_validation_before_launch(L):
+    cfg = moe.config(64, 64, 128, 8, 2)
+    need = moe.moe_forward_host_workspace_size(cfg)
+    INV, WS, UNS = moe.MOE_ERR_INVALID_ARGUMENT, moe.MOE_ERR_WORKSPACE, moe.MOE_ERR_UNSUPPORTED
+    f = L.moe_forward_host
+    w = moe.MoeWeights(w_gate=FAKE, w1=FAKE, w2=FAKE)
+    ptrs = (ctypes.c_void_p * 2)(FAKE, FAKE)
+    pp = ctypes.cast(ptrs, ctypes.POINTER(ctypes.c_void_p))
+    b = moe.MoeHostBatches(2, pp, pp, None)
+    TOPK, EC = moe.MOE_ROUTING_TOPK, moe.MOE_ROUTING_EXPERT_CHOICE
+
+    def call(cfg=cfg, routing=TOPK, w=w, b=b, ws=FAKE, n=need):
+        return f(ctypes.byref(cfg), routing, ctypes.byref(w) if w is not None else None,
+                 ctypes.byref(b) if b is not None else None, ws, n, None)
+
+    assert call(routing=7) == INV
+    assert call(w=None) == INV
+    assert call(b=None) == INV
+    assert call(b=moe.MoeHostBatches(0, pp, pp, None)) == INV
+    assert call(b=moe.MoeHostBatches(2, None, pp, None)) == INV
+    nulls = (ctypes.c_void_p * 2)(FAKE, None)
+    np_ = ctypes.cast(nulls, ctypes.POINTER(ctypes.c_void_p))
+    assert call(b=moe.MoeHostBatches(2, pp, np_, None)) == INV
+    assert call(n=need - 1) == WS
+    assert call(ws=None) == WS
+    assert call(ws=FAKE_ODD) == WS
+    # the layer's own checks of the weights
+    assert call(w=moe.MoeWeights(w_gate=FAKE, w1=FAKE)) == INV
+    assert call(w=moe.MoeWeights(w_gate=FAKE, w1=FAKE, w2=FAKE_ODD)) == INV
+    noisy = moe.config(64, 64, 128, 8, 2, noise=moe.MOE_NOISE_GUMBEL)
+    assert call(cfg=noisy, n=moe.moe_forward_host_workspace_size(noisy)) == UNS
+    assert call(cfg=moe.config(64, 60, 128, 8, 2)) == UNS
+    ec = moe.config(64, 64, 128, 8, 2, capacity_factor=2.0)
+    need_ec = moe.moe_forward_host_workspace_size(ec, "expert_choice")
+    aux = (ctypes.c_float * 2)()
+    assert call(cfg=ec, routing=EC, n=need_ec,
+                b=moe.MoeHostBatches(2, pp, pp, ctypes.addressof(aux))) == INV
+    assert call(cfg=moe.config(64, 64, 128, 8, 2), routing=EC) == INV  # EC needs cf > 0

@@ -1,0 +1,57 @@
+"""The reference arm of bench.py (the CPU oracle) prints one well-formed JSON line."""
+
+import json
+import os
+import subprocess
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_reference_arm_json_line():
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    out = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload",
+                          "tiny_f32", "--steps", "3", "--warmup", "3"], cwd=ROOT, env=env,
+                         capture_output=True, text=True, timeout=300, check=True).stdout
+    lines = [ln for ln in out.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    r = json.loads(lines[0])
+    assert r["impl"] == "reference"
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "cpu_baseline", "e2e"):
+        assert key in r, key
+    assert r["steps"] == 3 and r["warmup"] == 3 and r["n_gpus"] == 1
+    assert r["value"] > 0 and r["higher_is_better"] is True
+    assert r["config"]["workload"] == "tiny_f32"
+    assert r["cpu_baseline"]["kind"] == "oracle" and r["cpu_baseline"]["value"] == r["value"]
+    assert r["e2e"]["value"] == r["value"] and r["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_bench_rejects_short_warmup():
+    p = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--warmup", "2"],
+                       cwd=ROOT, capture_output=True, text=True, timeout=300)
+    assert p.returncode != 0 and "warmup" in p.stderr
+
+
+def test_roofline_bound_and_fraction():
+    """The roofline object picks the bound from the algorithmic flops and bytes and
+    divides by the right peak."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from moe_workloads import WORKLOADS
+
+    peaks = dict(hbm_gbs=6500.0, bf16_tflops=1800.0, bf16_tflops_sustained=1400.0,
+                 source="test")
+    w = WORKLOADS["mixtral_prefill"]
+    M = w.T * w.k
+    flops, byts = bench.ffn_algorithmic(w, M, w.E)
+    assert flops == 4.0 * M * w.d * w.h
+    r = bench.roofline(w, M, w.E, 1e-3, peaks)
+    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s"
+    assert abs(r["achieved"] - flops / 1e-3 / 1e12) < 0.1
+    assert abs(r["frac"] - r["achieved"] / 1800.0) < 1e-4
+    d = WORKLOADS["decode"]
+    r = bench.roofline(d, d.T * d.k, 24, 1e-3, peaks)
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s" and r["peak"] == 6500.0
+    assert r["algorithmic_bytes"] >= 24 * 2 * d.d * d.h * 2
