@@ -348,7 +348,10 @@ moe_status moe_expert_choice_forward(const moe_config* cfg, const moe_expert_cho
    two streams the call creates (and releases before returning; CUDA frees them when
    their work completes), each batch's x and y double-buffered in the workspace, so
    batch i+1's host-to-device copy and batch i-1's device-to-host copy overlap batch
-   i's layer.  Ordering: all of it starts after the work already enqueued on
+   i's layer.  A single batch, or batches of less than 256 KiB of x, run copy in,
+   layer, copy out in order on `stream` alone (no streams created): there the copies
+   are latency-bound and the hand-offs between streams cost more than they hide.
+   Ordering: all of it starts after the work already enqueued on
    `stream`, and work enqueued on `stream` afterwards starts after all of it,
    including the last copy back; synchronise `stream` before reading y.
    Host buffers are the caller's and must stay valid (x unmodified) until then; they

@@ -1,8 +1,10 @@
 // Combine: y[t,:] = sum_{j kept} w[t,j] * y_perm[slot_row[t,j], :]
 // ("MoE mixture-of-experts routing mechanism": y = sum_{i<=K} G(x)_i E_i(x); the
 // MoELayer listing adds each slot's weighted expert output in slot order).
-// One thread per 16-byte output vector; the k slot contributions are added in slot
-// order in fp32 and rounded once.  No atomics.
+// Each 16-byte output vector is computed by one lane: the k slot contributions are
+// added in slot order in fp32 and rounded once.  No atomics.
+
+#include <algorithm>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -10,7 +12,6 @@
 namespace moe {
 namespace {
 
-constexpr int kThreads = 128;
 
 template <typename T>
 struct Vec;
@@ -47,43 +48,80 @@ struct Vec<__nv_bfloat16> {
   }
 };
 
-// Block (t, cb): token t, 16-byte column vectors cb*kThreads .. +kThreads-1; each
-// thread owns one vector.  The token's k slots are read once into shared memory.
+// One warp per token, grid-stride over tokens: lanes 0..k-1 read the token's slots,
+// the warp shares them by shuffles, then each lane walks the 16-byte column vectors
+// lane, lane+32, ... two at a time (2k loads in flight per lane).  No shared memory
+// or barrier, so a small d does not leave the SM waiting on block launches.
+constexpr int kCombineWarps = 8;
+
 template <typename T>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kCombineWarps * 32)
     combine_kernel(const T* __restrict__ y_perm, const int32_t* __restrict__ slot_row,
-                   const float* __restrict__ topk_w, int d, int k, int64_t rows,
+                   const float* __restrict__ topk_w, int64_t ntok, int d, int k, int64_t rows,
                    T* __restrict__ y, int* flags) {
   pdl_enter();
   constexpr int V = Vec<T>::N;
-  __shared__ int s_row[kMaxK];
-  __shared__ float s_w[kMaxK];
-  const int64_t t = blockIdx.x;
-  if (threadIdx.x < k) {
-    int q = slot_row[t * k + threadIdx.x];
-    if (q < -1 || q >= rows) {
-      if (blockIdx.y == 0) raise_flag(flags, MOE_DEVERR_BAD_ROW);
-      q = -1;
+  const int lane = threadIdx.x & 31;
+  const int nvec = d / V;
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kCombineWarps;
+  for (int64_t t = static_cast<int64_t>(blockIdx.x) * kCombineWarps + (threadIdx.x >> 5);
+       t < ntok; t += nwarps) {
+    int my_q = -1;
+    float my_w = 0.f;
+    if (lane < k) {
+      my_q = slot_row[t * k + lane];
+      if (my_q < -1 || my_q >= rows) {
+        raise_flag(flags, MOE_DEVERR_BAD_ROW);
+        my_q = -1;
+      }
+      my_w = topk_w[t * k + lane];
     }
-    s_row[threadIdx.x] = q;
-    s_w[threadIdx.x] = topk_w[t * k + threadIdx.x];
-  }
-  __syncthreads();
-  const int v = blockIdx.y * kThreads + threadIdx.x;
-  if (v >= d / V) return;
-  float acc[V];
+    int64_t src[kMaxK];
+    float wj[kMaxK];
 #pragma unroll
-  for (int i = 0; i < V; ++i) acc[i] = 0.f;
+    for (int j = 0; j < kMaxK; ++j) {
+      const int q = __shfl_sync(0xffffffffu, my_q, j);
+      wj[j] = __shfl_sync(0xffffffffu, my_w, j);
+      src[j] = (j < k && q >= 0) ? static_cast<int64_t>(q) * d : -1;
+    }
+    T* dst = y + t * d;
+    int v = lane;
+    for (; v + 32 < nvec; v += 64) {
+      float a0[V], a1[V];
 #pragma unroll
-  for (int j = 0; j < kMaxK; ++j) {
-    if (j < k && s_row[j] >= 0) {
-      float val[V];
-      Vec<T>::load(y_perm + static_cast<int64_t>(s_row[j]) * d + v * V, val);
+      for (int i = 0; i < V; ++i) a0[i] = a1[i] = 0.f;
 #pragma unroll
-      for (int i = 0; i < V; ++i) acc[i] = fmaf(s_w[j], val[i], acc[i]);
+      for (int j = 0; j < kMaxK; ++j) {
+        if (src[j] >= 0) {
+          float x0[V], x1[V];
+          Vec<T>::load(y_perm + src[j] + v * V, x0);
+          Vec<T>::load(y_perm + src[j] + (v + 32) * V, x1);
+#pragma unroll
+          for (int i = 0; i < V; ++i) {
+            a0[i] = fmaf(wj[j], x0[i], a0[i]);
+            a1[i] = fmaf(wj[j], x1[i], a1[i]);
+          }
+        }
+      }
+      Vec<T>::store(dst + v * V, a0);
+      Vec<T>::store(dst + (v + 32) * V, a1);
+    }
+    if (v < nvec) {
+      float a0[V];
+#pragma unroll
+      for (int i = 0; i < V; ++i) a0[i] = 0.f;
+#pragma unroll
+      for (int j = 0; j < kMaxK; ++j) {
+        if (src[j] >= 0) {
+          float x0[V];
+          Vec<T>::load(y_perm + src[j] + v * V, x0);
+#pragma unroll
+          for (int i = 0; i < V; ++i) a0[i] = fmaf(wj[j], x0[i], a0[i]);
+        }
+      }
+      Vec<T>::store(dst + v * V, a0);
     }
   }
-  Vec<T>::store(y + t * d + v * V, acc);
 }
 
 // Expert-choice combine ("Expert Choice routing and capacity-factor tuning" section
@@ -168,17 +206,21 @@ cudaError_t launch_combine(int dtype, const void* y_perm, const int32_t* slot_ro
                            const float* topk_w, int64_t T, int d, int k, void* y, int* flags,
                            cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
-  const int vec = dtype == MOE_F32 ? Vec<float>::N : Vec<__nv_bfloat16>::N;
-  const dim3 grid(static_cast<unsigned>(T), static_cast<unsigned>((d / vec + kThreads - 1) / kThreads));
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return cudaErrorUnknown;
+  const unsigned grid = static_cast<unsigned>(
+      std::min<int64_t>((T + kCombineWarps - 1) / kCombineWarps, static_cast<int64_t>(sms) * 8));
   const int64_t rows = T * k;
   if (dtype == MOE_F32)
-    launch_pdl(combine_kernel<float>, grid, kThreads, 0, stream, static_cast<const float*>(y_perm),
-                                                         slot_row, topk_w, d, k, rows,
-                                                         static_cast<float*>(y), flags);
+    launch_pdl(combine_kernel<float>, grid, kCombineWarps * 32, 0, stream,
+               static_cast<const float*>(y_perm), slot_row, topk_w, T, d, k, rows,
+               static_cast<float*>(y), flags);
   else
-    launch_pdl(combine_kernel<__nv_bfloat16>, grid, kThreads, 0, stream, 
-        static_cast<const __nv_bfloat16*>(y_perm), slot_row, topk_w, d, k, rows,
-        static_cast<__nv_bfloat16*>(y), flags);
+    launch_pdl(combine_kernel<__nv_bfloat16>, grid, kCombineWarps * 32, 0, stream,
+               static_cast<const __nv_bfloat16*>(y_perm), slot_row, topk_w, T, d, k, rows,
+               static_cast<__nv_bfloat16*>(y), flags);
   return cudaGetLastError();
 }
 

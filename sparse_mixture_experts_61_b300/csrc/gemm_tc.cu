@@ -449,10 +449,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           tmem_ld_16cols(t_row + col, v);
         tc_wait_ld();
         if (row < p.m_rows) {
+          const int e0 = c.n0 + col;
+          float* dst = out + row * p.N + e0;
+          if ((p.N & 3) == 0 && e0 + CH <= p.N) {
+            // Whole chunk in range and 16-byte aligned (N % 4 == 0, e0 % 16 == 0).
 #pragma unroll
-          for (int i = 0; i < CH; ++i) {
-            const int e = c.n0 + col + i;
-            if (e < p.N) out[row * p.N + e] = v[i];
+            for (int i = 0; i < CH; i += 4)
+              *reinterpret_cast<float4*>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+          } else {
+#pragma unroll
+            for (int i = 0; i < CH; ++i)
+              if (e0 + i < p.N) dst[i] = v[i];
           }
         }
       }

@@ -23,16 +23,36 @@
 namespace moe {
 namespace {
 
+__device__ __forceinline__ double warp_sum_d(double v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ double warp_max_d(double v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmax(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// s += v with the rounding error carried in c (Kahan); order-fixed, so deterministic.
+__device__ __forceinline__ void kahan_add(float& s, float& c, float v) {
+  const float y = v - c;
+  const float t = s + y;
+  c = (t - s) - y;
+  s = t;
+}
+
 constexpr int kRouteWarps = 32;
 constexpr int kTokensPerWarp = kChunk / kRouteWarps;
 
 // One CTA per chunk of kChunk tokens, one warp per token at a time.  Lane l holds
-// experts l, l+32, ... (EPL of them).
-template <int EPL>
+// experts l, l+32, ... (EPL of them); K = k, so the per-slot loops have exact trip
+// counts instead of kMaxK predicated iterations.
+template <int EPL, int K>
 __global__ void __launch_bounds__(kRouteWarps * 32)
     route_topk_kernel(const float* __restrict__ src, int nsplit, int64_t split_stride,
                       const float* __restrict__ bias, const float* __restrict__ noise,
-                      int noise_mode, float* __restrict__ logits_out, int64_t T, int E, int k,
+                      int noise_mode, float* __restrict__ logits_out, int64_t T, int E,
                       int gate, int32_t* __restrict__ topk_idx,
                       float* __restrict__ topk_w, int32_t* __restrict__ hist,
                       float* __restrict__ psum, int* flags) {
@@ -143,19 +163,18 @@ __global__ void __launch_bounds__(kRouteWarps * 32)
       s += ex[q];
     }
     s = warp_sum(s);
+    const float inv_s = 1.f / s;
 #pragma unroll
-    for (int q = 0; q < EPL; ++q) ps[q] += ex[q] / s;
+    for (int q = 0; q < EPL; ++q) ps[q] += ex[q] * inv_s;
 
     // top-k on the scores: k rounds of a warp arg-max under (value desc, index asc).
     // Each candidate carries its b value for the weights.
     uint32_t taken = 0;
-    int sel_e[kMaxK];
-    float sel_b[kMaxK];
+    int sel_e[K];
+    float sel_b[K];
 #pragma unroll
-    for (int j = 0; j < kMaxK; ++j) {
-      sel_e[j] = 0;
-      sel_b[j] = 0.f;
-      if (j < k) {
+    for (int j = 0; j < K; ++j) {
+      {
         float bv = -INFINITY, bb = 0.f;
         int be = E;  // sentinel: larger than any valid index
 #pragma unroll
@@ -188,31 +207,27 @@ __global__ void __launch_bounds__(kRouteWarps * 32)
     // gate weights of the kept experts
     float bmax = sel_b[0];
 #pragma unroll
-    for (int j = 1; j < kMaxK; ++j)
-      if (j < k) bmax = fmaxf(bmax, sel_b[j]);
-    float w[kMaxK];
+    for (int j = 1; j < K; ++j) bmax = fmaxf(bmax, sel_b[j]);
+    float w[K];
     float den = 0.f;
 #pragma unroll
-    for (int j = 0; j < kMaxK; ++j) {
-      w[j] = 0.f;
-      if (j < k) {
-        // mode 0: softmax over the kept logits, shifted by the largest kept one;
-        // mode 1: the full-softmax probability p_j = exp(b_j - m) / s.
-        w[j] = (gate == 0) ? expf(sel_b[j] - bmax) : expf(sel_b[j] - m) / s;
-        den += w[j];
-      }
+    for (int j = 0; j < K; ++j) {
+      // mode 0: softmax over the kept logits, shifted by the largest kept one;
+      // mode 1: the full-softmax probability p_j = exp(b_j - m) / s.
+      w[j] = (gate == 0) ? expf(sel_b[j] - bmax) : expf(sel_b[j] - m) / s;
+      den += w[j];
     }
     int my_e = 0;
     float my_w = 0.f;
 #pragma unroll
-    for (int j = 0; j < kMaxK; ++j)
+    for (int j = 0; j < K; ++j)
       if (j == lane) {
         my_e = sel_e[j];
         my_w = w[j] / den;
       }
-    if (lane < k) {
-      topk_idx[t * k + lane] = my_e;
-      topk_w[t * k + lane] = my_w;
+    if (lane < K) {
+      topk_idx[t * K + lane] = my_e;
+      topk_w[t * K + lane] = my_w;
       atomicAdd(&s_hist[my_e], 1);
     }
   }
@@ -243,12 +258,14 @@ __global__ void __launch_bounds__(kFinThreads)
                           int32_t* __restrict__ kept, int32_t* __restrict__ offsets,
                           int32_t* __restrict__ dropped, float* __restrict__ stats) {
   pdl_enter();
-  __shared__ double s_red[kMaxExperts];
-  __shared__ int s_scan[kMaxExperts];
+  __shared__ double s_red[kMaxExperts / 32];
+  __shared__ float s_loss[kMaxExperts / 32];
+  __shared__ int s_scan[kMaxExperts / 32];
   __shared__ int s_drop;
   __shared__ int s_cnt[kFinThreads];
-  __shared__ double s_ps[kFinThreads];
+  __shared__ float s_ps[kFinThreads];
   const int tid = threadIdx.x;
+  if (tid == 0) s_drop = 0;
   int EP = 32;
   while (EP < E) EP <<= 1;
   const int nslices = kFinThreads / EP;
@@ -258,7 +275,7 @@ __global__ void __launch_bounds__(kFinThreads)
     const int sl = tid / EP, ex = tid % EP;
     const int c_lo = sl * per, c_hi = min(nchunks, c_lo + per);
     int cnt = 0;
-    double ps = 0.0;
+    float ps = 0.f, pc = 0.f;  // compensated (Kahan) sum of the chunks' softmax sums
     if (ex < E) {
       // Eight chunks at a time: the loads are issued together, then added in order.
       constexpr int B = 8;
@@ -274,12 +291,12 @@ __global__ void __launch_bounds__(kFinThreads)
 #pragma unroll
         for (int i = 0; i < B; ++i) {
           cnt += hv[i];
-          ps += static_cast<double>(pv[i]);
+          kahan_add(ps, pc, pv[i]);
         }
       }
     }
     s_cnt[tid] = cnt;
-    s_ps[tid] = ps;
+    s_ps[tid] = ps - pc;
     __syncthreads();
     // Position bases: the counts of the lower slices, then this slice's chunks in order
     // (loads issued eight at a time).
@@ -300,81 +317,77 @@ __global__ void __launch_bounds__(kFinThreads)
       }
     }
   }
-  const int e = tid;
-  if (e == 0) s_drop = 0;
+  // From here thread e handles expert e; warps 0 .. kExpertWarps-1 cover every expert.
+  // Reductions over the experts are butterfly sums within each warp, then the warp
+  // partials added in warp order: a fixed order, one barrier each.
+  constexpr int kExpertWarps = kMaxExperts / 32;
+  const int e = tid, lane = tid & 31, warp = tid >> 5;
   int cnt = 0;
-  double ps = 0.0;
+  float ps = 0.f, pc = 0.f;
   if (e < E) {
     for (int q = 0; q < nslices; ++q) {
       cnt += s_cnt[q * EP + e];
-      ps += s_ps[q * EP + e];
+      kahan_add(ps, pc, s_ps[q * EP + e]);
     }
     if (counts) counts[e] = cnt;
   }
-  // balance loss: E * sum_e (psum_e / T) * (count_e / T), fixed-order tree sum
-  if (e < kMaxExperts)
-    s_red[e] = (e < E && T > 0) ? (ps / static_cast<double>(T)) *
-                                      (static_cast<double>(cnt) / static_cast<double>(T))
-                                : 0.0;
-  __syncthreads();
-  for (int o = kMaxExperts / 2; o > 0; o >>= 1) {
-    if (e < o) s_red[e] += s_red[e + o];
-    __syncthreads();
-  }
-  if (e == 0 && psum && aux) aux[0] = static_cast<float>(static_cast<double>(E) * s_red[0]);
+  // balance loss: E * sum_e (psum_e / T) * (count_e / T) = E * sum_e psum_e count_e / T^2.
+  // fp32 throughout (this GPU's FP64 rate is a small fraction of its FP32 rate):
+  // compensated sums over the chunks, one rounding per product, a 32-term butterfly.
+  const float lv = warp_sum((e < E) ? (ps - pc) * static_cast<float>(cnt) : 0.f);
+  if (lane == 0 && warp < kExpertWarps) s_loss[warp] = lv;
 
   // capacity, kept counts and the exclusive scan of the offsets
   int kp = 0;
   if (e < E) kp = (C < 0 || cnt < C) ? cnt : static_cast<int>(C);
   if (kept && e < E) kept[e] = kp;
   if (e < E && cnt > kp) atomicAdd(&s_drop, cnt - kp);
-  if (e < kMaxExperts) s_scan[e] = kp;
+  int incl = kp;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += n;
+  }
+  if (lane == 31 && warp < kExpertWarps) s_scan[warp] = incl;
   __syncthreads();
-  for (int o = 1; o < kMaxExperts; o <<= 1) {
-    const int add = (e >= o && e < kMaxExperts) ? s_scan[e - o] : 0;
-    __syncthreads();
-    if (e < kMaxExperts) s_scan[e] += add;
-    __syncthreads();
+  if (e == 0) {
+    if (psum && aux) {
+      double tot = 0.0;
+      for (int w = 0; w < kExpertWarps; ++w) tot += s_loss[w];
+      const double TT = static_cast<double>(T) * static_cast<double>(T);
+      aux[0] = T > 0 ? static_cast<float>(static_cast<double>(E) * tot / TT) : 0.f;
+    }
+    if (dropped) dropped[0] = s_drop;
   }
+  if (warp < kExpertWarps)
+    for (int w = 0; w < warp; ++w) incl += s_scan[w];
   if (offsets) {
-    if (e < E) offsets[e] = s_scan[e] - kp;
-    if (e == E - 1) offsets[E] = s_scan[e];
+    if (e < E) offsets[e] = incl - kp;
+    if (e == E - 1) offsets[E] = incl;
   }
-  if (e == 0 && dropped) dropped[0] = s_drop;
 
-  // Routing statistics of the pre-drop counts (every thread takes part: the block
-  // reductions synchronise).  load_e = count_e / total; sample standard deviations.
+  // Routing statistics of the pre-drop counts.  load_e = count_e / total; sample
+  // standard deviations.  Every thread takes part (the reductions synchronise).
   if (stats) {
-    auto block_sum = [&](double v) {
+    auto block_reduce = [&](double v, bool is_max) {
+      v = is_max ? warp_max_d(v) : warp_sum_d(v);
+      __syncthreads();  // earlier readers of s_red are done
+      if (lane == 0 && warp < kExpertWarps) s_red[warp] = v;
       __syncthreads();
-      if (e < kMaxExperts) s_red[e] = v;
-      __syncthreads();
-      for (int o = kMaxExperts / 2; o > 0; o >>= 1) {
-        if (e < o) s_red[e] += s_red[e + o];
-        __syncthreads();
-      }
-      return s_red[0];
-    };
-    auto block_max = [&](double v) {
-      __syncthreads();
-      if (e < kMaxExperts) s_red[e] = v;
-      __syncthreads();
-      for (int o = kMaxExperts / 2; o > 0; o >>= 1) {
-        if (e < o) s_red[e] = fmax(s_red[e], s_red[e + o]);
-        __syncthreads();
-      }
-      return s_red[0];
+      double r = s_red[0];
+      for (int w = 1; w < kExpertWarps; ++w) r = is_max ? fmax(r, s_red[w]) : r + s_red[w];
+      return r;
     };
     const bool own = e < E;
     const double c = own ? static_cast<double>(cnt) : 0.0;
-    const double total = block_sum(c);
+    const double total = block_reduce(c, false);
     const double load = (own && total > 0.0) ? c / total : 0.0;
-    const double lmean = block_sum(load) / E, cmean = total / E;
-    const double lvar = block_sum(own ? (load - lmean) * (load - lmean) : 0.0);
-    const double cvar = block_sum(own ? (c - cmean) * (c - cmean) : 0.0);
-    const double lmax = block_max(own ? load : 0.0);
-    const double dead = block_sum((own && load < 1e-4) ? 1.0 : 0.0);
-    const double ent = block_sum(own ? -load * log(load + 1e-10) : 0.0);
+    const double lmean = block_reduce(load, false) / E, cmean = total / E;
+    const double lvar = block_reduce(own ? (load - lmean) * (load - lmean) : 0.0, false);
+    const double cvar = block_reduce(own ? (c - cmean) * (c - cmean) : 0.0, false);
+    const double lmax = block_reduce(own ? load : 0.0, true);
+    const double dead = block_reduce((own && load < 1e-4) ? 1.0 : 0.0, false);
+    const double ent = block_reduce(own ? -load * log(load + 1e-10) : 0.0, false);
     if (e == 0) {
       if (total > 0.0) {
         const double lstd = E > 1 ? sqrt(lvar / (E - 1)) : 0.0;
@@ -392,6 +405,21 @@ __global__ void __launch_bounds__(kFinThreads)
   }
 }
 
+// route_topk_kernel<EPL, k> for the runtime k (1..kMaxK).
+template <int EPL, typename... Args>
+void launch_topk_k(int k, dim3 grid, dim3 block, cudaStream_t stream, Args... args) {
+  switch (k) {
+    case 1: launch_pdl(route_topk_kernel<EPL, 1>, grid, block, 0, stream, args...); break;
+    case 2: launch_pdl(route_topk_kernel<EPL, 2>, grid, block, 0, stream, args...); break;
+    case 3: launch_pdl(route_topk_kernel<EPL, 3>, grid, block, 0, stream, args...); break;
+    case 4: launch_pdl(route_topk_kernel<EPL, 4>, grid, block, 0, stream, args...); break;
+    case 5: launch_pdl(route_topk_kernel<EPL, 5>, grid, block, 0, stream, args...); break;
+    case 6: launch_pdl(route_topk_kernel<EPL, 6>, grid, block, 0, stream, args...); break;
+    case 7: launch_pdl(route_topk_kernel<EPL, 7>, grid, block, 0, stream, args...); break;
+    default: launch_pdl(route_topk_kernel<EPL, 8>, grid, block, 0, stream, args...); break;
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_route_topk(const float* src, int nsplit, int64_t split_stride,
@@ -402,19 +430,19 @@ cudaError_t launch_route_topk(const float* src, int nsplit, int64_t split_stride
   const int64_t nchunks = (T + kChunk - 1) / kChunk;
   if (nchunks == 0) return cudaSuccess;
   const dim3 grid(static_cast<unsigned>(nchunks)), block(kRouteWarps * 32);
-#define MOE_TOPK_LAUNCH(EPL)                                                                   \
-  launch_pdl(route_topk_kernel<EPL>, grid, block, 0, stream, src, nsplit, split_stride, bias, noise,   \
-                                                     noise_mode, logits_out, T, E, k, gate,    \
-                                                     topk_idx, topk_w, hist, psum, flags)
+  if (k < 1 || k > kMaxK) return cudaErrorInvalidValue;
   if (E <= 32)
-    MOE_TOPK_LAUNCH(1);
+    launch_topk_k<1>(k, grid, block, stream, src, nsplit, split_stride, bias, noise, noise_mode,
+                     logits_out, T, E, gate, topk_idx, topk_w, hist, psum, flags);
   else if (E <= 64)
-    MOE_TOPK_LAUNCH(2);
+    launch_topk_k<2>(k, grid, block, stream, src, nsplit, split_stride, bias, noise, noise_mode,
+                     logits_out, T, E, gate, topk_idx, topk_w, hist, psum, flags);
   else if (E <= 128)
-    MOE_TOPK_LAUNCH(4);
+    launch_topk_k<4>(k, grid, block, stream, src, nsplit, split_stride, bias, noise, noise_mode,
+                     logits_out, T, E, gate, topk_idx, topk_w, hist, psum, flags);
   else
-    MOE_TOPK_LAUNCH(8);
-#undef MOE_TOPK_LAUNCH
+    launch_topk_k<8>(k, grid, block, stream, src, nsplit, split_stride, bias, noise, noise_mode,
+                     logits_out, T, E, gate, topk_idx, topk_w, hist, psum, flags);
   return cudaGetLastError();
 }
 

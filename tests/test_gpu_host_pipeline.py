@@ -4,7 +4,10 @@ Every batch's y must be bitwise the y of moe_forward (or moe_expert_choice_forwa
 on the same x through the same workspace layout, and one batch is checked against
 the oracle as well.  Covers both routings, bf16 and fp32, page-locked and pageable
 host buffers, a single batch, more batches than the two device slots, empty batches
-and device flags raised by an early batch surviving the later ones.
+and device flags raised by an early batch surviving the later ones; and both ways
+the call runs batches: overlapped on three streams (the 777 x 512 and 2048 x 256
+bf16 cases, at least 256 KiB of x per batch) and in order on one stream (one batch,
+or the 256 x 128 fp32 and 64 x 64 cases).
 """
 
 import numpy as np
