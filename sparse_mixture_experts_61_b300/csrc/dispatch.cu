@@ -13,8 +13,9 @@
 // give each chunk's first position per expert, and inside a chunk the position
 // of an assignment is that base plus the number of earlier assignments of the
 // chunk (in token-then-slot order) with the same expert.  The row copy into the
-// expert-contiguous buffer is a separate grid-stride kernel over all kept rows, so
-// that it uses the whole GPU whatever the number of chunks.
+// expert-contiguous buffer is a separate grid-stride kernel (over the tokens for
+// top-k routing, over the rows for expert choice), so that it uses the whole GPU
+// whatever the number of chunks.
 
 #include <algorithm>
 
@@ -113,6 +114,46 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
+// Row scatter Xp[slot_row[t, j], :] = x[t, :] for every kept slot: one warp per token,
+// grid-stride over tokens.  Each token row is read once and written to each of its
+// kept rows (the gather above reads a row once per slot: k times the reads when the
+// rows do not stay in L2).  Every row below M is some kept slot's, so all are written.
+__global__ void __launch_bounds__(kThreads)
+    scatter_rows_kernel(const int32_t* __restrict__ slot_row, int64_t T, int k,
+                        const uint4* __restrict__ x, uint4* __restrict__ x_perm, int nvec) {
+  pdl_enter();
+  const int lane = threadIdx.x & 31;
+  const int64_t wpb = kThreads / 32;
+  for (int64_t t = static_cast<int64_t>(blockIdx.x) * wpb + (threadIdx.x >> 5); t < T;
+       t += static_cast<int64_t>(gridDim.x) * wpb) {
+    const int my_row = lane < k ? slot_row[t * k + lane] : -1;
+    int64_t dst[kMaxK];
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j) {
+      const int r = __shfl_sync(0xffffffffu, my_row, j);
+      dst[j] = (j < k && r >= 0) ? static_cast<int64_t>(r) * nvec : -1;
+    }
+    const uint4* src = x + t * nvec;
+    for (int v0 = 0; v0 < nvec; v0 += 128) {
+      uint4 q[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int v = v0 + lane + 32 * i;
+        if (v < nvec) q[i] = __ldg(src + v);
+      }
+#pragma unroll
+      for (int j = 0; j < kMaxK; ++j) {
+        if (dst[j] < 0) continue;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int v = v0 + lane + 32 * i;
+          if (v < nvec) x_perm[dst[j] + v] = q[i];
+        }
+      }
+    }
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_dispatch_hist(const int32_t* topk_idx, int64_t T, int E, int k, int32_t* hist,
@@ -134,7 +175,13 @@ cudaError_t launch_dispatch_place(int dtype, const int32_t* topk_idx, int64_t T,
       topk_idx, T, E, k, C, chunk_base, offsets, slot_row, row_token, flags);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  return launch_gather_rows(dtype, row_token, offsets, E, x, x_perm, d, T * k, stream);
+  // Xp by scatter from the tokens (each x row read once).
+  const int nvec = d * (dtype == MOE_F32 ? 4 : 2) / 16;
+  const unsigned grid = static_cast<unsigned>(
+      std::min<int64_t>((T + kThreads / 32 - 1) / (kThreads / 32), 4096));
+  launch_pdl(scatter_rows_kernel, grid, kThreads, 0, stream, slot_row, T, k,
+             static_cast<const uint4*>(x), static_cast<uint4*>(x_perm), nvec);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_gather_rows(int dtype, const int32_t* row_token, const int32_t* offsets, int E,
