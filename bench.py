@@ -60,12 +60,12 @@ D_AUX = 0.01
 # profiles/traffic_expert_gemms_bf16_workloads.md.  Only workloads whose current kernels
 # were captured appear here; others report null.
 NCU_TRAFFIC_BYTES = {
-    "mixtral_prefill": 2723900672,
-    "deepseek_fine": 17651939072,
-    "mixtral_prefill_ec": 2653917952,
-    "deepseek_fine_ec": 17547154944,
-    "decode": 4480856832,
-    "switch_capacity": 156232192,
+    "mixtral_prefill": 2723980800,
+    "deepseek_fine": 17652525568,
+    "mixtral_prefill_ec": 2653969920,
+    "deepseek_fine_ec": 17529011456,
+    "decode": 4480745984,
+    "switch_capacity": 156264960,
 }
 
 
