@@ -531,9 +531,9 @@ cudaError_t launch_router(const GemmArgs& a, int sm_count, cudaStream_t stream) 
 // holds the largest group the routing can produce.
 template <int EPI>
 cudaError_t launch_ffn_for(const GemmArgs& a, int max_group, int sm_count, cudaStream_t stream) {
-  if (max_group <= 32) return launch_ffn<32, 8, EPI>(a, sm_count, stream);
-  if (max_group <= 64) return launch_ffn<64, 8, EPI>(a, sm_count, stream);
-  if (max_group <= 128) return launch_ffn<128, 6, EPI>(a, sm_count, stream);
+  if (max_group <= 32) return launch_ffn<32, 11, EPI>(a, sm_count, stream);
+  if (max_group <= 64) return launch_ffn<64, 9, EPI>(a, sm_count, stream);
+  if (max_group <= 128) return launch_ffn<128, 7, EPI>(a, sm_count, stream);
   return launch_ffn<256, 4, EPI>(a, sm_count, stream);
 }
 
