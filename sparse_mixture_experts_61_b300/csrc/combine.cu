@@ -48,30 +48,37 @@ struct Vec<__nv_bfloat16> {
   }
 };
 
-// One warp per token, grid-stride over tokens: lanes 0..k-1 read the token's slots,
-// the warp shares them by shuffles, then each lane walks the 16-byte column vectors
-// lane, lane+32, ... two at a time (2k loads in flight per lane).  No shared memory
-// or barrier, so a small d does not leave the SM waiting on block launches.
+// Work unit = (token, `uv` consecutive 16-byte column vectors); one warp per unit,
+// grid-stride.  Lanes 0..k-1 read the token's slots, the warp shares them by shuffles,
+// then each lane walks the unit's vectors two at a time, issuing all 2k loads before
+// adding.  A unit is the whole row when there are enough tokens to fill the GPU
+// (cutting rows up then only repeats the slot reads: measured slower on the prefill
+// layers), and a slice of it when there are few (decode), so every SM has work.  No
+// shared memory or barrier.
 constexpr int kCombineWarps = 8;
 
 template <typename T>
 __global__ void __launch_bounds__(kCombineWarps * 32)
     combine_kernel(const T* __restrict__ y_perm, const int32_t* __restrict__ slot_row,
                    const float* __restrict__ topk_w, int64_t ntok, int d, int k, int64_t rows,
-                   T* __restrict__ y, int* flags) {
+                   int uv, T* __restrict__ y, int* flags) {
   pdl_enter();
   constexpr int V = Vec<T>::N;
   const int lane = threadIdx.x & 31;
   const int nvec = d / V;
+  const int chunks = (nvec + uv - 1) / uv;
+  const int64_t units = ntok * chunks;
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kCombineWarps;
-  for (int64_t t = static_cast<int64_t>(blockIdx.x) * kCombineWarps + (threadIdx.x >> 5);
-       t < ntok; t += nwarps) {
+  for (int64_t u = static_cast<int64_t>(blockIdx.x) * kCombineWarps + (threadIdx.x >> 5);
+       u < units; u += nwarps) {
+    const int64_t t = chunks == 1 ? u : u / chunks;
+    const int c = static_cast<int>(u - t * chunks);
     int my_q = -1;
     float my_w = 0.f;
     if (lane < k) {
       my_q = slot_row[t * k + lane];
       if (my_q < -1 || my_q >= rows) {
-        raise_flag(flags, MOE_DEVERR_BAD_ROW);
+        if (c == 0) raise_flag(flags, MOE_DEVERR_BAD_ROW);
         my_q = -1;
       }
       my_w = topk_w[t * k + lane];
@@ -85,8 +92,9 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
       src[j] = (j < k && q >= 0) ? static_cast<int64_t>(q) * d : -1;
     }
     T* dst = y + t * d;
-    int v = lane;
-    for (; v + 32 < nvec; v += 64) {
+    const int vend = min(nvec, (c + 1) * uv);
+    int v = c * uv + lane;
+    for (; v + 32 < vend; v += 64) {
       float a0[V], a1[V];
 #pragma unroll
       for (int i = 0; i < V; ++i) a0[i] = a1[i] = 0.f;
@@ -106,7 +114,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
       Vec<T>::store(dst + v * V, a0);
       Vec<T>::store(dst + (v + 32) * V, a1);
     }
-    if (v < nvec) {
+    if (v < vend) {
       float a0[V];
 #pragma unroll
       for (int i = 0; i < V; ++i) a0[i] = 0.f;
@@ -210,16 +218,24 @@ cudaError_t launch_combine(int dtype, const void* y_perm, const int32_t* slot_ro
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return cudaErrorUnknown;
-  const unsigned grid = static_cast<unsigned>(
-      std::min<int64_t>((T + kCombineWarps - 1) / kCombineWarps, static_cast<int64_t>(sms) * 8));
+  // Vectors per unit: whole rows when T alone gives every SM 16 warps, else rows cut
+  // into slices (multiples of 64 vectors) until it does.
+  const int vec = dtype == MOE_F32 ? Vec<float>::N : Vec<__nv_bfloat16>::N;
+  const int nvec = d / vec;
+  const int64_t want = static_cast<int64_t>(sms) * 16;
+  const int split = static_cast<int>(std::min<int64_t>((want + T - 1) / T, (nvec + 63) / 64));
+  const int uv = ((nvec + split - 1) / split + 63) / 64 * 64;
+  const int64_t units = T * ((nvec + uv - 1) / uv);
+  const unsigned grid = static_cast<unsigned>(std::min<int64_t>(
+      (units + kCombineWarps - 1) / kCombineWarps, static_cast<int64_t>(sms) * 8));
   const int64_t rows = T * k;
   if (dtype == MOE_F32)
     launch_pdl(combine_kernel<float>, grid, kCombineWarps * 32, 0, stream,
-               static_cast<const float*>(y_perm), slot_row, topk_w, T, d, k, rows,
+               static_cast<const float*>(y_perm), slot_row, topk_w, T, d, k, rows, uv,
                static_cast<float*>(y), flags);
   else
     launch_pdl(combine_kernel<__nv_bfloat16>, grid, kCombineWarps * 32, 0, stream,
-               static_cast<const __nv_bfloat16*>(y_perm), slot_row, topk_w, T, d, k, rows,
+               static_cast<const __nv_bfloat16*>(y_perm), slot_row, topk_w, T, d, k, rows, uv,
                static_cast<__nv_bfloat16*>(y), flags);
   return cudaGetLastError();
 }

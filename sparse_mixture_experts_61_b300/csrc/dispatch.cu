@@ -114,18 +114,25 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
-// Row scatter Xp[slot_row[t, j], :] = x[t, :] for every kept slot: one warp per token,
-// grid-stride over tokens.  Each token row is read once and written to each of its
-// kept rows (the gather above reads a row once per slot: k times the reads when the
-// rows do not stay in L2).  Every row below M is some kept slot's, so all are written.
+// Row scatter Xp[slot_row[t, j], :] = x[t, :] for every kept slot.  Work unit =
+// (token, 128 consecutive 16-byte vectors), one warp per unit, grid-stride: each lane
+// loads its 4 vectors once and stores them to each of the token's kept rows (the
+// gather above reads a row once per slot: k times the reads when the rows do not
+// stay in L2).  Every row below M is some kept slot's, so all are written.
+constexpr int kScatterVecs = 128;
+
 __global__ void __launch_bounds__(kThreads)
     scatter_rows_kernel(const int32_t* __restrict__ slot_row, int64_t T, int k,
                         const uint4* __restrict__ x, uint4* __restrict__ x_perm, int nvec) {
   pdl_enter();
   const int lane = threadIdx.x & 31;
   const int64_t wpb = kThreads / 32;
-  for (int64_t t = static_cast<int64_t>(blockIdx.x) * wpb + (threadIdx.x >> 5); t < T;
-       t += static_cast<int64_t>(gridDim.x) * wpb) {
+  const int chunks = (nvec + kScatterVecs - 1) / kScatterVecs;
+  const int64_t units = T * chunks;
+  for (int64_t u = static_cast<int64_t>(blockIdx.x) * wpb + (threadIdx.x >> 5); u < units;
+       u += static_cast<int64_t>(gridDim.x) * wpb) {
+    const int64_t t = chunks == 1 ? u : u / chunks;
+    const int v0 = static_cast<int>(u - t * chunks) * kScatterVecs;
     const int my_row = lane < k ? slot_row[t * k + lane] : -1;
     int64_t dst[kMaxK];
 #pragma unroll
@@ -134,21 +141,19 @@ __global__ void __launch_bounds__(kThreads)
       dst[j] = (j < k && r >= 0) ? static_cast<int64_t>(r) * nvec : -1;
     }
     const uint4* src = x + t * nvec;
-    for (int v0 = 0; v0 < nvec; v0 += 128) {
-      uint4 q[4];
+    uint4 q[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int v = v0 + lane + 32 * i;
+      if (v < nvec) q[i] = __ldg(src + v);
+    }
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j) {
+      if (dst[j] < 0) continue;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int v = v0 + lane + 32 * i;
-        if (v < nvec) q[i] = __ldg(src + v);
-      }
-#pragma unroll
-      for (int j = 0; j < kMaxK; ++j) {
-        if (dst[j] < 0) continue;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int v = v0 + lane + 32 * i;
-          if (v < nvec) x_perm[dst[j] + v] = q[i];
-        }
+        if (v < nvec) x_perm[dst[j] + v] = q[i];
       }
     }
   }
@@ -177,8 +182,9 @@ cudaError_t launch_dispatch_place(int dtype, const int32_t* topk_idx, int64_t T,
   if (e != cudaSuccess) return e;
   // Xp by scatter from the tokens (each x row read once).
   const int nvec = d * (dtype == MOE_F32 ? 4 : 2) / 16;
+  const int64_t units = T * ((nvec + kScatterVecs - 1) / kScatterVecs);
   const unsigned grid = static_cast<unsigned>(
-      std::min<int64_t>((T + kThreads / 32 - 1) / (kThreads / 32), 4096));
+      std::min<int64_t>((units + kThreads / 32 - 1) / (kThreads / 32), 4096));
   launch_pdl(scatter_rows_kernel, grid, kThreads, 0, stream, slot_row, T, k,
              static_cast<const uint4*>(x), static_cast<uint4*>(x_perm), nvec);
   return cudaGetLastError();

@@ -78,10 +78,17 @@ __global__ void __launch_bounds__(kRouteWarps * 32)
       const int e = lane + 32 * q;
       v[q] = -INFINITY;
       if (e < E) {
-        // Splits added in order; their loads are issued four at a time.
+        // Splits added in order; their loads are issued eight or four at a time.
         const float* p0 = src + t * E + e;
         float l = p0[0];
         int sp = 1;
+        for (; sp + 7 < nsplit; sp += 8) {
+          float q[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) q[i] = p0[(sp + i) * split_stride];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) l += q[i];
+        }
         for (; sp + 3 < nsplit; sp += 4) {
           const float a = p0[sp * split_stride], b = p0[(sp + 1) * split_stride],
                       c = p0[(sp + 2) * split_stride], d = p0[(sp + 3) * split_stride];
