@@ -64,8 +64,8 @@ NCU_TRAFFIC_BYTES = {
     "deepseek_fine": 17652525568,
     "mixtral_prefill_ec": 2653969920,
     "deepseek_fine_ec": 17529011456,
-    "decode": 4480745984,
-    "switch_capacity": 156264960,
+    "decode": 4481113856,
+    "switch_capacity": 156258816,
 }
 
 

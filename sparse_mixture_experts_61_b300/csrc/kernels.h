@@ -32,7 +32,8 @@ cudaError_t launch_route_finalize(const int32_t* hist, const float* psum, int nc
 cudaError_t launch_dispatch_hist(const int32_t* topk_idx, int64_t T, int E, int k, int32_t* hist,
                                  int* flags, cudaStream_t stream);
 
-// D2 + D3: stable positions, capacity drop, slot_row / row_token and the row gather.
+// D2 + D3: stable positions, capacity drop, slot_row / row_token and the expert-ordered
+// rows (copied token by token to each kept row).
 cudaError_t launch_dispatch_place(int dtype, const int32_t* topk_idx, int64_t T, int E, int k,
                                   int64_t C, const int32_t* chunk_base, const int32_t* offsets,
                                   int32_t* slot_row, int32_t* row_token, const void* x,
