@@ -68,174 +68,198 @@ __global__ void __launch_bounds__(kRouteWarps * 32)
   for (int q = 0; q < EPL; ++q) ps[q] = 0.f;
 
   const int64_t t_first = static_cast<int64_t>(blockIdx.x) * kChunk + warp * kTokensPerWarp;
-  for (int i = 0; i < kTokensPerWarp; ++i) {
-    const int64_t t = t_first + i;
-    if (t >= T) break;  // warp-uniform
-    // v: the router logits (split partials added in order, then the bias).
-    float v[EPL];
+  // The router logits (split partials added in split order, then the bias) of TP
+  // tokens at a time, loaded before any of them is processed so that their loads are
+  // in flight together; U splits' loads are issued at a time.  TP * EPL * (U + 1)
+  // values stay within the 64 registers a thread of this 1024-thread CTA has.
+  constexpr int TP = EPL >= 8 ? 1 : kTokensPerWarp;
+  constexpr int U = EPL >= 4 ? 2 : 4;
+  for (int i0 = 0; i0 < kTokensPerWarp; i0 += TP) {
+    float vv[TP][EPL];
 #pragma unroll
-    for (int q = 0; q < EPL; ++q) {
-      const int e = lane + 32 * q;
-      v[q] = -INFINITY;
-      if (e < E) {
-        // Splits added in order; their loads are issued eight or four at a time.
-        const float* p0 = src + t * E + e;
-        float l = p0[0];
-        int sp = 1;
-        for (; sp + 7 < nsplit; sp += 8) {
-          float q[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) q[i] = p0[(sp + i) * split_stride];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) l += q[i];
-        }
-        for (; sp + 3 < nsplit; sp += 4) {
-          const float a = p0[sp * split_stride], b = p0[(sp + 1) * split_stride],
-                      c = p0[(sp + 2) * split_stride], d = p0[(sp + 3) * split_stride];
-          l += a;
-          l += b;
-          l += c;
-          l += d;
-        }
-        for (; sp < nsplit; ++sp) l += p0[sp * split_stride];
-        if (bias) l += bias[e];
-        v[q] = l;
-      }
-    }
-    // sc: the selection scores (the logits themselves without noise).
-    float sc[EPL];
-    if (noise_mode == MOE_NOISE_PROB_GAUSS || noise_mode == MOE_NOISE_LOGIT_SOFTMAX) {
-      float mc = -INFINITY;
-#pragma unroll
-      for (int q = 0; q < EPL; ++q)
-        if (lane + 32 * q < E) mc = fmaxf(mc, v[q]);
-      mc = warp_max(mc);
-      float sc_sum = 0.f;
+    for (int i = 0; i < TP; ++i)
 #pragma unroll
       for (int q = 0; q < EPL; ++q) {
-        sc[q] = (lane + 32 * q < E) ? expf(v[q] - mc) : 0.f;
-        sc_sum += sc[q];
+        const int64_t t = t_first + i0 + i;
+        const int e = lane + 32 * q;
+        vv[i][q] = (t < T && e < E) ? src[t * E + e] : -INFINITY;
       }
-      sc_sum = warp_sum(sc_sum);
+    int sp = 1;
+    for (; sp + U - 1 < nsplit; sp += U) {
+      float part[U][TP][EPL];
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+#pragma unroll
+        for (int i = 0; i < TP; ++i)
+#pragma unroll
+          for (int q = 0; q < EPL; ++q) {
+            const int64_t t = t_first + i0 + i;
+            const int e = lane + 32 * q;
+            part[u][i][q] = (t < T && e < E) ? src[(sp + u) * split_stride + t * E + e] : 0.f;
+          }
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+#pragma unroll
+        for (int i = 0; i < TP; ++i)
+#pragma unroll
+          for (int q = 0; q < EPL; ++q) vv[i][q] += part[u][i][q];
+    }
+    for (; sp < nsplit; ++sp)
+#pragma unroll
+      for (int i = 0; i < TP; ++i)
+#pragma unroll
+        for (int q = 0; q < EPL; ++q) {
+          const int64_t t = t_first + i0 + i;
+          const int e = lane + 32 * q;
+          if (t < T && e < E) vv[i][q] += src[sp * split_stride + t * E + e];
+        }
+
+#pragma unroll
+    for (int i = 0; i < TP; ++i) {
+      const int64_t t = t_first + i0 + i;
+      if (t >= T) break;  // warp-uniform
+      float v[EPL];
+#pragma unroll
+      for (int q = 0; q < EPL; ++q) {
+        const int e = lane + 32 * q;
+        v[q] = vv[i][q];
+        if (e < E && bias) v[q] += bias[e];
+      }
+      // sc: the selection scores (the logits themselves without noise).
+      float sc[EPL];
+      if (noise_mode == MOE_NOISE_PROB_GAUSS || noise_mode == MOE_NOISE_LOGIT_SOFTMAX) {
+        float mc = -INFINITY;
+#pragma unroll
+        for (int q = 0; q < EPL; ++q)
+          if (lane + 32 * q < E) mc = fmaxf(mc, v[q]);
+        mc = warp_max(mc);
+        float sc_sum = 0.f;
+#pragma unroll
+        for (int q = 0; q < EPL; ++q) {
+          sc[q] = (lane + 32 * q < E) ? expf(v[q] - mc) : 0.f;
+          sc_sum += sc[q];
+        }
+        sc_sum = warp_sum(sc_sum);
+#pragma unroll
+        for (int q = 0; q < EPL; ++q) {
+          const int e = lane + 32 * q;
+          if (e < E) {
+            const float pc = sc[q] / sc_sum;
+            const float n = noise[t * E + e];
+            sc[q] = (noise_mode == MOE_NOISE_PROB_GAUSS) ? pc + n : v[q] + n * pc;
+          } else {
+            sc[q] = -INFINITY;
+          }
+        }
+      } else {
+#pragma unroll
+        for (int q = 0; q < EPL; ++q) {
+          const int e = lane + 32 * q;
+          sc[q] = v[q];
+          if (noise_mode == MOE_NOISE_GUMBEL && e < E) {
+            // g = -log(-log(u + 1e-9) + 1e-9).  For u > 1/2, u - 1 is exact and
+            // log1p keeps -log(u + 1e-9) accurate where it is tiny (u near 1).
+            const float u = noise[t * E + e];
+            const float a = (u > 0.5f) ? -log1pf((u - 1.0f) + 1e-9f) : -logf(u + 1e-9f);
+            sc[q] = v[q] - logf(a + 1e-9f);
+          }
+        }
+      }
+      bool bad = false;
 #pragma unroll
       for (int q = 0; q < EPL; ++q) {
         const int e = lane + 32 * q;
         if (e < E) {
-          const float pc = sc[q] / sc_sum;
-          const float n = noise[t * E + e];
-          sc[q] = (noise_mode == MOE_NOISE_PROB_GAUSS) ? pc + n : v[q] + n * pc;
-        } else {
-          sc[q] = -INFINITY;
+          if (logits_out) logits_out[t * E + e] = sc[q];
+          if (!isfinite(sc[q])) bad = true;
         }
       }
-    } else {
+      if (__any_sync(0xffffffffu, bad) && lane == 0) raise_flag(flags, MOE_DEVERR_NONFINITE);
+      // b: the logits the gate weights and f use -- the clean ones when the noise was
+      // added to the probabilities, the scores otherwise.
+      const bool clean_base = noise_mode == MOE_NOISE_PROB_GAUSS;
+
+      // softmax of b: m = max, s = sum exp(b - m)
+      float m = -INFINITY;
+#pragma unroll
+      for (int q = 0; q < EPL; ++q)
+        if (lane + 32 * q < E) m = fmaxf(m, clean_base ? v[q] : sc[q]);
+      m = warp_max(m);
+      float ex[EPL];
+      float s = 0.f;
 #pragma unroll
       for (int q = 0; q < EPL; ++q) {
-        const int e = lane + 32 * q;
-        sc[q] = v[q];
-        if (noise_mode == MOE_NOISE_GUMBEL && e < E) {
-          // g = -log(-log(u + 1e-9) + 1e-9).  For u > 1/2, u - 1 is exact and
-          // log1p keeps -log(u + 1e-9) accurate where it is tiny (u near 1).
-          const float u = noise[t * E + e];
-          const float a = (u > 0.5f) ? -log1pf((u - 1.0f) + 1e-9f) : -logf(u + 1e-9f);
-          sc[q] = v[q] - logf(a + 1e-9f);
-        }
+        ex[q] = (lane + 32 * q < E) ? expf((clean_base ? v[q] : sc[q]) - m) : 0.f;
+        s += ex[q];
       }
-    }
-    bool bad = false;
+      s = warp_sum(s);
+      const float inv_s = 1.f / s;
 #pragma unroll
-    for (int q = 0; q < EPL; ++q) {
-      const int e = lane + 32 * q;
-      if (e < E) {
-        if (logits_out) logits_out[t * E + e] = sc[q];
-        if (!isfinite(sc[q])) bad = true;
-      }
-    }
-    if (__any_sync(0xffffffffu, bad) && lane == 0) raise_flag(flags, MOE_DEVERR_NONFINITE);
-    // b: the logits the gate weights and f use -- the clean ones when the noise was
-    // added to the probabilities, the scores otherwise.
-    const bool clean_base = noise_mode == MOE_NOISE_PROB_GAUSS;
+      for (int q = 0; q < EPL; ++q) ps[q] += ex[q] * inv_s;
 
-    // softmax of b: m = max, s = sum exp(b - m)
-    float m = -INFINITY;
+      // top-k on the scores: k rounds of a warp arg-max under (value desc, index asc).
+      // Each candidate carries its b value for the weights.
+      uint32_t taken = 0;
+      int sel_e[K];
+      float sel_b[K];
 #pragma unroll
-    for (int q = 0; q < EPL; ++q)
-      if (lane + 32 * q < E) m = fmaxf(m, clean_base ? v[q] : sc[q]);
-    m = warp_max(m);
-    float ex[EPL];
-    float s = 0.f;
+      for (int j = 0; j < K; ++j) {
+        {
+          float bv = -INFINITY, bb = 0.f;
+          int be = E;  // sentinel: larger than any valid index
 #pragma unroll
-    for (int q = 0; q < EPL; ++q) {
-      ex[q] = (lane + 32 * q < E) ? expf((clean_base ? v[q] : sc[q]) - m) : 0.f;
-      s += ex[q];
-    }
-    s = warp_sum(s);
-    const float inv_s = 1.f / s;
-#pragma unroll
-    for (int q = 0; q < EPL; ++q) ps[q] += ex[q] * inv_s;
-
-    // top-k on the scores: k rounds of a warp arg-max under (value desc, index asc).
-    // Each candidate carries its b value for the weights.
-    uint32_t taken = 0;
-    int sel_e[K];
-    float sel_b[K];
-#pragma unroll
-    for (int j = 0; j < K; ++j) {
-      {
-        float bv = -INFINITY, bb = 0.f;
-        int be = E;  // sentinel: larger than any valid index
-#pragma unroll
-        for (int q = 0; q < EPL; ++q) {
-          const int e = lane + 32 * q;
-          if (e < E && !((taken >> q) & 1u) && (sc[q] > bv || (sc[q] == bv && e < be))) {
-            bv = sc[q];
-            be = e;
-            bb = clean_base ? v[q] : sc[q];
+          for (int q = 0; q < EPL; ++q) {
+            const int e = lane + 32 * q;
+            if (e < E && !((taken >> q) & 1u) && (sc[q] > bv || (sc[q] == bv && e < be))) {
+              bv = sc[q];
+              be = e;
+              bb = clean_base ? v[q] : sc[q];
+            }
           }
-        }
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-          const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-          const float ob = __shfl_xor_sync(0xffffffffu, bb, o);
-          if (ov > bv || (ov == bv && oe < be)) {
-            bv = ov;
-            be = oe;
-            bb = ob;
+          for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+            const float ob = __shfl_xor_sync(0xffffffffu, bb, o);
+            if (ov > bv || (ov == bv && oe < be)) {
+              bv = ov;
+              be = oe;
+              bb = ob;
+            }
           }
+          if (be >= E) be = 0;  // only reachable with NaN scores, already flagged
+          if ((be & 31) == lane) taken |= 1u << (be >> 5);
+          sel_e[j] = be;
+          sel_b[j] = bb;
         }
-        if (be >= E) be = 0;  // only reachable with NaN scores, already flagged
-        if ((be & 31) == lane) taken |= 1u << (be >> 5);
-        sel_e[j] = be;
-        sel_b[j] = bb;
       }
-    }
 
-    // gate weights of the kept experts
-    float bmax = sel_b[0];
+      // gate weights of the kept experts
+      float bmax = sel_b[0];
 #pragma unroll
-    for (int j = 1; j < K; ++j) bmax = fmaxf(bmax, sel_b[j]);
-    float w[K];
-    float den = 0.f;
+      for (int j = 1; j < K; ++j) bmax = fmaxf(bmax, sel_b[j]);
+      float w[K];
+      float den = 0.f;
 #pragma unroll
-    for (int j = 0; j < K; ++j) {
-      // mode 0: softmax over the kept logits, shifted by the largest kept one;
-      // mode 1: the full-softmax probability p_j = exp(b_j - m) / s.
-      w[j] = (gate == 0) ? expf(sel_b[j] - bmax) : expf(sel_b[j] - m) / s;
-      den += w[j];
-    }
-    int my_e = 0;
-    float my_w = 0.f;
-#pragma unroll
-    for (int j = 0; j < K; ++j)
-      if (j == lane) {
-        my_e = sel_e[j];
-        my_w = w[j] / den;
+      for (int j = 0; j < K; ++j) {
+        // mode 0: softmax over the kept logits, shifted by the largest kept one;
+        // mode 1: the full-softmax probability p_j = exp(b_j - m) / s.
+        w[j] = (gate == 0) ? expf(sel_b[j] - bmax) : expf(sel_b[j] - m) / s;
+        den += w[j];
       }
-    if (lane < K) {
-      topk_idx[t * K + lane] = my_e;
-      topk_w[t * K + lane] = my_w;
-      atomicAdd(&s_hist[my_e], 1);
+      int my_e = 0;
+      float my_w = 0.f;
+#pragma unroll
+      for (int j = 0; j < K; ++j)
+        if (j == lane) {
+          my_e = sel_e[j];
+          my_w = w[j] / den;
+        }
+      if (lane < K) {
+        topk_idx[t * K + lane] = my_e;
+        topk_w[t * K + lane] = my_w;
+        atomicAdd(&s_hist[my_e], 1);
+      }
     }
   }
 
