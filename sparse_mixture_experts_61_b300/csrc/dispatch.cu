@@ -87,7 +87,9 @@ __global__ void __launch_bounds__(kThreads)
 }
 
 // Row gather Xp[r, :] = x[row_token[r], :] for r < M = offsets[E]: one warp per row,
-// grid-stride over rows, four independent 16-byte loads in flight per lane.
+// grid-stride over rows, four independent 16-byte loads in flight per lane.  Used by
+// expert-choice routing, whose selection lists each expert's rows by token; top-k
+// dispatch copies token by token instead (scatter_rows_kernel below).
 template <typename Tin>
 __global__ void __launch_bounds__(kThreads)
     gather_rows_kernel(const int32_t* __restrict__ row_token, const int32_t* __restrict__ offsets,
