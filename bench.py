@@ -11,8 +11,10 @@ CUDA-event pair.  Under torchrun each rank runs an independent replica on its ow
 batch (token-parallel, no data-path collective): value = tokens of all ranks / the
 slowest rank's time.  Rank 0 prints one JSON line.
 
-The line carries: the device-timed tokens/s (`value`), the end-to-end tokens/s with
-host-resident x and y copied in and out inside the timed region (`e2e`), the grouped
+The line carries: the device-timed tokens/s (`value`, T over the median step), the
+end-to-end tokens/s with host-resident x and y copied in and out inside the timed region
+(`e2e`: moe_forward_host over `steps` pinned batches, copies overlapped with the layer;
+`e2e.serial_value` one step at a time), the grouped
 expert GEMM pair timed alone against the measured roofline (`roofline`), the CPU
 oracle timed on a bounded sample of the same workload (`cpu_baseline`), SM clocks
 sampled during the timed region (`clocks`) and the number of our kernel launches in
@@ -47,7 +49,7 @@ METRIC = "MoE-layer fwd tokens/s at 1 B300; grouped-GEMM % BF16 peak; decode % H
 UNIT = "tokens/s"
 DEFAULT_WORKLOAD = "mixtral_prefill"
 L2_FLUSH_BYTES = 256 << 20
-KERNELS_PER_FORWARD = 8   # router GEMM, softmax/top-k, finalize/scan, place, gather, GEMM1, GEMM2, combine
+KERNELS_PER_FORWARD = 8   # router GEMM, softmax/top-k, finalize/scan, place, row copy, GEMM1, GEMM2, combine
 KERNELS_PER_EC_FORWARD = 7  # router GEMM, softmax, per-expert select, gather, GEMM1, GEMM2, combine
 # moe_backward: combine and gate backward, dA / dXp / router-dx GEMMs, the dx sum, dW2 / dW1 /
 # dW_g GEMMs with two tail-packing kernels before each expert one, three two-kernel column sums
