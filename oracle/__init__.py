@@ -29,7 +29,9 @@ _D = ctypes.c_double
 def lib():
     global _lib
     if _lib is None:
-        path = _build.build()
+        # MOE_ORACLE_LIB names a prebuilt copy of the oracle instead (the test that plants
+        # mistakes in copies of the source and checks that the pins catch each one).
+        path = os.environ.get("MOE_ORACLE_LIB") or _build.build()
         L = ctypes.CDLL(path)
         L.orc_num_threads.restype = _I
         L.orc_set_num_threads.argtypes = [_I]

@@ -1,0 +1,91 @@
+"""The oracle's pins catch planted mistakes.
+
+Each case copies ``oracle/moe_oracle.cpp``, plants one plausible mistake in the copy
+(a wrong tie-break, a wrong normaliser, an off-by-one capacity test, a dropped term, a
+sign, a transposed operand, a missing weight, a wrong derivative), compiles it with the
+oracle's own flags and runs ``tests/test_oracle_pins.py`` against it in a subprocess: at
+least one pin must fail.  The unchanged copy, compiled the same way, must pass them all,
+so a failure is the mistake's and not the harness's.  The mistakes live only in
+temporary copies; the oracle itself is never modified.
+"""
+
+import concurrent.futures as cf
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "moe_oracle.cpp")
+
+# name -> [(text in the oracle, planted replacement)]; each text occurs exactly once.
+MUTANTS = {
+    "topk_tie_to_higher_index": [
+        ("if (best < 0 || l[e] > l[best]) best = e;", "if (best < 0 || l[e] >= l[best]) best = e;")],
+    "P_over_T_times_k": [
+        ("pe = (double)c[e] / (double)T;", "pe = (double)c[e] / ((double)T * k);")],
+    "capacity_keeps_C_plus_one": [
+        ("if (C < 0 || pos[t * k + j] < C) nkept[e] += 1;",
+         "if (C < 0 || pos[t * k + j] <= C) nkept[e] += 1;"),
+        ("if (C < 0 || q < C) {", "if (C < 0 || q <= C) {")],
+    "softmax_denominator_drops_expert_0": [
+        ("for (int e = 0; e < E; ++e) s += std::exp(l[e] - m);",
+         "for (int e = 1; e < E; ++e) s += std::exp(l[e] - m);")],
+    "b2_subtracted": [
+        ("if (b2) acc += elem(b2, dtype, o);", "if (b2) acc -= elem(b2, dtype, o);")],
+    "silu_sign": [
+        ("double silu(double a) { return a / (1.0 + std::exp(-a)); }",
+         "double silu(double a) { return a / (1.0 + std::exp(a)); }")],
+    "w1_transposed": [
+        ("a += elem(w1, dtype, (int64_t)i * d + c) * elem(x_rows, dtype, r * d + c);",
+         "a += elem(w1, dtype, (int64_t)c * h + i) * elem(x_rows, dtype, r * d + c);")],
+    "combine_ignores_gate_weight": [
+        ("for (int o = 0; o < d; ++o) y[t * d + o] += w[t * k + j] * zz[o];",
+         "for (int o = 0; o < d; ++o) y[t * d + o] += zz[o];")],
+    "silu_grad_missing_term": [
+        ("return sg * (1.0 + a * (1.0 - sg));", "return sg * (1.0 + a * sg);")],
+}
+
+FLAGS = ["g++", "-std=c++17", "-O2", "-fno-fast-math", "-ffp-contract=off", "-fopenmp",
+         "-shared", "-fPIC"]
+
+
+def _build(tmp, name, edits):
+    text = open(SRC).read()
+    for old, new in edits:
+        assert text.count(old) == 1, (name, old)
+        text = text.replace(old, new)
+    src = os.path.join(tmp, f"{name}.cpp")
+    lib = os.path.join(tmp, f"lib{name}.so")
+    with open(src, "w") as f:
+        f.write(text)
+    subprocess.run(FLAGS + [src, "-o", lib], check=True)
+    return lib
+
+
+def _pins(lib):
+    env = dict(os.environ, MOE_ORACLE_LIB=lib, OMP_NUM_THREADS="2")
+    return subprocess.run([sys.executable, "-m", "pytest", "tests/test_oracle_pins.py", "-x", "-q",
+                           "-p", "no:cacheprovider"], cwd=ROOT, env=env, capture_output=True,
+                          text=True, timeout=600)
+
+
+@pytest.fixture(scope="module")
+def libs(tmp_path_factory):
+    tmp = str(tmp_path_factory.mktemp("oracle_mutants"))
+    cases = dict(MUTANTS, unchanged=[])
+    with cf.ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 1)) as ex:
+        futs = {name: ex.submit(_build, tmp, name, edits) for name, edits in cases.items()}
+        return {name: f.result() for name, f in futs.items()}
+
+
+def test_unchanged_copy_passes_every_pin(libs):
+    r = _pins(libs["unchanged"])
+    assert r.returncode == 0, r.stdout[-2000:]
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_planted_mistake(libs, name):
+    r = _pins(libs[name])
+    assert r.returncode == 1 and " failed" in r.stdout, (name, r.stdout[-2000:])
