@@ -2,7 +2,8 @@
 
 Each case copies ``oracle/moe_oracle.cpp``, plants one plausible mistake in the copy
 (a wrong tie-break, a wrong normaliser, an off-by-one capacity test, a dropped term, a
-sign, a transposed operand, a missing weight, a wrong derivative), compiles it with the
+sign, a transposed operand, a missing weight, a wrong derivative, in the top-k, expert-choice
+and noisy-routing stages), compiles it with the
 oracle's own flags and runs ``tests/test_oracle_pins.py`` against it in a subprocess: at
 least one pin must fail.  The unchanged copy, compiled the same way, must pass them all,
 so a failure is the mistake's and not the harness's.  The mistakes live only in
@@ -45,6 +46,17 @@ MUTANTS = {
          "for (int o = 0; o < d; ++o) y[t * d + o] += zz[o];")],
     "silu_grad_missing_term": [
         ("return sg * (1.0 + a * (1.0 - sg));", "return sg * (1.0 + a * sg);")],
+    "expert_choice_ties_to_higher_token": [
+        ("for (int64_t t = 0; t < T; ++t) order[t] = t;",
+         "for (int64_t t = 0; t < T; ++t) order[t] = T - 1 - t;")],
+    "expert_choice_combine_ignores_weight": [
+        ("for (int o = 0; o < d; ++o) y[t * d + o] += sel_w[e * C + c] * zz[o];",
+         "for (int o = 0; o < d; ++o) y[t * d + o] += zz[o];")],
+    "gumbel_sign": [
+        ("v = l[e] - std::log(-std::log((double)n[e] + 1e-9) + 1e-9);",
+         "v = l[e] + std::log(-std::log((double)n[e] + 1e-9) + 1e-9);")],
+    "logit_noise_not_scaled": [
+        ("v = l[e] + (double)n[e] * p[e];", "v = l[e] + (double)n[e];")],
 }
 
 FLAGS = ["g++", "-std=c++17", "-O2", "-fno-fast-math", "-ffp-contract=off", "-fopenmp",

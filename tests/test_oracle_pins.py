@@ -420,7 +420,9 @@ def test_expert_choice_matches_rank_brute_force(T, E, C):
     """Token t is chosen by expert e iff fewer than C tokens rank above it in column e,
     where t' ranks above t when p[t',e] > p[t,e], or they are equal and t' < t."""
     rng = np.random.default_rng(T + E)
-    p = oracle.softmax(np.round(rng.standard_normal((T, E)), 1))   # rounding forces ties
+    # Scores from a few values, so every column holds runs of equal scores and the rule
+    # for equal values decides which tokens straddling the C-th place are taken.
+    p = rng.integers(1, 5, size=(T, E)) / 8.0
     tok, w = oracle.expert_choice(p, C)
     for e in range(E):
         above = [sum(1 for q in range(T) if p[q, e] > p[t, e] or (p[q, e] == p[t, e] and q < t))
