@@ -57,6 +57,28 @@ MUTANTS = {
          "v = l[e] + std::log(-std::log((double)n[e] + 1e-9) + 1e-9);")],
     "logit_noise_not_scaled": [
         ("v = l[e] + (double)n[e] * p[e];", "v = l[e] + (double)n[e];")],
+    "renorm_gate_not_renormalised": [
+        ("for (int j = 0; j < k; ++j) w[t * k + j] = p[idx[t * k + j]] / den;",
+         "for (int j = 0; j < k; ++j) w[t * k + j] = p[idx[t * k + j]];")],
+    "loss_missing_factor_E": [
+        ("return (double)E * loss;", "return loss;")],
+    "stats_population_std": [
+        ("const double lstd = E > 1 ? std::sqrt(lvar / (E - 1)) : 0.0;",
+         "const double lstd = E > 1 ? std::sqrt(lvar / E) : 0.0;")],
+    "stats_entropy_sign": [
+        ("ent -= load[e] * std::log(load[e] + 1e-10);", "ent += load[e] * std::log(load[e] + 1e-10);")],
+    "capacity_rounds_down": [
+        ("return (int64_t)std::ceil((double)T * capacity_factor / (double)E);",
+         "return (int64_t)std::floor((double)T * capacity_factor / (double)E);")],
+    "dispatch_slot_major_priority": [
+        ("""  for (int64_t t = 0; t < T; ++t)
+    for (int j = 0; j < k; ++j) {
+      int e = idx[t * k + j];
+      pos[t * k + j] = next[e]++;""",
+         """  for (int j = 0; j < k; ++j)
+    for (int64_t t = 0; t < T; ++t) {
+      int e = idx[t * k + j];
+      pos[t * k + j] = next[e]++;""")],
 }
 
 FLAGS = ["g++", "-std=c++17", "-O2", "-fno-fast-math", "-ffp-contract=off", "-fopenmp",
