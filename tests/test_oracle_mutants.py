@@ -79,6 +79,17 @@ MUTANTS = {
     for (int64_t t = 0; t < T; ++t) {
       int e = idx[t * k + j];
       pos[t * k + j] = next[e]++;""")],
+    "gate_jacobian_without_mean_term": [
+        ("dl[t * E + idx[t * k + j]] += w[t * k + j] * (dw[t * k + j] - inner);",
+         "dl[t * E + idx[t * k + j]] += w[t * k + j] * dw[t * k + j];")],
+    "gate_jacobian_skips_dropped_slots": [
+        ("""    for (int j = 0; j < k; ++j)
+      dl[t * E + idx[t * k + j]] += w[t * k + j] * (dw[t * k + j] - inner);""",
+         """    for (int j = 0; j < k; ++j)
+      if (slot_row[t * k + j] >= 0)
+        dl[t * E + idx[t * k + j]] += w[t * k + j] * (dw[t * k + j] - inner);""")],
+    "balance_gradient_without_mean_term": [
+        ("((double)counts[c] / (double)T - pp);", "((double)counts[c] / (double)T);")],
 }
 
 FLAGS = ["g++", "-std=c++17", "-O2", "-fno-fast-math", "-ffp-contract=off", "-fopenmp",
@@ -106,20 +117,22 @@ def _pins(lib):
 
 
 @pytest.fixture(scope="module")
-def libs(tmp_path_factory):
+def runs(tmp_path_factory):
+    """Every copy built and its pin run done, several at a time."""
     tmp = str(tmp_path_factory.mktemp("oracle_mutants"))
     cases = dict(MUTANTS, unchanged=[])
     with cf.ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 1)) as ex:
-        futs = {name: ex.submit(_build, tmp, name, edits) for name, edits in cases.items()}
+        futs = {name: ex.submit(lambda n, e: _pins(_build(tmp, n, e)), name, edits)
+                for name, edits in cases.items()}
         return {name: f.result() for name, f in futs.items()}
 
 
-def test_unchanged_copy_passes_every_pin(libs):
-    r = _pins(libs["unchanged"])
+def test_unchanged_copy_passes_every_pin(runs):
+    r = runs["unchanged"]
     assert r.returncode == 0, r.stdout[-2000:]
 
 
 @pytest.mark.parametrize("name", sorted(MUTANTS))
-def test_pins_catch_planted_mistake(libs, name):
-    r = _pins(libs[name])
+def test_pins_catch_planted_mistake(runs, name):
+    r = runs[name]
     assert r.returncode == 1 and " failed" in r.stdout, (name, r.stdout[-2000:])
