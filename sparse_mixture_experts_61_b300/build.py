@@ -28,6 +28,9 @@ NVCC = os.environ.get("NVCC", "nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-std=c++17", "-O3", "-lineinfo", "--expt-relaxed-constexpr", "-Xcompiler", "-fPIC",
          "-Xcompiler", "-fvisibility=hidden", "-I", os.path.join(ROOT, "include")]
+# MOE_NVTX=1: compile in NVTX ranges around moe_forward's stages (rebuild with --force).
+if os.environ.get("MOE_NVTX") == "1":
+    FLAGS += ["-DMOE_NVTX=1"]
 
 
 def sources():

@@ -16,6 +16,25 @@
 
 #define MOE_EXPORT extern "C" __attribute__((visibility("default")))
 
+// Trace ranges, compiled in only with MOE_NVTX (python -m sparse_mixture_experts_61_b300.build
+// --force with MOE_NVTX=1 in the environment): each stage of moe_forward's enqueue becomes
+// an NVTX range on the calling host thread, which a timeline tool shows over that stage's
+// kernel launches.  Without the switch the macro expands to nothing.
+#ifdef MOE_NVTX
+#include <nvtx3/nvToolsExt.h>
+namespace moe {
+struct TraceRange {
+  explicit TraceRange(const char* name) { nvtxRangePushA(name); }
+  ~TraceRange() { nvtxRangePop(); }
+  TraceRange(const TraceRange&) = delete;
+  TraceRange& operator=(const TraceRange&) = delete;
+};
+}  // namespace moe
+#define MOE_TRACE(name) ::moe::TraceRange moe_trace_range_(name)
+#else
+#define MOE_TRACE(name) static_cast<void>(0)
+#endif
+
 namespace moe {
 namespace {
 
@@ -462,17 +481,29 @@ moe_status moe::forward_entry(const moe_config* cfg, const moe_forward_args* a, 
   void* y_perm = a->y_perm ? a->y_perm : at<void>(ws, L.y_perm);
   const int64_t C = capacity_of(c);
 
-  if ((s = run_router(c, L, ws, a->x, a->w_gate, a->logit_bias, a->noise, a->logits, idx, w,
-                      flags, sms, st)) != MOE_OK)
-    return s;
-  MOE_CUDA(launch_route_finalize(hist, psum, static_cast<int>(L.nchunks), c.E, c.T, C, counts, aux,
-                                 chunk_base, kept, offsets, dropped, a->routing_stats, st));
-  MOE_CUDA(launch_dispatch_place(c.dtype, idx, c.T, c.E, c.k, C, chunk_base, offsets, slot_row,
-                                 row_token, a->x, x_perm, c.d, flags, st));
-  if ((s = run_expert_ffn(c, x_perm, offsets, a->w1, a->b1, a->w2, a->b2, h_buf, y_perm, flags,
-                          sms, st, a->h_pre)) != MOE_OK)
-    return s;
-  MOE_CUDA(launch_combine(c.dtype, y_perm, slot_row, w, c.T, c.d, c.k, a->y, flags, st));
+  {
+    MOE_TRACE("moe_forward: route");
+    if ((s = run_router(c, L, ws, a->x, a->w_gate, a->logit_bias, a->noise, a->logits, idx, w,
+                        flags, sms, st)) != MOE_OK)
+      return s;
+    MOE_CUDA(launch_route_finalize(hist, psum, static_cast<int>(L.nchunks), c.E, c.T, C, counts,
+                                   aux, chunk_base, kept, offsets, dropped, a->routing_stats, st));
+  }
+  {
+    MOE_TRACE("moe_forward: dispatch");
+    MOE_CUDA(launch_dispatch_place(c.dtype, idx, c.T, c.E, c.k, C, chunk_base, offsets, slot_row,
+                                   row_token, a->x, x_perm, c.d, flags, st));
+  }
+  {
+    MOE_TRACE("moe_forward: expert_ffn");
+    if ((s = run_expert_ffn(c, x_perm, offsets, a->w1, a->b1, a->w2, a->b2, h_buf, y_perm, flags,
+                            sms, st, a->h_pre)) != MOE_OK)
+      return s;
+  }
+  {
+    MOE_TRACE("moe_forward: combine");
+    MOE_CUDA(launch_combine(c.dtype, y_perm, slot_row, w, c.T, c.d, c.k, a->y, flags, st));
+  }
   return MOE_OK;
 }
 
