@@ -415,6 +415,38 @@ def test_logit_softmax_noise_closed_forms():
     assert np.all(oracle.topk(sc, 2) == np.array([3, 2]))
 
 
+@pytest.mark.parametrize("noise_mode", [oracle.NOISE_PROB_GAUSS, oracle.NOISE_LOGIT_SOFTMAX])
+@pytest.mark.parametrize("mode,cf", [(0, None), (1, 1.0)])
+def test_noisy_routing_with_zero_draws_is_clean_routing(noise_mode, mode, cf):
+    """Zero draws leave the probabilities (noise on p) or the logits (noise scaled by p)
+    unchanged, so the noisy routing reference reduces to the clean one: same selection,
+    gate weights, counts, loss and placement."""
+    rng = np.random.default_rng(20 + noise_mode)
+    lg = rng.standard_normal((40, 8)).astype(np.float32)
+    sc = oracle.noisy_scores(lg, np.zeros_like(lg), noise_mode).astype(np.float32)
+    noisy = oracle.noisy_routed_reference(2, mode, cf, sc, noise_mode, lg.astype(np.float64))
+    clean = oracle.routed_reference(None, 2, mode, cf, lg)
+    for key in ("idx", "counts", "slot_row", "offsets", "kept"):
+        np.testing.assert_array_equal(noisy[key], clean[key], err_msg=key)
+    np.testing.assert_allclose(noisy["w"], clean["w"], rtol=1e-6, atol=1e-7)
+    assert abs(noisy["aux"] - clean["aux"]) <= 1e-6 * abs(clean["aux"])
+
+
+def test_probability_noise_keeps_clean_gate_weights():
+    """Noise on the probabilities only picks the experts: the kept experts' weights are
+    the clean gate's, a distribution over the kept set, whatever the draws."""
+    rng = np.random.default_rng(31)
+    lg = rng.standard_normal((40, 8))
+    n = (0.3 * rng.standard_normal((40, 8))).astype(np.float32)
+    sc = oracle.noisy_scores(lg, n, oracle.NOISE_PROB_GAUSS).astype(np.float32)
+    for mode in (0, 1):
+        r = oracle.noisy_routed_reference(2, mode, None, sc, oracle.NOISE_PROB_GAUSS, lg)
+        np.testing.assert_array_equal(r["w"], oracle.gate_weights(lg, r["idx"], mode))
+        np.testing.assert_allclose(r["w"].sum(axis=1), 1.0, rtol=1e-12)
+        # the noise moved some selections away from the clean top-2
+        assert np.any(r["idx"] != oracle.topk(lg, 2))
+
+
 @pytest.mark.parametrize("T,E,C", [(50, 4, 13), (64, 8, 1), (7, 3, 7), (100, 16, 0)])
 def test_expert_choice_matches_rank_brute_force(T, E, C):
     """Token t is chosen by expert e iff fewer than C tokens rank above it in column e,
