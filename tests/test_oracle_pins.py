@@ -415,6 +415,27 @@ def test_logit_softmax_noise_closed_forms():
     assert np.all(oracle.topk(sc, 2) == np.array([3, 2]))
 
 
+@pytest.mark.parametrize("mode,cf,k", [(0, None, 2), (1, 1.0, 2), (1, 0.75, 3)])
+def test_routed_reference_is_the_forward_routing(mode, cf, k):
+    """Fed the forward's own logits, the routing reference (what the GPU tests run on the
+    GPU's logits) reproduces the whole layer's routing.  x in {-1, 0, 1} and W_g in
+    multiples of 1/8 make every logit exact in fp32, so the fp32 hand-off loses nothing,
+    and leave many equal logits for the tie rule."""
+    g = torch.Generator().manual_seed(40 + k)
+    T, d, h, E = 48, 16, 8, 6
+    inp = dict(x=torch.randint(-1, 2, (T, d), generator=g).float(),
+               w_gate=torch.randint(-8, 9, (E, d), generator=g).float() / 8,
+               w1=torch.randn((E, h, d), generator=g), b1=None,
+               w2=torch.randn((E, d, h), generator=g), b2=None, logit_bias=None)
+    out = oracle.forward(inp, k, mode, cf)
+    assert np.array_equal(out["logits"].astype(np.float32).astype(np.float64), out["logits"])
+    ref = oracle.routed_reference(None, k, mode, cf, out["logits"].astype(np.float32))
+    for key in ("idx", "counts", "kept", "offsets", "slot_row", "row_token"):
+        np.testing.assert_array_equal(ref[key], out[key], err_msg=key)
+    np.testing.assert_array_equal(ref["w"], out["w"])
+    assert ref["aux"] == out["aux"] and ref["dropped"] == out["dropped"]
+
+
 @pytest.mark.parametrize("noise_mode", [oracle.NOISE_PROB_GAUSS, oracle.NOISE_LOGIT_SOFTMAX])
 @pytest.mark.parametrize("mode,cf", [(0, None), (1, 1.0)])
 def test_noisy_routing_with_zero_draws_is_clean_routing(noise_mode, mode, cf):
