@@ -436,6 +436,19 @@ def test_routed_reference_is_the_forward_routing(mode, cf, k):
     assert ref["aux"] == out["aux"] and ref["dropped"] == out["dropped"]
 
 
+@pytest.mark.parametrize("name", ["tiny_f32", "switch_capacity"])
+def test_expert_path_on_given_routing_is_the_forward_output(name):
+    """The GPU tests' expert path on a given routing (the test library's y_on_routing,
+    oracle expert rows and combine), fed the forward's own routing, gives the forward's y."""
+    import moe_testlib as tl
+    w = PARITY_WORKLOADS[name].scaled(T=96, d=32, h=48)
+    inp = make_inputs(w, seed=3)
+    cf = w.capacity_factor if w.capacity_factor > 0 else None
+    out = oracle.forward(inp, w.k, w.gate, cf)
+    y = tl.y_on_routing(inp, out["idx"], out["slot_row"], out["w"])
+    np.testing.assert_allclose(y, out["y"], rtol=1e-12, atol=1e-14)
+
+
 @pytest.mark.parametrize("noise_mode", [oracle.NOISE_PROB_GAUSS, oracle.NOISE_LOGIT_SOFTMAX])
 @pytest.mark.parametrize("mode,cf", [(0, None), (1, 1.0)])
 def test_noisy_routing_with_zero_draws_is_clean_routing(noise_mode, mode, cf):
