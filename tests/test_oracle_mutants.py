@@ -90,6 +90,22 @@ MUTANTS = {
         dl[t * E + idx[t * k + j]] += w[t * k + j] * (dw[t * k + j] - inner);""")],
     "balance_gradient_without_mean_term": [
         ("((double)counts[c] / (double)T - pp);", "((double)counts[c] / (double)T);")],
+    "logit_bias_ignored": [
+        ("if (logit_bias) acc += (double)logit_bias[e];", "(void)logit_bias;")],
+    "b1_ignored": [
+        ("if (b1) a += elem(b1, dtype, i);", "(void)b1;")],
+    "offsets_inclusive": [
+        ("""    offsets[e] = (int32_t)run;
+    kept[e] = (int32_t)nkept[e];
+    run += nkept[e];""",
+         """    kept[e] = (int32_t)nkept[e];
+    run += nkept[e];
+    offsets[e] = (int32_t)run;""")],
+    "dx_missing_router_term": [
+        ("""      for (int e = 0; e < E; ++e) acc += dl[t * E + e] * elem(wg, dtype, (int64_t)e * d + c);
+      dx[t * d + c] += acc;""",
+         """      for (int e = 0; e < E; ++e) acc += dl[t * E + e] * elem(wg, dtype, (int64_t)e * d + c);
+      (void)acc;""")],
 }
 
 FLAGS = ["g++", "-std=c++17", "-O2", "-fno-fast-math", "-ffp-contract=off", "-fopenmp",
