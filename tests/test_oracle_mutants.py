@@ -20,7 +20,8 @@ import pytest
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SRC = os.path.join(ROOT, "oracle", "moe_oracle.cpp")
 
-# name -> [(text in the oracle, planted replacement)]; each text occurs exactly once.
+# name -> [(text in the oracle, planted replacement)]; each text occurs exactly once.  Every
+# mistake keeps memory accesses in bounds, so a copy fails by its results, not by a crash.
 MUTANTS = {
     "topk_tie_to_higher_index": [
         ("if (best < 0 || l[e] > l[best]) best = e;", "if (best < 0 || l[e] >= l[best]) best = e;")],
@@ -94,13 +95,10 @@ MUTANTS = {
         ("if (logit_bias) acc += (double)logit_bias[e];", "(void)logit_bias;")],
     "b1_ignored": [
         ("if (b1) a += elem(b1, dtype, i);", "(void)b1;")],
-    "offsets_inclusive": [
-        ("""    offsets[e] = (int32_t)run;
-    kept[e] = (int32_t)nkept[e];
-    run += nkept[e];""",
-         """    kept[e] = (int32_t)nkept[e];
-    run += nkept[e];
-    offsets[e] = (int32_t)run;""")],
+    "kept_counts_include_drops": [
+        ("kept[e] = (int32_t)nkept[e];", "kept[e] = (int32_t)next[e];")],
+    "row_token_holds_slot": [
+        ("row_token[row] = (int32_t)t;", "row_token[row] = (int32_t)j;")],
     "dx_missing_router_term": [
         ("""      for (int e = 0; e < E; ++e) acc += dl[t * E + e] * elem(wg, dtype, (int64_t)e * d + c);
       dx[t * d + c] += acc;""",
