@@ -20,6 +20,15 @@ oracle timed on a bounded sample of the same workload (`cpu_baseline`), SM clock
 sampled during the timed region (`clocks`) and the number of our kernel launches in
 the timed region (`gpu_launches`).
 
+With the default workload the line also carries `workloads`: every configuration of
+the layer family (tiny fp32, 8-expert prefill, 128-expert Switch with capacity,
+256-expert top-8, 64-token decode) timed the same way (CUDA events, median step, L2
+flushed before each step), each with its expert-GEMM pair against the measured roofline,
+its routing stage's share of the forward and its own clock record.
+
+--gpus N without a launcher starts N ranks of this script itself (torch.distributed.run
+on 127.0.0.1); under a launcher --gpus must equal WORLD_SIZE.
+
 --impl reference times the CPU oracle itself (the plain fp64 implementation the
 parity tests use) on the host cores, each step a bounded sample of the workload.
 """
@@ -27,9 +36,11 @@ parity tests use) on the host cores, each step a bounded sample of the workload.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import math
 import os
+import socket
 import statistics
 import subprocess
 import sys
@@ -57,18 +68,31 @@ KERNELS_PER_BACKWARD = 19
 TRAIN_METRIC = "MoE-layer fwd+bwd (training step) tokens/s at 1 B300; backward GEMMs % BF16 peak"
 D_AUX = 0.01
 
-# dram__bytes_read.sum + dram__bytes_write.sum per launch of the grouped GEMM pair
-# (G1 + G2), from the ncu capture summarised in
-# profiles/traffic_expert_gemms_bf16_workloads.md.  Only workloads whose current kernels
-# were captured appear here; others report null.
-NCU_TRAFFIC_BYTES = {
-    "mixtral_prefill": 2723980800,
-    "deepseek_fine": 17652525568,
-    "mixtral_prefill_ec": 2653969920,
-    "deepseek_fine_ec": 17529011456,
-    "decode": 4481113856,
-    "switch_capacity": 156258816,
-}
+# dram__bytes_read.sum + dram__bytes_write.sum of one moe_expert_ffn (the grouped GEMM
+# pair G1 + G2) from an ncu capture, with the hash (gemm_source_hash) of the GEMM sources
+# that capture ran.  A figure whose hash differs from the current sources' is stale and
+# reported as null.
+NCU_TRAFFIC_BYTES = {}
+GEMM_SOURCES = ("sparse_mixture_experts_61_b300/csrc/gemm_tc.cu",
+                "sparse_mixture_experts_61_b300/csrc/tc_pipe.cuh",
+                "sparse_mixture_experts_61_b300/csrc/common.cuh")
+# Configurations of the layer family reported in the default run's `workloads` map.
+FAMILY = ("tiny_f32", "mixtral_prefill", "switch_capacity", "deepseek_fine", "decode")
+
+
+def gemm_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in GEMM_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(name: str):
+    entry = NCU_TRAFFIC_BYTES.get(name)
+    if entry is None or entry[0] != gemm_source_hash():
+        return None
+    return entry[1]
 
 
 def load_peaks():
@@ -308,7 +332,7 @@ def roofline(w, M, nonempty, t_ffn_s, peaks):
     flops, byts = ffn_algorithmic(w, M, nonempty)
     t_tensor = flops / (peaks["bf16_tflops"] * 1e12)
     t_hbm = byts / (peaks["hbm_gbs"] * 1e9)
-    traffic = NCU_TRAFFIC_BYTES.get(w.name)
+    traffic = ncu_traffic(w.name)
     if t_tensor >= t_hbm:
         achieved = flops / t_ffn_s / 1e12
         r = dict(bound="tensor", achieved=round(achieved, 1), peak=peaks["bf16_tflops"],
@@ -326,6 +350,130 @@ def roofline(w, M, nonempty, t_ffn_s, peaks):
 
 
 # ------------------------------------------------------------------ our arm
+def _median_event_ms(fn, steps, warmup, flush, stream):
+    """Median CUDA-event time of fn() over `steps` calls after `warmup` calls, with L2
+    flushed (a 256 MB write) before every call, outside the event pair."""
+    ev = []
+    for i in range(steps + warmup):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        if i >= warmup:
+            ev.append((a, b))
+    torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(b) for a, b in ev)
+
+
+def ffn_alone(moe, w, cfg, inp, outs, C, dev):
+    """Callable of the grouped expert GEMM pair alone (moe_expert_ffn) on the rows the
+    layer's routing produces, plus its stage workspace.  Expert choice: the same call on
+    its E groups of C rows, through a top-k configuration with capacity C (identical
+    tile height and row count)."""
+    i32 = dict(dtype=torch.int32, device=dev)
+    ec = w.routing == "expert_choice"
+    ffn_cfg = cfg
+    if ec:
+        ffn_cfg = moe.config(w.T, w.d, w.h, w.E, w.k, w.dtype, w.gate, w.capacity_factor)
+        assert moe.moe_capacity(ffn_cfg) == C
+    sws = torch.empty(moe.moe_stage_workspace_size(ffn_cfg), dtype=torch.uint8, device=dev)
+    rows = w.T * w.k
+    x_perm = torch.empty((rows, w.d), dtype=w.torch_dtype, device=dev)
+    h_buf = torch.empty((rows, w.h), dtype=w.torch_dtype, device=dev)
+    y_perm = torch.empty((rows, w.d), dtype=w.torch_dtype, device=dev)
+    offsets = torch.empty((w.E + 1,), **i32)
+    if ec:
+        M = w.E * C
+        torch.index_select(inp["x"], 0, outs["sel_token"].flatten().long(), out=x_perm[:M])
+        offsets.copy_(torch.arange(w.E + 1, dtype=torch.int32, device=dev) * C)
+    else:
+        idx = torch.empty((w.T, w.k), **i32)
+        wts = torch.empty((w.T, w.k), dtype=torch.float32, device=dev)
+        slot_row = torch.empty((w.T, w.k), **i32)
+        row_token = torch.empty((rows,), **i32)
+        moe.moe_route(cfg, inp["x"], inp["w_gate"], inp["logit_bias"], None, idx, wts, None, None,
+                      sws)
+        moe.moe_dispatch(cfg, inp["x"], idx, offsets, None, slot_row, row_token, None, x_perm, sws)
+
+    def call():
+        moe.moe_expert_ffn(ffn_cfg, x_perm, offsets, inp["w1"], inp["b1"], inp["w2"], inp["b2"],
+                           h_buf, y_perm, sws)
+    return call, sws
+
+
+def family_entry(moe, w, steps, warmup, flush, stream, dev, rank, world, peaks):
+    """One configuration of the layer family: the forward's tokens/s (median of `steps`
+    steps), the expert-GEMM pair alone against the roofline, the routing stage
+    (moe_route with counts and balance loss) and its share of the forward, and the SM
+    clocks sampled while they ran."""
+    inp = make_inputs(w, seed=rank, device=str(dev))
+    cfg = moe.config_from_workload(w)
+    i32 = dict(dtype=torch.int32, device=dev)
+    outs = dict(y=torch.empty((w.T, w.d), dtype=w.torch_dtype, device=dev),
+                offsets=torch.empty((w.E + 1,), **i32), kept_counts=torch.empty((w.E,), **i32))
+    ws = torch.empty(moe.moe_workspace_size(cfg), dtype=torch.uint8, device=dev)
+    fwd_args = moe.forward_args(inp, outs)
+
+    def fwd():
+        moe.moe_forward(cfg, inp, outs, ws, stream, args=fwd_args)
+
+    sws = torch.empty(moe.moe_stage_workspace_size(cfg), dtype=torch.uint8, device=dev)
+    idx = torch.empty((w.T, w.k), **i32)
+    wts = torch.empty((w.T, w.k), dtype=torch.float32, device=dev)
+    counts = torch.empty((w.E,), **i32)
+    aux = torch.empty((1,), dtype=torch.float32, device=dev)
+
+    def route():
+        moe.moe_route(cfg, inp["x"], inp["w_gate"], inp["logit_bias"], None, idx, wts, counts, aux,
+                      sws)
+
+    for _ in range(warmup):
+        fwd()
+    assert moe.moe_device_error(ws) == 0
+    M = int(outs["offsets"][-1])
+    nonempty = int((outs["kept_counts"] > 0).sum())
+    ffn, fws = ffn_alone(moe, w, cfg, inp, outs, None, dev)
+    clocks = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    if clocks:
+        clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    fwd_ms = _median_event_ms(fwd, steps, 0, flush, stream)
+    ffn_ms = _median_event_ms(ffn, steps, warmup, flush, stream)
+    route_ms = _median_event_ms(route, steps, warmup, flush, stream)
+    t1 = time.time()
+    if clocks:
+        clocks.stop()
+    assert moe.moe_device_error(ws) == 0 and moe.moe_device_error(fws) == 0
+    assert moe.moe_device_error(sws) == 0
+    fwd_ms = allreduce_max(fwd_ms, world)
+    ffn_ms = allreduce_max(ffn_ms, world)
+    route_ms = allreduce_max(route_ms, world)
+    entry = {
+        "tokens_per_s": round(replica_throughput(world, w.T, fwd_ms), 1),
+        "ms_per_step": round(fwd_ms, 4),
+        "kept_rows": M, "nonempty_experts": nonempty,
+        "routing_ms": round(route_ms, 4), "routing_share": round(route_ms / fwd_ms, 4),
+        "inputs": input_recipe(w),
+        "clocks": clocks.summary(t0, t1) if clocks else None,
+    }
+    if w.dtype == "bf16":
+        r = roofline(w, M, nonempty, ffn_ms / 1e3, peaks)
+        flops, byts = r["algorithmic_flops"], r["algorithmic_bytes"]
+        r["frac_of_hbm"] = round(byts / (ffn_ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4)
+        r["frac_of_bf16_burst"] = round(flops / (ffn_ms / 1e3) / 1e12 / peaks["bf16_tflops"], 4)
+        if peaks.get("bf16_tflops_sustained"):
+            r["frac_of_bf16_sustained"] = round(
+                flops / (ffn_ms / 1e3) / 1e12 / peaks["bf16_tflops_sustained"], 4)
+        entry["roofline"] = r
+    else:
+        entry["gemm_pair_ms"] = round(ffn_ms, 4)
+        entry["roofline"] = {"bound": "latency (fp32 SIMT GEMMs)", "ms": round(ffn_ms, 4)}
+    return entry
+
+
 def run_ours(args, world, rank, local):
     import sparse_mixture_experts_61_b300 as moe
 
@@ -391,43 +539,12 @@ def run_ours(args, world, rank, local):
     assert moe.moe_device_error(ws) == 0
 
     # The grouped expert GEMM pair alone (same rows, same stream), for the roofline.
-    # Expert choice: the same moe_expert_ffn call on its E groups of C rows, through a
-    # top-k configuration with capacity C (identical tile height and row count).
-    ffn_cfg = cfg
+    ffn, sws = ffn_alone(moe, w, cfg, inp, outs, C if ec else None, dev)
     if ec:
-        ffn_cfg = moe.config(w.T, w.d, w.h, w.E, w.k, w.dtype, w.gate, w.capacity_factor)
-        assert moe.moe_capacity(ffn_cfg) == C and M <= w.T * w.k
-    sws = torch.empty(moe.moe_stage_workspace_size(ffn_cfg), dtype=torch.uint8, device=dev)
-    rows = w.T * w.k
-    x_perm = torch.empty((rows, w.d), dtype=w.torch_dtype, device=dev)
-    h_buf = torch.empty((rows, w.h), dtype=w.torch_dtype, device=dev)
-    y_perm = torch.empty((rows, w.d), dtype=w.torch_dtype, device=dev)
-    offsets = torch.empty((w.E + 1,), **i32)
-    if ec:
-        torch.index_select(inp["x"], 0, outs["sel_token"].flatten().long(), out=x_perm[:M])
-        offsets.copy_(torch.arange(w.E + 1, dtype=torch.int32, device=dev) * C)
-    else:
-        idx = torch.empty((w.T, w.k), **i32)
-        wts = torch.empty((w.T, w.k), dtype=torch.float32, device=dev)
-        slot_row = torch.empty((w.T, w.k), **i32)
-        row_token = torch.empty((rows,), **i32)
-        moe.moe_route(cfg, inp["x"], inp["w_gate"], inp["logit_bias"], None, idx, wts, None, None,
-                      sws)
-        moe.moe_dispatch(cfg, inp["x"], idx, offsets, None, slot_row, row_token, None, x_perm, sws)
-    ffn_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(args.steps)]
-    for i in range(args.steps + args.warmup):
-        flush.zero_()
-        if i >= args.warmup:
-            ffn_ev[i - args.warmup][0].record(stream)
-        moe.moe_expert_ffn(ffn_cfg, x_perm, offsets, inp["w1"], inp["b1"], inp["w2"], inp["b2"],
-                           h_buf, y_perm, sws)
-        if i >= args.warmup:
-            ffn_ev[i - args.warmup][1].record(stream)
-    torch.cuda.synchronize()
+        assert M <= w.T * w.k
+    t_ffn = _median_event_ms(ffn, args.steps, args.warmup, flush, stream) / 1e3
     assert moe.moe_device_error(sws) == 0
-    t_ffn = statistics.median(a.elapsed_time(b) for a, b in ffn_ev) / 1e3
-    del x_perm, h_buf, y_perm
+    del ffn, sws
 
     # End to end with x and y in (pinned) host memory.  Headline: moe_forward_host, the
     # C call that takes host batches and overlaps their copies with the layer, over
@@ -515,6 +632,24 @@ def run_ours(args, world, rank, local):
     }
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, inp)
+    return line
+
+
+def run_family(args, world, rank, local, line):
+    """Adds the `workloads` map (every configuration of the layer family) to the line."""
+    import sparse_mixture_experts_61_b300 as moe
+
+    dev = torch.device("cuda", local)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    peaks = load_peaks()
+    fam = {}
+    for name in FAMILY:
+        torch.cuda.empty_cache()
+        fam[name] = family_entry(moe, WORKLOADS[name], args.steps, args.warmup, flush, stream, dev,
+                                 rank, world, peaks)
+    if line is not None:
+        line["workloads"] = fam
     return line
 
 
@@ -635,8 +770,22 @@ def run_train(args, world, rank, local):
 
 # ------------------------------------------------------------------ reference arm
 def run_reference(args, world, rank, local):
+    """The CPU oracle on rank 0; under N ranks the others join a gloo group, wait for
+    rank 0 at a barrier and return without work."""
+    if world > 1 and args is not None:
+        import torch.distributed as dist
+        dist_init(world, local, backend="gloo")
+        try:
+            return _reference_line(args, world) if rank == 0 else None
+        finally:
+            dist.barrier()
+            dist.destroy_process_group()
     if rank != 0:
         return None
+    return _reference_line(args, world)
+
+
+def _reference_line(args, world):
     import oracle
 
     w = WORKLOADS[args.workload]
@@ -696,15 +845,35 @@ def main():
                     help="skip the timed CPU-oracle sample (for quick runs)")
     ap.add_argument("--pass", dest="pass_", default="forward", choices=["forward", "train"],
                     help="forward (default) or train: forward + backward of the layer per step")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the `workloads` map of the other layer configurations")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.gpus < 1:
+        ap.error("--gpus must be at least 1")
+    if "WORLD_SIZE" not in os.environ and args.gpus > 1:
+        # One process per GPU: start N ranks of this script and return their status.
+        with socket.socket() as s:
+            s.bind(("127.0.0.1", 0))
+            port = s.getsockname()[1]
+        cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+               f"--nproc-per-node={args.gpus}", "--master-addr", "127.0.0.1", "--master-port",
+               str(port), os.path.abspath(__file__), *sys.argv[1:]]
+        sys.exit(subprocess.call(cmd))
     world, rank, local = dist_env()
+    if world != args.gpus:
+        ap.error(f"--gpus {args.gpus} does not match WORLD_SIZE={world}")
     if args.impl == "reference":
         line = run_reference(args, world, rank, local)
     else:
         dist_init(world, local)
-        line = (run_train if args.pass_ == "train" else run_ours)(args, world, rank, local)
+        if args.pass_ == "train":
+            line = run_train(args, world, rank, local)
+        else:
+            line = run_ours(args, world, rank, local)
+            if args.workload == DEFAULT_WORKLOAD and not args.no_workloads:
+                line = run_family(args, world, rank, local, line)
         if world > 1:
             import torch.distributed as dist
             dist.destroy_process_group()

@@ -37,7 +37,10 @@
  *    Problems only the GPU can see (an expert index out of range, a row index
  *    out of range, a non-finite logit, a pipeline wait that gave up) set bits
  *    in a flag word at the start of the workspace; moe_device_error reads it.
- *    Kernels never trap.  Each entry point clears the flag word first.
+ *    Kernels never trap.  Each entry point first clears the flag word and the
+ *    bookkeeping that follows it (the first 5376 bytes of the workspace; the
+ *    expert GEMMs' split-tile counters, which every completed layer leaves
+ *    zeroed again).
  *  - Supported range: 1 <= k <= 8, k <= E <= 256, d and h multiples of 8 (and
  *    at least 8), 0 <= T and T*k < 2^31.  Outside it: MOE_ERR_UNSUPPORTED.
  *  - Weights use the nn.Linear orientation [out_features, in_features] stacked
@@ -182,7 +185,9 @@ moe_status moe_workspace_size(const moe_config* cfg, size_t* bytes);
 
 /* Workspace bytes the stage calls (moe_route, moe_dispatch, moe_expert_ffn,
    moe_combine) need: the flag word, per-chunk histograms and partial sums,
-   and the [T,E] logits when moe_route is not given a logits buffer.  Host only. */
+   the [T,E] logits when moe_route is not given a logits buffer, and, when no
+   expert can get more than 128 rows (bf16), the fp32 pieces of expert-GEMM tiles
+   split between SMs (at most 20 MiB).  Host only. */
 moe_status moe_stage_workspace_size(const moe_config* cfg, size_t* bytes);
 
 /* Router (gating formula and TopKRouter.forward):
@@ -426,8 +431,12 @@ moe_status moe_selftest_wait_timeout(int32_t* device_flags, uint64_t limit_ns,
     - every call shares the array and it keeps the last call's contents; each call
       rewrites what it reads and clears the flag word, but calls whose GPU work
       overlaps (other streams, other host threads) race on it: serialise them;
-    - the array's device address is looked up on the first call made with a given
-      device current; make that first call before any stream capture begins.
+    - the array's device address is looked up by the first call made in a CUDA
+      context (the device's primary context, for runtime-API callers) and reused
+      while that context is current; a call in a new context (after
+      cudaDeviceReset, say) looks it up again.  Make the first call in a context
+      before any stream capture begins.
+   Arguments are validated exactly as moe_dispatch validates them.
    device_flags: optional [1] int32 device buffer that receives the device flag word
    (MOE_DEVERR_BAD_INDEX); NULL keeps it inside the library's array. */
 moe_status moe_dispatch_static(const moe_config* cfg, const void* x, const int32_t* topk_idx,

@@ -15,10 +15,13 @@
 // start of each call.  Calls whose work overlaps on the GPU (different streams, or
 // different host threads) race on the array and must be serialised by the caller.
 //
-// Its device address is looked up once per device (cudaGetSymbolAddress) by the
-// first call made while that device is current; make that first call before any
+// Its device address is looked up (cudaGetSymbolAddress) by the first call made in a
+// given CUDA context -- the device's primary context, for runtime-API callers -- and
+// kept for as long as that context is current: a call made in a new context (after
+// cudaDeviceReset, say) looks it up again.  Make the first call in a context before any
 // stream capture begins.
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -27,6 +30,7 @@
 
 #include "../../include/moe.h"
 #include "common.cuh"
+#include "entry.h"
 #include "kernels.h"
 
 namespace {
@@ -39,19 +43,51 @@ static __device__ __align__(256) int32_t g_dispatch_scratch[kFlagInts + 2 * kCel
 
 constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mu;
+// Per device: the address and the unique id of the context it was looked up in.
 int32_t* g_scratch_addr[kMaxDevices] = {};
+unsigned long long g_scratch_ctx[kMaxDevices] = {};
 
-// Device address of g_dispatch_scratch on the current device (looked up once).
+// Unique id of the calling thread's current context (ids are never reused within a
+// process), from the driver entry points cuCtxGetCurrent and cuCtxGetId.
+bool current_context_id(unsigned long long* id) {
+  using GetCurrent = CUresult (*)(CUcontext*);
+  using GetId = CUresult (*)(CUcontext, unsigned long long*);
+  static GetCurrent get_current = nullptr;
+  static GetId get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrent>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetId>(p);
+  });
+  CUcontext ctx = nullptr;
+  return get_current && get_id && get_current(&ctx) == CUDA_SUCCESS && ctx != nullptr &&
+         get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+// Device address of g_dispatch_scratch in the current context (looked up once per
+// context).
 moe_status scratch_address(int32_t** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_UNSUPPORTED;
+  unsigned long long ctx = 0;
+  const bool have_ctx = current_context_id(&ctx);
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (g_scratch_addr[dev] == nullptr) {
+  if (!have_ctx || g_scratch_addr[dev] == nullptr || g_scratch_ctx[dev] != ctx) {
+    // The lookup also makes the device's primary context current when no context is.
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_dispatch_scratch) != cudaSuccess || p == nullptr)
       return MOE_ERR_CUDA;
+    if (!current_context_id(&ctx)) return MOE_ERR_CUDA;
     g_scratch_addr[dev] = static_cast<int32_t*>(p);
+    g_scratch_ctx[dev] = ctx;
   }
   *out = g_scratch_addr[dev];
   return MOE_OK;
@@ -69,16 +105,10 @@ extern "C" __attribute__((visibility("default"))) moe_status moe_dispatch_static
     const moe_config* cfg, const void* x, const int32_t* topk_idx, int32_t* offsets,
     int32_t* kept_counts, int32_t* slot_row, int32_t* row_token, int32_t* dropped, void* x_perm,
     int32_t* device_flags, moe_stream_t stream) {
-  if (!cfg) return MOE_ERR_INVALID_ARGUMENT;
+  // The same validation as moe_dispatch.
+  const moe_status valid = moe::check_config(cfg);
+  if (valid != MOE_OK) return valid;
   const moe_config& c = *cfg;
-  if ((c.dtype != MOE_F32 && c.dtype != MOE_BF16) ||
-      (c.gate != MOE_GATE_TOPK_SOFTMAX && c.gate != MOE_GATE_SOFTMAX_TOPK_RENORM) ||
-      !std::isfinite(c.capacity_factor))
-    return MOE_ERR_INVALID_ARGUMENT;
-  if (c.T < 0 || c.k < 1 || c.k > moe::kMaxK || c.E < c.k || c.E > moe::kMaxExperts ||
-      c.d < 8 || c.d % 8 != 0 || c.h < 8 || c.h % 8 != 0 ||
-      c.T * static_cast<int64_t>(c.k) >= (int64_t{1} << 31))
-    return MOE_ERR_UNSUPPORTED;
   const int64_t nchunks = (c.T + moe::kChunk - 1) / moe::kChunk;
   if (nchunks * c.E > kCells) return MOE_ERR_UNSUPPORTED;  // beyond the static scratch
   if (!token_buf(c, x, 16) || !token_buf(c, topk_idx, 4) || !offsets || !aligned(offsets, 4) ||

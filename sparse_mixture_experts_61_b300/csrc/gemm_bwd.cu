@@ -48,7 +48,6 @@ template <int EPI>
 __global__ void __launch_bounds__(ROWS_THREADS, 1)
     tc_bwd_rows_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB, const GemmArgs p) {
-  pdl_enter();
   static_assert(EPI == EPI_DSILU || EPI == EPI_PLAIN, "backward epilogues");
   constexpr int BN = 256, STAGES = 4;
   constexpr uint32_t kTmemCols = 2 * BN;
@@ -58,7 +57,7 @@ __global__ void __launch_bounds__(ROWS_THREADS, 1)
   Smem& S = smem_aligned<Smem>();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.offsets ? p.G : 1;
-  pipe_prologue<Smem, STAGES, 1>(S, kTmemCols, p, G, TILE_M, &tmA, &tmB, 32 * ROWS_EPI_WARPS);
+  pipe_prologue<Smem, STAGES>(S, kTmemCols, p, G, TILE_M, &tmA, &tmB, 32 * ROWS_EPI_WARPS);
 
   const int NB = (p.N + BN - 1) / BN;
   const int total = S.pref[G] * NB;
@@ -98,7 +97,7 @@ __global__ void __launch_bounds__(ROWS_THREADS, 1)
           abort, p.flags);
   } else if (warp == 1) {
     if (lane == 0)
-      run_mma<STAGES, BN, 1, true>(S, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x),
+      run_mma<STAGES, BN, true>(S, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x),
                                    total, S.tmem_base, decode, [](const Coord&) { return kIdesc; },
                                    abort, p.flags);
   } else {
@@ -163,7 +162,7 @@ __global__ void __launch_bounds__(ROWS_THREADS, 1)
       if (acc == 0) aph ^= 1u;
     }
   }
-  pipe_teardown<1>(S, kTmemCols);
+  pipe_teardown(S, kTmemCols);
 }
 
 // ------------------------------------------------------------- weight gradients
@@ -201,7 +200,6 @@ __global__ void __launch_bounds__(WG_THREADS, 1)
                     const __grid_constant__ CUtensorMap tmAt,
                     const __grid_constant__ CUtensorMap tmBt,
                     const __grid_constant__ CUtensorMap tmO, const WgradArgs p) {
-  pdl_enter();
   constexpr uint32_t kTmemCols = 2 * WG_BN;
   constexpr uint32_t kIdesc = bf16_idesc(WG_BM, WG_BN) | kIdescAMnMajor | kIdescBMnMajor;
   constexpr uint32_t kStageBytes = (WG_BM + WG_BN) * WG_BK * 2;
@@ -231,6 +229,8 @@ __global__ void __launch_bounds__(WG_THREADS, 1)
     tmem_alloc(smem_u32(&S.tmem_base), kTmemCols);
     tmem_relinquish();
   }
+  // Nothing above touches global memory; wait for the predecessor here.
+  pdl_enter();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();

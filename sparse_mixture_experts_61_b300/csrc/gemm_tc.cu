@@ -19,21 +19,23 @@
 //  * Every wait is bounded (common.cuh); on a timeout the CTA records
 //    MOE_DEVERR_TIMEOUT, lets its own TMA copies and MMAs land, frees TMEM, returns.
 //
-// Expert GEMMs use the "weights as M" orientation: the MMA's M = 128 side is a block
-// of 128 weight rows (output features), which always fills the tile, and its N side
-// is a block of one expert's token rows, set per tile in the instruction descriptor.
-// An expert's n rows are cut into nt = ceil(n / TB) equal blocks of ceil(n / nt)
-// rows rounded up to 16, so a ragged group costs at most 15 padded token columns per
-// block.  CTAs work in clusters of two: both take the same token block and
-// neighbouring weight blocks; each loads its own 128 weight rows and half of the
-// token rows, multicasting them into both CTAs' shared memory, so a 64-deep k-block
-// moves 16 KB of weights + TB*64 B of tokens per CTA instead of 16 KB + TB*128 B.
-// A stage is released when both CTAs' MMAs have read it (each MMA commit arrives on
-// both CTAs' "empty" barriers).  Tiles are ordered (group, weight-block pair, token
-// block) so clusters running side by side read the same weight tiles, which come
-// from HBM once.  The tile list is derived on the device from the group offsets:
-// the kept-row count never goes to the host.
+// Small expert groups use the "weights as M" orientation: the MMA's M = 128 side is a
+// block of 128 weight rows (output features), which always fills the tile, and its N
+// side is a block of one expert's token rows, set per tile in the instruction
+// descriptor.  An expert's n rows are cut into nt = ceil(n / TB) equal blocks of
+// ceil(n / nt) rows rounded up to 16, so a ragged group costs at most 15 padded token
+// columns per block.  Every CTA loads its own weight rows and token rows with plain
+// TMA tile loads.  The (tile, k-block) iterations of the whole layer are divided evenly
+// over the CTAs (a stream-K split): a CTA's share may start or end inside a tile, so a
+// few tiles are computed in pieces by consecutive CTAs.  Each piece parks its fp32 sums
+// in the workspace; the CTA whose piece lands last adds the pieces in k order (a fixed
+// order, so results do not depend on timing) and runs the epilogue.  This keeps every
+// SM busy to the end whether the layer has fewer tiles than SMs (a Switch layer's
+// second GEMM: 72 tiles of 64 k-blocks) or a few more than a multiple of them.  The
+// tile list is derived on the device from the group offsets: the kept-row count never
+// goes to the host.
 //
+// Large groups use row tiles: 128 token rows x 256 weight rows, tokens as M.
 // The router keeps tokens as M (128 rows per tile) and the E experts as N.
 
 #include "tc_pipe.cuh"
@@ -43,48 +45,105 @@ namespace {
 
 // ------------------------------------------------------------- expert FFN GEMM
 // A = weight block [128 x 64] of W[g] (3-D map over [G, N, K]); B = token block of
-// up to TB rows, loaded as 32-row boxes (2-D map over [rows_alloc, K]) and shared by
-// the two CTAs of a cluster; D[128 x ntok] in TMEM, lane = output feature, column =
-// token.
+// up to TB rows, loaded as 32-row boxes (2-D map over [rows_alloc, K]); D[128 x ntok]
+// in TMEM, lane = output feature, column = token.
 constexpr int TOK_BOX = 32;
+// Fewest iterations (k-blocks) in a CTA's share of the split; a layer with fewer than
+// this many per CTA runs on fewer CTAs.
+constexpr int kMinSplitKb = 8;
+// What parking and adding up a split tile's pieces costs, in k-block iterations: the
+// split is taken only when it shortens the longest CTA's share by more than this and
+// by at least an eighth.  Measured on the Switch layer: parking a piece and counting it
+// in takes ~1 us, and the CTA that finishes a tile spends 2-4 us per 32 token columns
+// on L2 round trips, ~9 us in all, about 24-32 k-blocks of a saturated main loop (a
+// split of its 72-tile second GEMM ran 12 us slower than whole tiles on 72 SMs; on the
+// 64-token decode layer, whose second GEMM has 4.1 waves of whole tiles, it is 4.5%
+// faster).
+constexpr int kSplitCostKb = 32;
+// Pieces whose parked sums the finishing CTA loads at once.
+constexpr int kReduceBatch = 2;
+
+// The even division of `total` (tile, k-block) iterations over `parts` CTAs: CTA c
+// runs iterations [begin(c), begin(c + 1)).
+struct SplitK {
+  int64_t total;
+  int parts;
+  __device__ __forceinline__ int64_t begin(int c) const { return total * c / parts; }
+  // The CTA whose share holds iteration `it`: the largest c with begin(c) <= it, which
+  // never has an empty share.
+  __device__ __forceinline__ int owner(int64_t it) const {
+    return static_cast<int>(((it + 1) * parts + total - 1) / total - 1);
+  }
+  __device__ __forceinline__ bool busy(int c) const { return begin(c) < begin(c + 1); }
+};
 
 template <int TB, int STAGES, int EPI>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
+__global__ void __launch_bounds__(TC_THREADS, 1)
     tc_ffn_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                   const GemmArgs p) {
-  pdl_enter();
-  static_assert(TB >= TOK_BOX && TB <= 256 && (TB & (TB - 1)) == 0,
-                "TB: power of two in [32, 256]");
+  static_assert(TB >= TOK_BOX && TB <= 128 && (TB & (TB - 1)) == 0,
+                "TB: power of two in [32, 128]");
   static_assert(EPI == EPI_BIAS_SILU || EPI == EPI_BIAS, "expert epilogues only");
-  constexpr int CTAS = 2;
   constexpr uint32_t kTmemCols = 2 * TB;
   constexpr uint32_t kWeightBytes = TILE_M * TC_BK * 2;
   constexpr uint32_t kBoxBytes = TOK_BOX * TC_BK * 2;
+  constexpr int64_t kPartFloats = int64_t{TILE_M} * TB;  // one parked piece
   using Smem = PipeSmem<TILE_M * TC_BK * 2, TB * TC_BK * 2, STAGES>;
   Smem& S = smem_aligned<Smem>();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int rank = static_cast<int>(cluster_ctarank());
   const int G = p.G;
-  pipe_prologue<Smem, STAGES, CTAS>(S, kTmemCols, p, G, TB, &tmW, &tmX);
+  pipe_prologue<Smem, STAGES>(S, kTmemCols, p, G, TB, &tmW, &tmX);
 
   const int MB = (p.N + TILE_M - 1) / TILE_M;  // weight blocks per group
-  const int MP = (MB + 1) / 2;                  // weight-block pairs per group
-  const int total = S.pref[G] * MP;
   const int KB = (p.K + TC_BK - 1) / TC_BK;
-  const int first = static_cast<int>(blockIdx.x) / CTAS, step = static_cast<int>(gridDim.x) / CTAS;
+  const int64_t ntiles = static_cast<int64_t>(S.pref[G]) * MB;
+  const int grid = static_cast<int>(gridDim.x), cta = static_cast<int>(blockIdx.x);
+  SplitK sk;
+  sk.total = ntiles * KB;
+  {
+    const int64_t by_size = sk.total / kMinSplitKb;
+    sk.parts = static_cast<int>(by_size < 1 ? 1 : by_size < grid ? by_size : grid);
+  }
+  // Whole tiles round-robin (the longest share is ceil(tiles / grid) tiles), or the
+  // even split of the iterations; every CTA takes the same decision.
+  const int64_t longest_whole = (ntiles + grid - 1) / grid * KB;
+  const int64_t longest_split = (sk.total + sk.parts - 1) / sk.parts;
+  const bool split = sk.parts > 1 && longest_split + kSplitCostKb < longest_whole &&
+                     (longest_whole - longest_split) * 8 >= longest_whole;
+  int64_t it0 = 0, it1 = 0;
+  int npieces = 0;
+  if (split) {
+    it0 = cta < sk.parts ? sk.begin(cta) : 0;
+    it1 = cta < sk.parts ? sk.begin(cta + 1) : 0;
+    npieces = it1 > it0 ? static_cast<int>((it1 - 1) / KB - it0 / KB + 1) : 0;
+  } else {
+    npieces = ntiles > cta ? static_cast<int>((ntiles - cta + grid - 1) / grid) : 0;
+  }
   volatile int* abort = &S.abort;
 
   struct Coord {
     int g, n0, ntok, nbox, kb0, kb1;
     uint32_t bytes;
-    int64_t row0, row_end;
+    int64_t row0, row_end, tile;
   };
-  auto decode = [&](int tile) {
+  // Piece q of this CTA: the tile it belongs to and its k-blocks [kb0, kb1).
+  auto decode = [&](int q) {
     Coord c;
-    c.g = find_group(S.pref, G, MP, tile);
+    if (split) {
+      c.tile = it0 / KB + q;
+      const int64_t t0 = c.tile * KB;
+      c.kb0 = static_cast<int>((t0 > it0 ? t0 : it0) - t0);
+      c.kb1 = static_cast<int>((t0 + KB < it1 ? t0 + KB : it1) - t0);
+    } else {
+      c.tile = cta + static_cast<int64_t>(q) * grid;
+      c.kb0 = 0;
+      c.kb1 = KB;
+    }
+    const int tile = static_cast<int>(c.tile);
+    c.g = find_group(S.pref, G, MB, tile);
     const int nt = S.pref[c.g + 1] - S.pref[c.g];
-    const int local = tile - S.pref[c.g] * MP;
-    c.n0 = (2 * (local / nt) + rank) * TILE_M;
+    const int local = tile - S.pref[c.g] * MB;
+    c.n0 = (local / nt) * TILE_M;
     const int64_t base = p.offsets[c.g], end = p.offsets[c.g + 1];
     const int64_t bsz = (((end - base) + nt - 1) / nt + 15) & ~int64_t{15};
     c.row0 = base + (local % nt) * bsz;
@@ -92,35 +151,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
     c.ntok = static_cast<int>((c.row_end - c.row0 + 15) & ~int64_t{15});
     c.nbox = (c.ntok + TOK_BOX - 1) / TOK_BOX;
     c.bytes = kWeightBytes + static_cast<uint32_t>(c.nbox) * kBoxBytes;
-    c.kb0 = 0;
-    c.kb1 = KB;
     return c;
   };
 
   if (warp == 0) {
     if (lane == 0)
       run_producer<STAGES>(
-          S, first, step, total, decode,
+          S, 0, 1, npieces, decode,
           [&](const Coord& c, int kb, uint32_t sa, uint32_t sb, uint32_t bar) {
             tma_load_3d(sa, &tmW, bar, kb * TC_BK, c.n0, c.g);
-            for (int j = rank; j < c.nbox; j += CTAS)
-              tma_load_2d_multicast(sb + j * kBoxBytes, &tmX, bar, kb * TC_BK,
-                                    static_cast<int>(c.row0) + j * TOK_BOX, 0x3);
+            for (int j = 0; j < c.nbox; ++j)
+              tma_load_2d(sb + j * kBoxBytes, &tmX, bar, kb * TC_BK,
+                          static_cast<int>(c.row0) + j * TOK_BOX);
           },
           abort, p.flags);
   } else if (warp == 1) {
     if (lane == 0)
-      run_mma<STAGES, TB, CTAS>(
-          S, first, step, total, S.tmem_base, decode,
-          [](const Coord& c) { return bf16_idesc(TILE_M, c.ntok); }, abort, p.flags);
+      run_mma<STAGES, TB>(S, 0, 1, npieces, S.tmem_base, decode,
+                          [](const Coord& c) { return bf16_idesc(TILE_M, c.ntok); }, abort,
+                          p.flags);
   } else {
     const int quad = warp & 3;  // TMEM lanes this warp may read: 32*quad .. 32*quad+31
     int acc = 0;
     uint32_t aph = 0;
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
     const __nv_bfloat16* bias = static_cast<const __nv_bfloat16*>(p.bias);
-    for (int tile = first; tile < total; tile += step) {
-      const Coord c = decode(tile);
+    for (int q = 0; q < npieces; ++q) {
+      const Coord c = decode(q);
       const int n = c.n0 + quad * 32 + lane;
       const bool n_ok = n < p.N;
       const float b = (bias && n_ok) ? __bfloat162float(bias[static_cast<int64_t>(c.g) * p.N + n])
@@ -131,35 +188,107 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
       const uint32_t t_row = S.tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
                              static_cast<uint32_t>(acc * TB);
       const int nrows = static_cast<int>(c.row_end - c.row0);
-#pragma unroll 1
-      for (int col = 0; col < c.ntok; col += 32) {
-        float v[32];
-        tmem_ld_32cols(t_row + col, v);
-        tc_wait_ld();
-        if (n_ok) {
-          __nv_bfloat16* o = out + (c.row0 + col) * p.N + n;
+      // Bias, activation and bf16 store of feature n for token columns [col, col + 32).
+      auto store = [&](int col, const float(&v)[32]) {
+        if (!n_ok) return;
+        __nv_bfloat16* o = out + (c.row0 + col) * p.N + n;
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            if (col + i < nrows) {
-              float x = v[i] + b;
-              if (EPI == EPI_BIAS_SILU) {
-                if (p.pre_out)
-                  static_cast<__nv_bfloat16*>(p.pre_out)[(o - out) + static_cast<int64_t>(i) * p.N] =
-                      __float2bfloat16_rn(x);
-                x = silu(x);
-              }
-              o[static_cast<int64_t>(i) * p.N] = __float2bfloat16_rn(x);
+        for (int i = 0; i < 32; ++i) {
+          if (col + i < nrows) {
+            float x = v[i] + b;
+            if (EPI == EPI_BIAS_SILU) {
+              if (p.pre_out)
+                static_cast<__nv_bfloat16*>(p.pre_out)[(o - out) + static_cast<int64_t>(i) * p.N] =
+                    __float2bfloat16_rn(x);
+              x = silu(x);
             }
+            o[static_cast<int64_t>(i) * p.N] = __float2bfloat16_rn(x);
+          }
+        }
+      };
+      if (c.kb0 == 0 && c.kb1 == KB) {
+#pragma unroll 1
+        for (int col = 0; col < c.ntok; col += 32) {
+          float v[32];
+          tmem_ld_32cols(t_row + col, v);
+          tc_wait_ld();
+          store(col, v);
+        }
+        tc_fence_before();
+        mbar_arrive(smem_u32(&S.tempty[acc]));
+      } else {
+        // A piece of a split tile.  Park its sums ([token][feature] within the piece's
+        // slot: slot 1 for a tile's first piece, slot 0 for a later one; a CTA holds at
+        // most one of each), then count the piece in on the tile's counter (one per
+        // lane quadrant, indexed by the CTA holding the tile's first piece).
+        const int64_t t0 = c.tile * KB;
+        const int first = sk.owner(t0), last = sk.owner(t0 + KB - 1);
+        float* mine = p.sk_part + (static_cast<int64_t>(cta) * 2 + (c.kb0 > 0 ? 0 : 1)) * kPartFloats +
+                      quad * 32 + lane;
+#pragma unroll 1
+        for (int col = 0; col < c.ntok; col += 32) {
+          float v[32];
+          tmem_ld_32cols(t_row + col, v);
+          tc_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (col + i < nrows) mine[static_cast<int64_t>(col + i) * TILE_M] = v[i];
+        }
+        tc_fence_before();
+        mbar_arrive(smem_u32(&S.tempty[acc]));  // the accumulator is free again
+        __threadfence();
+        __syncwarp();
+        int pieces = 0;
+        for (int cc = first; cc <= last; ++cc) pieces += sk.busy(cc) ? 1 : 0;
+        int* ctr = p.sk_ctr + first * 4 + quad;
+        int arrived = 0;
+        if (lane == 0) arrived = atomicAdd(ctr, 1);
+        arrived = __shfl_sync(0xffffffffu, arrived, 0);
+        if (arrived == pieces - 1) {
+          // Every other piece has landed: add them in k order and finish the tile.
+          // The loads of kReduceBatch pieces are issued together, then added in order.
+          if (lane == 0) atomicExch(ctr, 0);  // ready for the next launch
+          __threadfence();
+#pragma unroll 1
+          for (int col = 0; col < nrows; col += 32) {
+            float v[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = 0.f;
+            bool lead = true;
+#pragma unroll 1
+            for (int cc0 = first; cc0 <= last; cc0 += kReduceBatch) {
+              float x[kReduceBatch][32];
+              bool use[kReduceBatch];
+#pragma unroll
+              for (int u = 0; u < kReduceBatch; ++u) {
+                const int cc = cc0 + u;
+                use[u] = cc <= last && sk.busy(cc);
+                const float* src =
+                    p.sk_part + (static_cast<int64_t>(cc) * 2 + (cc == first ? 1 : 0)) * kPartFloats +
+                    quad * 32 + lane;
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                  x[u][i] = (use[u] && col + i < nrows)
+                                ? __ldcg(src + static_cast<int64_t>(col + i) * TILE_M)
+                                : 0.f;
+              }
+#pragma unroll
+              for (int u = 0; u < kReduceBatch; ++u) {
+                if (!use[u]) continue;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = lead ? x[u][i] : v[i] + x[u][i];
+                lead = false;
+              }
+            }
+            store(col, v);
           }
         }
       }
-      tc_fence_before();
-      mbar_arrive(smem_u32(&S.tempty[acc]));
       acc ^= 1;
       if (acc == 0) aph ^= 1u;
     }
   }
-  pipe_teardown<CTAS>(S, kTmemCols);
+  pipe_teardown(S, kTmemCols);
 }
 
 // ------------------------------------------------------------- expert FFN, row tiles
@@ -180,7 +309,6 @@ __global__ void __launch_bounds__(ROWS_THREADS, 1)
     tc_rows_ffn_kernel(const __grid_constant__ CUtensorMap tmX,
                        const __grid_constant__ CUtensorMap tmW,
                        const __grid_constant__ CUtensorMap tmO, const GemmArgs p) {
-  pdl_enter();
   static_assert(BN % 32 == 0 && BN <= 256 && (BN & (BN - 1)) == 0, "BN: power of two, <= 256");
   static_assert(EPI == EPI_BIAS_SILU || EPI == EPI_BIAS, "expert epilogues only");
   constexpr uint32_t kTmemCols = 2 * BN;
@@ -190,7 +318,7 @@ __global__ void __launch_bounds__(ROWS_THREADS, 1)
   Smem& S = smem_aligned<Smem>();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.G;
-  pipe_prologue<Smem, STAGES, 1>(S, kTmemCols, p, G, TILE_M, &tmX, &tmW, 32 * ROWS_EPI_WARPS);
+  pipe_prologue<Smem, STAGES>(S, kTmemCols, p, G, TILE_M, &tmX, &tmW, 32 * ROWS_EPI_WARPS);
 
   const int NB = (p.N + BN - 1) / BN;
   const int total = S.pref[G] * NB;
@@ -227,7 +355,7 @@ __global__ void __launch_bounds__(ROWS_THREADS, 1)
           abort, p.flags);
   } else if (warp == 1) {
     if (lane == 0)
-      run_mma<STAGES, BN, 1>(S, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), total,
+      run_mma<STAGES, BN>(S, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), total,
                              S.tmem_base, decode, [](const Coord&) { return kIdesc; }, abort,
                              p.flags);
   } else {
@@ -364,7 +492,7 @@ __global__ void __launch_bounds__(ROWS_THREADS, 1)
     }
     if (lane == 0) bulk_wait_group0();
   }
-  pipe_teardown<1>(S, kTmemCols);
+  pipe_teardown(S, kTmemCols);
 }
 
 // ------------------------------------------------------------- router GEMM
@@ -377,7 +505,6 @@ template <int BN, int STAGES>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     tc_router_kernel(const __grid_constant__ CUtensorMap tmX,
                      const __grid_constant__ CUtensorMap tmW, const GemmArgs p) {
-  pdl_enter();
   static_assert(BN >= 16 && BN <= 256 && (BN & (BN - 1)) == 0, "BN: power of two in [16, 256]");
   constexpr uint32_t kTmemCols = (2 * BN < 32) ? 32 : 2 * BN;
   constexpr uint32_t kIdesc = bf16_idesc(TILE_M, BN);
@@ -386,7 +513,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   using Smem = PipeSmem<TILE_M * TC_BK * 2, BN * TC_BK * 2, STAGES>;
   Smem& S = smem_aligned<Smem>();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  pipe_prologue<Smem, STAGES, 1>(S, kTmemCols, p, 1, TILE_M, &tmX, &tmW);
+  pipe_prologue<Smem, STAGES>(S, kTmemCols, p, 1, TILE_M, &tmX, &tmW);
 
   const int NB = (p.N + BN - 1) / BN;
   const int MT = S.pref[1];
@@ -424,7 +551,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           abort, p.flags);
   } else if (warp == 1) {
     if (lane == 0)
-      run_mma<STAGES, BN, 1>(S, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), total,
+      run_mma<STAGES, BN>(S, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), total,
                              S.tmem_base, decode, [](const Coord&) { return kIdesc; }, abort,
                              p.flags);
   } else {
@@ -469,29 +596,21 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       if (acc == 0) aph ^= 1u;
     }
   }
-  pipe_teardown<1>(S, kTmemCols);
+  pipe_teardown(S, kTmemCols);
 }
 
 template <int TB, int STAGES, int EPI>
 cudaError_t launch_ffn(const GemmArgs& a, int sm_count, cudaStream_t stream) {
+  if (!a.sk_ctr || !a.sk_part) return cudaErrorInvalidValue;
   CUtensorMap tmW, tmX;
   if (!stacked_map(&tmW, a.B, a.G, a.N, a.K, TILE_M) ||
       !rows_map(&tmX, a.A, a.rows_alloc, a.K, TOK_BOX))
     return cudaErrorInvalidValue;
   using Smem = PipeSmem<TILE_M * TC_BK * 2, TB * TC_BK * 2, STAGES>;
-  const size_t smem = sizeof(Smem) + 1024;
-  auto kern = tc_ffn_kernel<TB, STAGES, EPI>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
-  if (e != cudaSuccess) return e;
-  // Upper bound on tile pairs: sum_g ceil(rows_g / TB) <= rows_alloc / TB + G.
-  const int64_t bound =
-      ((a.rows_alloc + TB - 1) / TB + a.G) * (((a.N + TILE_M - 1) / TILE_M + 1) / 2);
-  const int64_t clusters =
-      std::min<int64_t>(bound, resident_clusters(kern, smem, sm_count));
-  if (clusters <= 0) return cudaSuccess;
-  launch_pdl(kern, static_cast<unsigned>(2 * clusters), TC_THREADS, smem, stream, tmW, tmX, a);
-  return cudaGetLastError();
+  // One CTA per SM; the parked pieces and counters are sized for kMaxSmsForSizing.
+  const int grid = std::min(sm_count, kMaxSmsForSizing);
+  return launch_pipe(tc_ffn_kernel<TB, STAGES, EPI>, sizeof(Smem) + 1024, grid, tmW, tmX, a,
+                     stream);
 }
 
 template <int BN, int STAGES, int EPI>
@@ -527,20 +646,18 @@ cudaError_t launch_router(const GemmArgs& a, int sm_count, cudaStream_t stream) 
   return launch_pipe(tc_router_kernel<BN, STAGES>, sizeof(Smem) + 1024, grid, tmX, tmW, a, stream);
 }
 
-// Token-block height for an expert GEMM: the smallest power of two (32..256) that
-// holds the largest group the routing can produce.
+// Token-block height for a weights-as-M expert GEMM: the smallest power of two
+// (32..128) that holds the largest group the routing can produce.
 template <int EPI>
 cudaError_t launch_ffn_for(const GemmArgs& a, int max_group, int sm_count, cudaStream_t stream) {
   if (max_group <= 32) return launch_ffn<32, 11, EPI>(a, sm_count, stream);
   if (max_group <= 64) return launch_ffn<64, 9, EPI>(a, sm_count, stream);
-  if (max_group <= 128) return launch_ffn<128, 7, EPI>(a, sm_count, stream);
-  return launch_ffn<256, 4, EPI>(a, sm_count, stream);
+  return launch_ffn<128, 7, EPI>(a, sm_count, stream);
 }
 
-// Largest expert group (rows) for which the weights-as-M cluster kernel is used:
-// there a 128-row tile would be mostly padding, while 128 weight rows always fill
-// the MMA's M side.  Larger groups use row tiles, whose main loop measured faster.
-constexpr int kSmallGroup = 128;
+// kSmallGroup (kernels.h) bounds the groups of the weights-as-M kernel: there a
+// 128-row tile would be mostly padding, while 128 weight rows always fill the MMA's M
+// side.  Larger groups use row tiles, whose main loop measured faster.
 
 // Router tile width for E experts: the narrowest power of two that covers them, at
 // most 128.

@@ -153,7 +153,9 @@ MOE_EXPORT moe_status moe_forward_host(const moe_config* cfg, int32_t routing,
   if ((s = run_layer(cfg, routing, *weights, ws, L, 0, st, moe::EntryMode::kValidate)) != MOE_OK)
     return s;
 
-  HP_CUDA(cudaMemsetAsync(ws, 0, sizeof(int32_t), st));  // the flag word, once
+  // The flag word and the expert GEMMs' split counters, once: the counters are left
+  // zeroed by every layer that completes.
+  HP_CUDA(cudaMemsetAsync(ws, 0, moe::kFlagRegionBytes, st));
   if (T == 0) {
     if (b->aux_loss)
       for (int64_t i = 0; i < b->n; ++i) b->aux_loss[i] = 0.f;

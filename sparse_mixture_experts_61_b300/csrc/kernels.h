@@ -88,6 +88,11 @@ struct GemmArgs {
   // Backward: EPI_DSILU multiplies by SiLU'(aux_in[row, n]) (the saved pre-activation).
   const void* aux_in;
   int64_t b_rows;  // backward B [G][b_rows][N] when b_rows differs from K (rows past it read 0)
+  // Weights-as-M expert GEMM (groups <= 128 rows), whose (tile, k-block) iterations are
+  // split evenly over the CTAs: kSplitCounters zeroed ints (left zeroed again) and
+  // split_part_floats(max_group) floats for the pieces of split tiles.
+  int* sk_ctr;
+  float* sk_part;
 };
 
 // K splits of the bf16 router contraction for T tokens, E experts, model width d on a
@@ -96,6 +101,20 @@ struct GemmArgs {
 // can bound it with an upper limit on the SM count.
 int router_splits(int64_t T, int E, int d, int sms);
 constexpr int kMaxSmsForSizing = 160;
+
+// Largest expert group (rows) for which the expert GEMMs use the weights-as-M kernel
+// (token tiles of 32, 64 or 128 rows); larger groups use 128-row tiles of tokens.
+constexpr int kSmallGroup = 128;
+// Counters of the weights-as-M expert GEMM's split tiles: one per (CTA, TMEM lane
+// quadrant).  Each GEMM of a layer has its own set.
+constexpr int kSplitCounters = 4 * kMaxSmsForSizing;
+// Floats for the parked pieces of that GEMM's split tiles: two [128 x token tile]
+// pieces per CTA; none when the groups are too large for that kernel.
+inline int64_t split_part_floats(int64_t max_group) {
+  if (max_group > kSmallGroup) return 0;
+  const int64_t tb = max_group <= 32 ? 32 : max_group <= 64 ? 64 : 128;
+  return int64_t{kMaxSmsForSizing} * 2 * 128 * tb;
+}
 
 enum Epilogue {
   EPI_BIAS_SILU = 0,

@@ -46,11 +46,20 @@ size_t align_up(size_t v) { return (v + kAlign - 1) & ~(kAlign - 1); }
 // router output region holds the [T,E] fp32 logits (fp32 layers) or the K-split
 // partial sums of the bf16 router GEMM.
 struct Layout {
-  size_t flags, hist, chunk_base, psum, logits, stage_end;
+  size_t flags, split_ctr, hist, chunk_base, psum, logits, split_part, stage_end;
   size_t idx, w, counts, aux, offsets, kept, slot_row, row_token, dropped, x_perm, h_buf, y_perm;
   size_t total;
   int64_t nchunks;
 };
+
+int64_t capacity_of(const moe_config& c);
+
+// Largest expert group a valid top-k routing can produce: T (one row per token), or C
+// under a capacity below T.
+int64_t max_group_of(const moe_config& c) {
+  const int64_t C = capacity_of(c);
+  return C >= 0 && C < c.T ? C : c.T;
+}
 
 Layout make_layout(const moe_config& c) {
   Layout L{};
@@ -59,12 +68,15 @@ Layout make_layout(const moe_config& c) {
   L.nchunks = (T + kChunk - 1) / kChunk;
   size_t o = 0;
   L.flags = o; o += kAlign;
+  L.split_ctr = o; o = align_up(o + 2 * kSplitCounters * sizeof(int));
   L.hist = o; o = align_up(o + L.nchunks * E * 4);
   L.chunk_base = o; o = align_up(o + L.nchunks * E * 4);
   L.psum = o; o = align_up(o + L.nchunks * E * 4);
   const int64_t splits =
       c.dtype == MOE_BF16 ? router_splits(c.T, c.E, c.d, kMaxSmsForSizing) : 1;
   L.logits = o; o = align_up(o + splits * T * E * 4);
+  L.split_part = o;
+  if (c.dtype == MOE_BF16) o = align_up(o + split_part_floats(max_group_of(c)) * 4);
   L.stage_end = o;
   L.idx = o; o = align_up(o + T * k * 4);
   L.w = o; o = align_up(o + T * k * 4);
@@ -81,7 +93,12 @@ Layout make_layout(const moe_config& c) {
   L.total = o;
   return L;
 }
+static_assert(kAlign + 2 * kSplitCounters * sizeof(int) == kFlagRegionBytes,
+              "the flag word and the split counters open every forward workspace");
 
+}  // namespace
+
+// Shared with moe_dispatch_static (entry.h).
 moe_status check_config(const moe_config* c) {
   if (!c) return MOE_ERR_INVALID_ARGUMENT;
   if (c->dtype != MOE_F32 && c->dtype != MOE_BF16) return MOE_ERR_INVALID_ARGUMENT;
@@ -96,6 +113,8 @@ moe_status check_config(const moe_config* c) {
   if (c->T * static_cast<int64_t>(c->k) >= (int64_t{1} << 31)) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }
+
+namespace {
 
 int64_t capacity_of(const moe_config& c) {
   if (!(c.capacity_factor > 0.0)) return -1;
@@ -186,11 +205,13 @@ moe_status run_router(const moe_config& c, const Layout& L, void* ws, const void
 
 // G1 + G2 over the expert-contiguous rows: `rows_alloc` rows in the buffers, no
 // expert with more than `max_group` rows.
+// sk_ctr: the two GEMMs' split counters (2 * kSplitCounters zeroed ints); sk_part:
+// split_part_floats(max_group) floats.
 moe_status run_expert_ffn_rows(const moe_config& c, int64_t rows_alloc, int64_t max_group,
                                const void* x_perm, const int32_t* offsets, const void* w1,
                                const void* b1, const void* w2, const void* b2, void* h_buf,
-                               void* y_perm, int* flags, int sms, cudaStream_t st,
-                               void* h_pre = nullptr) {
+                               void* y_perm, int* flags, int* sk_ctr, float* sk_part, int sms,
+                               cudaStream_t st, void* h_pre = nullptr) {
   GemmArgs g1{};
   g1.A = x_perm;
   g1.pre_out = h_pre;
@@ -204,7 +225,10 @@ moe_status run_expert_ffn_rows(const moe_config& c, int64_t rows_alloc, int64_t 
   g1.K = c.d;
   g1.max_group = static_cast<int>(max_group);
   g1.flags = flags;
+  g1.sk_ctr = sk_ctr;
+  g1.sk_part = sk_part;
   GemmArgs g2 = g1;
+  g2.sk_ctr = sk_ctr + kSplitCounters;
   g2.A = h_buf;
   g2.pre_out = nullptr;
   g2.B = w2;
@@ -224,20 +248,21 @@ moe_status run_expert_ffn_rows(const moe_config& c, int64_t rows_alloc, int64_t 
 
 // Top-k routing: a valid routing gives an expert at most T rows (one per token), and
 // at most C with a capacity; the tile height follows this bound.
-moe_status run_expert_ffn(const moe_config& c, const void* x_perm, const int32_t* offsets,
-                          const void* w1, const void* b1, const void* w2, const void* b2,
-                          void* h_buf, void* y_perm, int* flags, int sms, cudaStream_t st,
-                          void* h_pre = nullptr) {
-  const int64_t C = capacity_of(c);
-  return run_expert_ffn_rows(c, c.T * c.k, C >= 0 && C < c.T ? C : c.T, x_perm, offsets, w1, b1,
-                             w2, b2, h_buf, y_perm, flags, sms, st, h_pre);
+moe_status run_expert_ffn(const moe_config& c, const Layout& L, void* ws, const void* x_perm,
+                          const int32_t* offsets, const void* w1, const void* b1, const void* w2,
+                          const void* b2, void* h_buf, void* y_perm, int* flags, int sms,
+                          cudaStream_t st, void* h_pre = nullptr) {
+  return run_expert_ffn_rows(c, c.T * c.k, max_group_of(c), x_perm, offsets, w1, b1, w2, b2, h_buf,
+                             y_perm, flags, at<int>(ws, L.split_ctr), at<float>(ws, L.split_part),
+                             sms, st, h_pre);
 }
 
 // ---------------------------------------------------------------- expert choice
 // Workspace: [flags | router output | probs [E,T] | row map [E,T] | offsets |
 // sel_token | sel_w | token rows x_perm, h_buf, y_perm of E*C rows].
 struct EcLayout {
-  size_t flags, logits, probs_et, rowmap, offsets, sel_token, sel_w, x_perm, h_buf, y_perm, total;
+  size_t flags, split_ctr, logits, probs_et, rowmap, offsets, sel_token, sel_w, split_part, x_perm,
+      h_buf, y_perm, total;
   int64_t C;
 };
 
@@ -268,6 +293,7 @@ EcLayout make_ec_layout(const moe_config& c) {
   const int64_t rows = E * L.C;
   size_t o = 0;
   L.flags = o; o += kAlign;
+  L.split_ctr = o; o = align_up(o + 2 * kSplitCounters * sizeof(int));
   const int64_t splits =
       c.dtype == MOE_BF16 ? router_splits(c.T, c.E, c.d, kMaxSmsForSizing) : 1;
   L.logits = o; o = align_up(o + splits * T * E * 4);
@@ -276,6 +302,8 @@ EcLayout make_ec_layout(const moe_config& c) {
   L.offsets = o; o = align_up(o + (E + 1) * 4);
   L.sel_token = o; o = align_up(o + rows * 4);
   L.sel_w = o; o = align_up(o + rows * 4);
+  L.split_part = o;
+  if (c.dtype == MOE_BF16) o = align_up(o + split_part_floats(L.C) * 4);
   L.x_perm = o; o = align_up(o + rows * c.d * s);
   L.h_buf = o; o = align_up(o + rows * c.h * s);
   L.y_perm = o; o = align_up(o + rows * c.d * s);
@@ -346,7 +374,7 @@ MOE_EXPORT moe_status moe_route(const moe_config* cfg, const void* x, const void
   if (!ws || !al16(ws) || ws_bytes < L.stage_end) return MOE_ERR_WORKSPACE;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   int* flags = at<int>(ws, L.flags);
-  MOE_CUDA(cudaMemsetAsync(flags, 0, sizeof(int), st));
+  MOE_CUDA(cudaMemsetAsync(ws, 0, kFlagRegionBytes, st));
   if (c.T == 0) {
     if ((s = zero_async(counts, sizeof(int32_t) * c.E, st)) != MOE_OK) return s;
     if ((s = zero_async(routing_stats, sizeof(float) * MOE_ROUTING_STATS, st)) != MOE_OK) return s;
@@ -378,7 +406,7 @@ MOE_EXPORT moe_status moe_dispatch(const moe_config* cfg, const void* x, const i
   if (!ws || !al16(ws) || ws_bytes < L.stage_end) return MOE_ERR_WORKSPACE;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   int* flags = at<int>(ws, L.flags);
-  MOE_CUDA(cudaMemsetAsync(flags, 0, sizeof(int), st));
+  MOE_CUDA(cudaMemsetAsync(ws, 0, kFlagRegionBytes, st));
   if (c.T == 0) {
     if ((s = zero_async(offsets, sizeof(int32_t) * (c.E + 1), st)) != MOE_OK) return s;
     if ((s = zero_async(kept_counts, sizeof(int32_t) * c.E, st)) != MOE_OK) return s;
@@ -409,11 +437,11 @@ MOE_EXPORT moe_status moe_expert_ffn(const moe_config* cfg, const void* x_perm,
   if (!ws || !al16(ws) || ws_bytes < L.stage_end) return MOE_ERR_WORKSPACE;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   int* flags = at<int>(ws, L.flags);
-  MOE_CUDA(cudaMemsetAsync(flags, 0, sizeof(int), st));
+  MOE_CUDA(cudaMemsetAsync(ws, 0, kFlagRegionBytes, st));
   if (c.T == 0) return MOE_OK;
   const int sms = sm_count();
   if (sms <= 0) return MOE_ERR_CUDA;
-  return run_expert_ffn(c, x_perm, offsets, w1, b1, w2, b2, h_buf, y_perm, flags, sms, st);
+  return run_expert_ffn(c, L, ws, x_perm, offsets, w1, b1, w2, b2, h_buf, y_perm, flags, sms, st);
 }
 
 MOE_EXPORT moe_status moe_combine(const moe_config* cfg, const void* y_perm,
@@ -428,7 +456,7 @@ MOE_EXPORT moe_status moe_combine(const moe_config* cfg, const void* y_perm,
   if (!ws || !al16(ws) || ws_bytes < L.stage_end) return MOE_ERR_WORKSPACE;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   int* flags = at<int>(ws, L.flags);
-  MOE_CUDA(cudaMemsetAsync(flags, 0, sizeof(int), st));
+  MOE_CUDA(cudaMemsetAsync(ws, 0, kFlagRegionBytes, st));
   if (c.T == 0) return MOE_OK;
   MOE_CUDA(launch_combine(c.dtype, y_perm, slot_row, topk_w, c.T, c.d, c.k, y, flags, st));
   return MOE_OK;
@@ -452,7 +480,7 @@ moe_status moe::forward_entry(const moe_config* cfg, const moe_forward_args* a, 
   if (!ws || !al16(ws) || ws_bytes < L.total) return MOE_ERR_WORKSPACE;
   if (mode == EntryMode::kValidate) return MOE_OK;
   int* flags = at<int>(ws, L.flags);
-  if (mode == EntryMode::kRun) MOE_CUDA(cudaMemsetAsync(flags, 0, sizeof(int), st));
+  if (mode == EntryMode::kRun) MOE_CUDA(cudaMemsetAsync(ws, 0, kFlagRegionBytes, st));
   int32_t* idx = a->topk_idx ? a->topk_idx : at<int32_t>(ws, L.idx);
   float* w = a->topk_w ? a->topk_w : at<float>(ws, L.w);
   int32_t* counts = a->counts ? a->counts : at<int32_t>(ws, L.counts);
@@ -496,8 +524,8 @@ moe_status moe::forward_entry(const moe_config* cfg, const moe_forward_args* a, 
   }
   {
     MOE_TRACE("moe_forward: expert_ffn");
-    if ((s = run_expert_ffn(c, x_perm, offsets, a->w1, a->b1, a->w2, a->b2, h_buf, y_perm, flags,
-                            sms, st, a->h_pre)) != MOE_OK)
+    if ((s = run_expert_ffn(c, L, ws, x_perm, offsets, a->w1, a->b1, a->w2, a->b2, h_buf, y_perm,
+                            flags, sms, st, a->h_pre)) != MOE_OK)
       return s;
   }
   {
@@ -555,7 +583,7 @@ moe_status moe::ec_forward_entry(const moe_config* cfg, const moe_expert_choice_
   if (!ws || !al16(ws) || ws_bytes < L.total) return MOE_ERR_WORKSPACE;
   if (mode == EntryMode::kValidate) return MOE_OK;
   int* flags = at<int>(ws, L.flags);
-  if (mode == EntryMode::kRun) MOE_CUDA(cudaMemsetAsync(flags, 0, sizeof(int), st));
+  if (mode == EntryMode::kRun) MOE_CUDA(cudaMemsetAsync(ws, 0, kFlagRegionBytes, st));
   if ((s = zero_async(a->unrouted, sizeof(int32_t), st)) != MOE_OK) return s;
   if (c.T == 0) return MOE_OK;
   const int sms = sm_count();
@@ -601,7 +629,8 @@ moe_status moe::ec_forward_entry(const moe_config* cfg, const moe_expert_choice_
   MOE_CUDA(launch_ec_select(probs_et, c.T, c.E, C, sel_token, sel_w, rowmap, offsets, st));
   MOE_CUDA(launch_gather_rows(c.dtype, sel_token, offsets, c.E, a->x, x_perm, c.d, c.E * C, st));
   if ((s = run_expert_ffn_rows(c, c.E * C, C, x_perm, offsets, a->w1, a->b1, a->w2, a->b2, h_buf,
-                               y_perm, flags, sms, st)) != MOE_OK)
+                               y_perm, flags, at<int>(ws, L.split_ctr),
+                               at<float>(ws, L.split_part), sms, st)) != MOE_OK)
     return s;
   // EC3: per-token combine over the experts that took the token.
   MOE_CUDA(launch_ec_combine(c.dtype, y_perm, rowmap, probs_et, c.T, c.E, C, c.d, a->y,

@@ -46,19 +46,18 @@ __device__ __forceinline__ void mbar_wait_unwind(uint32_t bar, uint32_t parity) 
     if (global_ns() - t0 > kWaitLimitNs) return;
 }
 
-// Barrier set-up, TMEM allocation and the per-group prefix of ceil(rows_g / unit)
-// (rows_g from the offsets, or m_rows for a single dense group).  All threads call.
-// CTAS = CTAs per cluster whose MMAs read (and so must release) each stage.
-template <class Smem, int STAGES, int CTAS>
-__device__ __forceinline__ void pipe_prologue(Smem& S, uint32_t tmem_cols, const GemmArgs& p,
-                                              int G, int unit, const void* tmA,
-                                              const void* tmB, uint32_t epi_threads = 128) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+// Set-up that touches no global memory, so it runs before the kernel waits for its
+// predecessor in the stream: barrier initialisation, tensor-map prefetch and TMEM
+// allocation.  All threads call.
+template <class Smem, int STAGES>
+__device__ __forceinline__ void pipe_setup(Smem& S, uint32_t tmem_cols, const void* tmA,
+                                           const void* tmB, uint32_t epi_threads = 128) {
+  const int warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
 #pragma unroll
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(smem_u32(&S.full[s]), 1);
-      mbar_init(smem_u32(&S.empty[s]), CTAS);
+      mbar_init(smem_u32(&S.empty[s]), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&S.tfull[i]), 1);
@@ -74,32 +73,66 @@ __device__ __forceinline__ void pipe_prologue(Smem& S, uint32_t tmem_cols, const
     tmem_alloc(smem_u32(&S.tmem_base), tmem_cols);
     tmem_relinquish();
   }
+}
+
+// After the grid-dependency wait: the per-group prefix of ceil(rows_g / unit) (rows_g
+// from the offsets, or m_rows for a single dense group), then the CTA-wide barrier that
+// publishes it together with the set-up.  All threads call.  Every offset is loaded
+// before any is used, so the prefix costs one memory latency, not one per 32 groups.
+template <class Smem>
+__device__ __forceinline__ void pipe_prefix(Smem& S, const GemmArgs& p, int G, int unit) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (warp == 0) {
+    constexpr int kChunks = kMaxExperts / 32;
+    int units[kChunks];
+    if (p.offsets) {
+      int lo[kChunks], hi[kChunks];
+#pragma unroll
+      for (int i = 0; i < kChunks; ++i) {
+        const int g = i * 32 + lane;
+        lo[i] = g < G ? p.offsets[g] : 0;
+        hi[i] = g < G ? p.offsets[g + 1] : 0;
+      }
+#pragma unroll
+      for (int i = 0; i < kChunks; ++i) {
+        const int64_t rows = static_cast<int64_t>(hi[i]) - lo[i];
+        units[i] = rows > 0 ? static_cast<int>((rows + unit - 1) / unit) : 0;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < kChunks; ++i)
+        units[i] = (i == 0 && lane == 0 && G >= 1 && p.m_rows > 0)
+                       ? static_cast<int>((p.m_rows + unit - 1) / unit)
+                       : 0;
+    }
     int carry = 0;
     if (lane == 0) S.pref[0] = 0;
-    for (int base = 0; base < G; base += 32) {
-      const int g = base + lane;
-      int units = 0;
-      if (g < G) {
-        const int64_t rows = p.offsets ? (p.offsets[g + 1] - p.offsets[g]) : p.m_rows;
-        units = rows > 0 ? static_cast<int>((rows + unit - 1) / unit) : 0;
-      }
-      int v = units;
+#pragma unroll
+    for (int i = 0; i < kChunks; ++i) {
+      int v = units[i];
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int n = __shfl_up_sync(0xffffffffu, v, o);
         if (lane >= o) v += n;
       }
+      const int g = i * 32 + lane;
       if (g < G) S.pref[g + 1] = carry + v;
       carry += __shfl_sync(0xffffffffu, v, 31);
     }
   }
   tc_fence_before();
-  if (CTAS > 1)
-    cluster_sync_all();  // peers' barriers are initialised before anyone multicasts
-  else
-    __syncthreads();
+  __syncthreads();
   tc_fence_after();
+}
+
+// The whole prologue: set-up, grid-dependency wait, prefix.  All threads call.
+template <class Smem, int STAGES>
+__device__ __forceinline__ void pipe_prologue(Smem& S, uint32_t tmem_cols, const GemmArgs& p,
+                                              int G, int unit, const void* tmA,
+                                              const void* tmB, uint32_t epi_threads = 128) {
+  pipe_setup<Smem, STAGES>(S, tmem_cols, tmA, tmB, epi_threads);
+  pdl_enter();
+  pipe_prefix(S, p, G, unit);
 }
 
 // Group of a tile: the g with pref[g]*per <= tile < pref[g+1]*per.
@@ -148,11 +181,9 @@ __device__ __forceinline__ void run_producer(Smem& S, int first, int step, int t
 }
 
 // Warp 1, lane 0.  decode(tile) -> coordinates with the k-block range [.kb0, .kb1);
-// idesc_of(coords) -> instruction descriptor of the tile's MMAs.  With CTAS = 2 each
-// stage is released on both CTAs of the cluster.  B_MN: the B stage holds MN-major
-// boxes of [64 K rows x 64 N] (8 KB apart) instead of one K-major box.
-template <int STAGES, int ACC_COLS, int CTAS, bool B_MN = false, class Smem, class Decode,
-          class Idesc>
+// idesc_of(coords) -> instruction descriptor of the tile's MMAs.  B_MN: the B stage
+// holds MN-major boxes of [64 K rows x 64 N] (8 KB apart) instead of one K-major box.
+template <int STAGES, int ACC_COLS, bool B_MN = false, class Smem, class Decode, class Idesc>
 __device__ __forceinline__ void run_mma(Smem& S, int first, int step, int total,
                                         uint32_t tmem_base, Decode decode, Idesc idesc_of,
                                         volatile int* abort, int* flags) {
@@ -182,10 +213,7 @@ __device__ __forceinline__ void run_mma(Smem& S, int first, int step, int total,
                          : sw128_kmajor_desc(b0 + kk * 32),
                     idesc, (kb != c.kb0 || kk != 0) ? 1u : 0u);
       issued_any = true;
-      if (CTAS > 1)
-        tc_commit_multicast(smem_u32(&S.empty[s]), static_cast<uint16_t>((1u << CTAS) - 1u));
-      else
-        tc_commit(smem_u32(&S.empty[s]));
+      tc_commit(smem_u32(&S.empty[s]));
       if (++s == STAGES) {
         s = 0;
         ph ^= 1u;
@@ -204,9 +232,7 @@ __device__ __forceinline__ void run_mma(Smem& S, int first, int step, int total,
   }
 }
 
-// With CTAS > 1 no CTA leaves before its peer has stopped writing into its shared
-// memory (multicast copies, commit arrivals).
-template <int CTAS, class Smem>
+template <class Smem>
 __device__ __forceinline__ void pipe_teardown(Smem& S, uint32_t tmem_cols) {
   tc_fence_before();
   __syncthreads();
@@ -215,7 +241,6 @@ __device__ __forceinline__ void pipe_teardown(Smem& S, uint32_t tmem_cols) {
     tc_fence_after();
     tmem_dealloc(S.tmem_base, tmem_cols);
   }
-  if (CTAS > 1) cluster_sync_all();
 }
 
 template <class Smem>
@@ -282,26 +307,6 @@ cudaError_t launch_pipe(Kern kern, size_t smem, int grid, const CUtensorMap& a,
   if (e != cudaSuccess) return e;
   launch_pdl(kern, grid, threads, smem, stream, a, b, args);
   return cudaGetLastError();
-}
-
-// Clusters of two that can be resident at once (one CTA per SM), per device.
-template <class Kern>
-int resident_clusters(Kern kern, size_t smem, int sm_count) {
-  static int cached[64] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return sm_count / 2;
-  if (cached[dev] > 0) return cached[dev];
-  int n = 0;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(sm_count / 2 * 2));
-  cfg.blockDim = dim3(TC_THREADS);
-  cfg.dynamicSmemBytes = smem;
-  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
-    (void)cudaGetLastError();
-    n = sm_count / 2;
-  }
-  cached[dev] = n;
-  return n;
 }
 
 }  // namespace

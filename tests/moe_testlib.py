@@ -122,6 +122,23 @@ def topk_gaps(lg: np.ndarray, k: int) -> np.ndarray:
     return s[:, k - 1] - s[:, k]
 
 
+def check_routing_exact(g, ref, tol_w=TOL_W):
+    """Every routing and indexing output of the GPU (``g``, host arrays) equal to the
+    oracle's routing stages run on the GPU's own logits (``ref``); gate weights, the
+    balance loss and the routing statistics within their tolerances."""
+    np.testing.assert_array_equal(g["topk_idx"], ref["idx"])
+    np.testing.assert_array_equal(g["counts"], ref["counts"])
+    np.testing.assert_array_equal(g["kept_counts"], ref["kept"])
+    np.testing.assert_array_equal(g["offsets"], ref["offsets"])
+    np.testing.assert_array_equal(g["slot_row"], ref["slot_row"])
+    np.testing.assert_array_equal(g["row_token"], ref["row_token"])
+    assert int(g["dropped"][0]) == ref["dropped"]
+    assert float(np.abs(g["topk_w"] - ref["w"]).max()) <= tol_w
+    assert abs(float(g["aux_loss"][0]) - ref["aux"]) <= TOL_AUX * abs(ref["aux"])
+    st = oracle.routing_stats(ref["counts"])
+    np.testing.assert_allclose(g["routing_stats"], st, rtol=TOL_STATS, atol=1e-7)
+
+
 def max_rel_err(a: np.ndarray, ref: np.ndarray) -> float:
     scale = float(np.abs(ref).max())
     return float(np.abs(a - ref).max()) / (scale if scale > 0 else 1.0)

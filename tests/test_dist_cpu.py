@@ -55,3 +55,32 @@ def test_two_gloo_ranks_take_the_slowest_time_and_distinct_batches():
     assert res[0]["distinct"] and res[1]["distinct"]
     assert res[1]["ref_none"]                        # the reference arm runs on rank 0 only
     assert res[0]["value"] == pytest.approx(2 * 256 / 2e-3)
+
+
+def test_bench_gpus_flag_starts_that_many_ranks():
+    """`bench.py --gpus 2` without a launcher starts two ranks itself (torch.distributed.run
+    on 127.0.0.1); on CPU the reference arm joins a gloo group, rank 0 alone prints the
+    line, and it reports both ranks."""
+    import json
+    import subprocess
+
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    for k in ("WORLD_SIZE", "RANK", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT"):
+        env.pop(k, None)
+    p = subprocess.run([sys.executable, "bench.py", "--gpus", "2", "--impl", "reference",
+                        "--workload", "tiny_f32", "--steps", "3", "--warmup", "3"], cwd=ROOT,
+                       env=env, capture_output=True, text=True, timeout=600)
+    assert p.returncode == 0, p.stderr[-2000:]
+    lines = [ln for ln in p.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, p.stdout
+    r = json.loads(lines[0])
+    assert r["n_gpus"] == 2 and r["impl"] == "reference" and r["steps"] == 3
+
+
+def test_bench_gpus_flag_must_match_the_launcher():
+    import subprocess
+
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="", WORLD_SIZE="1", RANK="0", LOCAL_RANK="0")
+    p = subprocess.run([sys.executable, "bench.py", "--gpus", "2", "--impl", "reference"],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=300)
+    assert p.returncode != 0 and "WORLD_SIZE" in p.stderr

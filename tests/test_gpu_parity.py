@@ -29,18 +29,7 @@ def _built():
     moe.lib()
 
 
-def check_routing_exact(g, ref, tol_w=tl.TOL_W):
-    np.testing.assert_array_equal(g["topk_idx"], ref["idx"])
-    np.testing.assert_array_equal(g["counts"], ref["counts"])
-    np.testing.assert_array_equal(g["kept_counts"], ref["kept"])
-    np.testing.assert_array_equal(g["offsets"], ref["offsets"])
-    np.testing.assert_array_equal(g["slot_row"], ref["slot_row"])
-    np.testing.assert_array_equal(g["row_token"], ref["row_token"])
-    assert int(g["dropped"][0]) == ref["dropped"]
-    assert float(np.abs(g["topk_w"] - ref["w"]).max()) <= tol_w
-    assert abs(float(g["aux_loss"][0]) - ref["aux"]) <= tl.TOL_AUX * abs(ref["aux"])
-    st = oracle.routing_stats(ref["counts"])
-    np.testing.assert_allclose(g["routing_stats"], st, rtol=tl.TOL_STATS, atol=1e-7)
+check_routing_exact = tl.check_routing_exact
 
 
 @pytest.mark.parametrize("name", list(PARITY_WORKLOADS))
@@ -205,12 +194,49 @@ EDGE = [
     Workload("tight_capacity_k2", T=300, d=128, h=128, E=8, k=2, dtype="bf16", gate=1,
              capacity_factor=0.5, logit_bias="normal1.5"),
     Workload("narrow_d8", T=77, d=8, h=16, E=32, k=2, dtype="bf16", gate=0, capacity_factor=0),
+] + [
+    # Shapes whose weights-as-M expert GEMMs split tiles between SMs (on a 148-SM B300):
+    # GEMM1 here is 4 tiles of 150 k-blocks cut into ~19 pieces each (several load
+    # batches in the finishing CTA's sum) ...
+    Workload("split_k_many_pieces", T=48, d=9600, h=256, E=2, k=1, dtype="bf16", gate=1,
+             capacity_factor=0, bias_std=0.1),
+    # ... and here both GEMMs split: 64 tiles of 150 k-blocks and 150 tiles of 64.
+    Workload("split_k_both_gemms", T=64, d=9600, h=4096, E=2, k=1, dtype="bf16", gate=1,
+             capacity_factor=0, bias_std=0.1),
 ]
+SPLIT = [w for w in EDGE if w.name.startswith("split_k")]
 
 
 @pytest.mark.parametrize("w", EDGE, ids=[w.name for w in EDGE])
 def test_edge_shapes(w):
     _parity_small(w, make_inputs(w, seed=5))
+
+
+@pytest.mark.parametrize("w", SPLIT, ids=[w.name for w in SPLIT])
+def test_split_tiles_deterministic(w):
+    """Tiles computed in pieces by several SMs are summed in a fixed order: two runs,
+    and the stage calls, agree bit for bit."""
+    dev = tl.to_device(make_inputs(w, seed=6))
+    a = tl.host(tl.run_forward(w, dev)["outs"])
+    b = tl.host(tl.run_forward(w, dev)["outs"])
+    for key in a:
+        np.testing.assert_array_equal(a[key], b[key], err_msg=key)
+    cfg = moe.config_from_workload(w)
+    rows = w.T * w.k
+    ws = tl.poisoned_workspace(moe.moe_stage_workspace_size(cfg))
+    x_perm = torch.empty((rows, w.d), dtype=w.torch_dtype, device="cuda")
+    x_perm[:] = dev["x"][torch.as_tensor(a["row_token"], device="cuda").long().clamp(min=0)]
+    offsets = torch.as_tensor(a["offsets"], device="cuda")
+    h_buf = torch.empty((rows, w.h), dtype=w.torch_dtype, device="cuda")
+    y_perm = torch.empty((rows, w.d), dtype=w.torch_dtype, device="cuda")
+    for _ in range(2):
+        moe.moe_expert_ffn(cfg, x_perm, offsets, dev["w1"], dev["b1"], dev["w2"], dev["b2"], h_buf,
+                           y_perm, ws)
+        assert moe.moe_device_error(ws) == 0
+        y = torch.empty((w.T, w.d), dtype=w.torch_dtype, device="cuda")
+        moe.moe_combine(cfg, y_perm, torch.as_tensor(a["slot_row"], device="cuda"),
+                        torch.as_tensor(a["topk_w"], device="cuda"), y, ws)
+        np.testing.assert_array_equal(y.float().cpu().numpy(), a["y"])
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
@@ -307,7 +333,8 @@ FULL = ["mixtral_prefill", "switch_capacity", "deepseek_fine", "decode"]
 @pytest.mark.parametrize("name", FULL)
 def test_full_size_sampled(name):
     """Full workload sizes through the same moe_forward call the benchmark times:
-    every routing/indexing output exact on all tokens, logits and y on sampled tokens."""
+    every routing/indexing output exact on all tokens, logits on sampled tokens, and y
+    on sampled tokens that include every non-empty expert's first and last kept row."""
     w = WORKLOADS[name]
     cf = capacity_factor_or_none(w)
     inp = make_inputs(w, seed=0, device="cuda")
@@ -324,7 +351,17 @@ def test_full_size_sampled(name):
     lg_ref = oracle.logits(xs, inp["w_gate"].cpu(), lb)
     assert float(np.abs(g["logits"][rows] - lg_ref).max()) <= tl.logits_tol(lg_ref)
 
-    toks = np.unique(np.concatenate([[0, w.T - 1], rng.choice(w.T, min(w.T, 24), replace=False)]))
+    # y on: every token of a small batch; else the first and last token, 24 random ones,
+    # and the tokens of every non-empty expert's first and last kept row, so that each
+    # expert's ragged last tile is compared at the full K.
+    if w.T <= 256:
+        toks = np.arange(w.T)
+    else:
+        off, rt = g["offsets"], g["row_token"]
+        ends = [rt[off[e]] for e in range(w.E) if off[e + 1] > off[e]]
+        ends += [rt[off[e + 1] - 1] for e in range(w.E) if off[e + 1] > off[e]]
+        toks = np.unique(np.concatenate([[0, w.T - 1], rng.choice(w.T, 24, replace=False),
+                                         np.asarray(ends, dtype=np.int64)]))
     host_inp = {"x": inp["x"].cpu()}
     cache = {}
 

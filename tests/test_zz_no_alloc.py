@@ -64,6 +64,56 @@ def test_dispatch_static_matches_dispatch_twice():
             assert torch.equal(got[key], ref[key]), f"{w.name}: {key} differs"
 
 
+def test_dispatch_static_without_a_flags_buffer():
+    """device_flags = NULL keeps the flag word inside the library's array; the outputs are
+    still moe_dispatch's, bit for bit."""
+    w = CASES[0]
+    cfg, x, idx, ws = _route(w)
+    ref = _dispatch_outputs(w)
+    moe.moe_dispatch(cfg, x, idx, ref["offsets"], ref["kept"], ref["slot_row"], ref["row_token"],
+                     ref["dropped"], ref["x_perm"], ws)
+    got = _dispatch_outputs(w)
+    moe.moe_dispatch_static(cfg, x, idx, got["offsets"], got["kept"], got["slot_row"],
+                            got["row_token"], got["dropped"], got["x_perm"], None)
+    torch.cuda.synchronize()
+    for key in ref:
+        assert torch.equal(got[key], ref[key]), f"{key} differs"
+
+
+def test_dispatch_static_flags_an_out_of_range_index():
+    """Expert indices outside [0, E) (host-written, in-bounds data) are skipped as dropped
+    and raise MOE_DEVERR_BAD_INDEX in the caller's flag buffer, as moe_dispatch does."""
+    w = CASES[1]
+    cfg, x, idx, ws = _route(w)
+    idx[5, 1] = w.E
+    idx[17, 0] = -3
+    ref = _dispatch_outputs(w)
+    moe.moe_dispatch(cfg, x, idx, ref["offsets"], ref["kept"], ref["slot_row"], ref["row_token"],
+                     ref["dropped"], ref["x_perm"], ws)
+    assert moe.moe_device_error(ws) & moe.MOE_DEVERR_BAD_INDEX
+    got = _dispatch_outputs(w)
+    flags = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    moe.moe_dispatch_static(cfg, x, idx, got["offsets"], got["kept"], got["slot_row"],
+                            got["row_token"], got["dropped"], got["x_perm"], flags)
+    torch.cuda.synchronize()
+    assert flags.item() & moe.MOE_DEVERR_BAD_INDEX
+    assert got["slot_row"][5, 1].item() == -1 and got["slot_row"][17, 0].item() == -1
+    for key in ref:
+        assert torch.equal(got[key], ref[key]), f"{key} differs"
+
+
+def test_dispatch_static_validates_like_dispatch():
+    """A configuration moe_dispatch rejects (here an unknown routing-noise mode) is rejected
+    by moe_dispatch_static with the same status, before anything is enqueued."""
+    cfg = moe.config(64, 64, 64, 8, 2, "bf16", noise=9)
+    buf = torch.zeros(4096, dtype=torch.int32, device="cuda")
+    p = buf.data_ptr()
+    st_static = moe.lib().moe_dispatch_static(cfg, p, p, p, None, p, p, None, p, None, None)
+    st_dispatch = moe.lib().moe_dispatch(cfg, p, p, p, None, p, p, None, p, p, buf.numel() * 4,
+                                         None)
+    assert st_static == st_dispatch == moe.MOE_ERR_INVALID_ARGUMENT
+
+
 def test_dispatch_static_rejects_sizes_beyond_its_scratch():
     cells = moe.MOE_DISPATCH_STATIC_MAX_CELLS
     E = 256
