@@ -60,6 +60,11 @@ METRIC = "MoE-layer fwd tokens/s at 1 B300; grouped-GEMM % BF16 peak; decode % H
 UNIT = "tokens/s"
 DEFAULT_WORKLOAD = "mixtral_prefill"
 L2_FLUSH_BYTES = 256 << 20
+# A GPU-side wait (torch.cuda._sleep, in SM clock cycles: ~0.1 ms) enqueued after the L2
+# flush and before each device-timed call's start event, so that the host has finished
+# enqueueing the call before the event fires: device times exclude the host's enqueue
+# work, which on the small layers is longer than the layer itself (e2e includes it).
+HEAD_START_CYCLES = 200_000
 KERNELS_PER_FORWARD = 8   # router GEMM, softmax/top-k, finalize/scan, place, row copy, GEMM1, GEMM2, combine
 KERNELS_PER_EC_FORWARD = 7  # router GEMM, softmax, per-expert select, gather, GEMM1, GEMM2, combine
 # moe_backward: combine and gate backward, dA / dXp / router-dx GEMMs, the dx sum, dW2 / dW1 /
@@ -352,10 +357,12 @@ def roofline(w, M, nonempty, t_ffn_s, peaks):
 # ------------------------------------------------------------------ our arm
 def _median_event_ms(fn, steps, warmup, flush, stream):
     """Median CUDA-event time of fn() over `steps` calls after `warmup` calls, with L2
-    flushed (a 256 MB write) before every call, outside the event pair."""
+    flushed (a 256 MB write) and the host given a head start before every call, both
+    outside the event pair."""
     ev = []
     for i in range(steps + warmup):
         flush.zero_()
+        torch.cuda._sleep(HEAD_START_CYCLES)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         fn()
@@ -524,6 +531,7 @@ def run_ours(args, world, rank, local):
     t0 = time.time()
     for i in range(args.steps):
         flush.zero_()
+        torch.cuda._sleep(HEAD_START_CYCLES)
         ev[i][0].record(stream)
         step()
         ev[i][1].record(stream)
@@ -717,6 +725,7 @@ def run_train(args, world, rank, local):
     t0 = time.time()
     for i in range(args.steps):
         flush.zero_()
+        torch.cuda._sleep(HEAD_START_CYCLES)
         ev[i][0].record(stream)
         fwd()
         ev[i][1].record(stream)

@@ -83,6 +83,9 @@ WORKLOADS = {
 # multi-pass profiler captures while keeping the weights far larger than L2.
 WORKLOADS["deepseek_fine_e32"] = WORKLOADS["deepseek_fine"].scaled(name="deepseek_fine_e32",
                                                                   T=1024, E=32)
+# The decode layer's shapes (64 tokens, d=4096, h=14336, top-2, skewing logit bias) with 8
+# experts: 1.9 GB of weights, for profiler captures of the decode-sized kernels.
+WORKLOADS["decode_e8"] = WORKLOADS["decode"].scaled(name="decode_e8", E=8)
 
 # Expert-choice routing over the same layer shapes: each expert takes C =
 # ceil(T * capacity_factor / E) tokens.  A capacity factor of k gives the top-k layer's

@@ -120,7 +120,8 @@ __global__ void __launch_bounds__(kThreads)
 // (token, 128 consecutive 16-byte vectors), one warp per unit, grid-stride: each lane
 // loads its 4 vectors once and stores them to each of the token's kept rows (the
 // gather above reads a row once per slot: k times the reads when the rows do not
-// stay in L2).  Every row below M is some kept slot's, so all are written.
+// stay in L2); a token with no kept slot costs one slot_row read.  Every row below M
+// is some kept slot's, so all are written.
 constexpr int kScatterVecs = 128;
 
 __global__ void __launch_bounds__(kThreads)
@@ -136,6 +137,8 @@ __global__ void __launch_bounds__(kThreads)
     const int64_t t = chunks == 1 ? u : u / chunks;
     const int v0 = static_cast<int>(u - t * chunks) * kScatterVecs;
     const int my_row = lane < k ? slot_row[t * k + lane] : -1;
+    // A token whose every slot was dropped has no row to fill: its x row is not read.
+    if (!__any_sync(0xffffffffu, my_row >= 0)) continue;
     int64_t dst[kMaxK];
 #pragma unroll
     for (int j = 0; j < kMaxK; ++j) {

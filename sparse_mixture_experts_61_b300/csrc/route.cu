@@ -23,16 +23,6 @@
 namespace moe {
 namespace {
 
-__device__ __forceinline__ double warp_sum_d(double v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-__device__ __forceinline__ double warp_max_d(double v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmax(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return v;
-}
 
 // s += v with the rounding error carried in c (Kahan); order-fixed, so deterministic.
 __device__ __forceinline__ void kahan_add(float& s, float& c, float v) {
@@ -289,7 +279,7 @@ __global__ void __launch_bounds__(kFinThreads)
                           int32_t* __restrict__ kept, int32_t* __restrict__ offsets,
                           int32_t* __restrict__ dropped, float* __restrict__ stats) {
   pdl_enter();
-  __shared__ double s_red[kMaxExperts / 32];
+  __shared__ int s_c[kMaxExperts];
   __shared__ float s_loss[kMaxExperts / 32];
   __shared__ int s_scan[kMaxExperts / 32];
   __shared__ int s_drop;
@@ -307,9 +297,14 @@ __global__ void __launch_bounds__(kFinThreads)
     const int c_lo = sl * per, c_hi = min(nchunks, c_lo + per);
     int cnt = 0;
     float ps = 0.f, pc = 0.f;  // compensated (Kahan) sum of the chunks' softmax sums
+    // Sixteen chunks at a time: the loads are issued together (one memory latency per
+    // batch), then added in order.  The first batch's counts stay in registers for the
+    // position bases below, so a slice of at most sixteen chunks is read once.
+    constexpr int B = 16;
+    int first[B];
+#pragma unroll
+    for (int i = 0; i < B; ++i) first[i] = 0;
     if (ex < E) {
-      // Eight chunks at a time: the loads are issued together, then added in order.
-      constexpr int B = 8;
       for (int c0 = c_lo; c0 < c_hi; c0 += B) {
         int hv[B];
         float pv[B];
@@ -324,22 +319,25 @@ __global__ void __launch_bounds__(kFinThreads)
           cnt += hv[i];
           kahan_add(ps, pc, pv[i]);
         }
+        if (c0 == c_lo) {
+#pragma unroll
+          for (int i = 0; i < B; ++i) first[i] = hv[i];
+        }
       }
     }
     s_cnt[tid] = cnt;
     s_ps[tid] = ps - pc;
     __syncthreads();
-    // Position bases: the counts of the lower slices, then this slice's chunks in order
-    // (loads issued eight at a time).
+    // Position bases: the counts of the lower slices, then this slice's chunks in order.
     if (chunk_base && ex < E) {
       int base = 0;
       for (int q = 0; q < sl; ++q) base += s_cnt[q * EP + ex];
-      constexpr int B = 8;
       for (int c0 = c_lo; c0 < c_hi; c0 += B) {
         int hv[B];
 #pragma unroll
         for (int i = 0; i < B; ++i)
-          hv[i] = c0 + i < c_hi ? hist[static_cast<int64_t>(c0 + i) * E + ex] : 0;
+          hv[i] = c0 == c_lo ? first[i]
+                             : (c0 + i < c_hi ? hist[static_cast<int64_t>(c0 + i) * E + ex] : 0);
 #pragma unroll
         for (int i = 0; i < B; ++i) {
           if (c0 + i < c_hi) chunk_base[static_cast<int64_t>(c0 + i) * E + ex] = base;
@@ -397,40 +395,67 @@ __global__ void __launch_bounds__(kFinThreads)
     if (e == E - 1) offsets[E] = incl;
   }
 
-  // Routing statistics of the pre-drop counts.  load_e = count_e / total; sample
-  // standard deviations.  Every thread takes part (the reductions synchronise).
+  // Routing statistics of the pre-drop counts, in warp 0 once the counts are in shared
+  // memory (this GPU's FP64 rate is a small fraction of its FP32 rate, so block-wide
+  // double reductions over every warp cost more than the rest of the kernel):
+  // load_e = count_e / total; the total, the maximum and the dead test
+  // (load_e < 1e-4  <=>  10^4 * count_e < total) are exact integer arithmetic; the
+  // load mean is 1/E; loads and sums of squares are double (three FP64 operations per
+  // expert); each entropy term's logarithm is fp32 (logf), accumulated in double.
+  // Sample standard deviations (divisor E - 1).
   if (stats) {
-    auto block_reduce = [&](double v, bool is_max) {
-      v = is_max ? warp_max_d(v) : warp_sum_d(v);
-      __syncthreads();  // earlier readers of s_red are done
-      if (lane == 0 && warp < kExpertWarps) s_red[warp] = v;
-      __syncthreads();
-      double r = s_red[0];
-      for (int w = 1; w < kExpertWarps; ++w) r = is_max ? fmax(r, s_red[w]) : r + s_red[w];
-      return r;
-    };
-    const bool own = e < E;
-    const double c = own ? static_cast<double>(cnt) : 0.0;
-    const double total = block_reduce(c, false);
-    const double load = (own && total > 0.0) ? c / total : 0.0;
-    const double lmean = block_reduce(load, false) / E, cmean = total / E;
-    const double lvar = block_reduce(own ? (load - lmean) * (load - lmean) : 0.0, false);
-    const double cvar = block_reduce(own ? (c - cmean) * (c - cmean) : 0.0, false);
-    const double lmax = block_reduce(own ? load : 0.0, true);
-    const double dead = block_reduce((own && load < 1e-4) ? 1.0 : 0.0, false);
-    const double ent = block_reduce(own ? -load * log(load + 1e-10) : 0.0, false);
-    if (e == 0) {
-      if (total > 0.0) {
-        const double lstd = E > 1 ? sqrt(lvar / (E - 1)) : 0.0;
-        const double cstd = E > 1 ? sqrt(cvar / (E - 1)) : 0.0;
-        stats[0] = static_cast<float>(lstd / lmean);
-        stats[1] = static_cast<float>(dead / E);
-        stats[2] = static_cast<float>(lmax / lmean);
-        stats[3] = static_cast<float>(ent);
-        stats[4] = static_cast<float>(exp(ent));
-        stats[5] = static_cast<float>(cstd / (cmean + 1e-6));
-      } else {
-        for (int i = 0; i < 6; ++i) stats[i] = 0.f;
+    if (e < E) s_c[e] = cnt;
+    __syncthreads();
+    if (warp == 0) {
+      long long tot = 0;
+      int mx = 0;
+      for (int i = lane; i < E; i += 32) {
+        tot += s_c[i];
+        mx = max(mx, s_c[i]);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        tot += __shfl_xor_sync(0xffffffffu, tot, o);
+        mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      }
+      double lvar = 0.0, cvar = 0.0, ent = 0.0;
+      int dead = 0;
+      const double total = static_cast<double>(tot);
+      const double inv = tot > 0 ? 1.0 / total : 0.0;
+      const double lmean = 1.0 / E, cmean = total * lmean;
+      for (int i = lane; i < E; i += 32) {
+        const int c = s_c[i];
+        const double load = static_cast<double>(c) * inv;
+        const double dl = load - lmean, dc = static_cast<double>(c) - cmean;
+        lvar = fma(dl, dl, lvar);
+        cvar = fma(dc, dc, cvar);
+        const float lf = static_cast<float>(load);
+        ent -= static_cast<double>(lf * logf(lf + 1e-10f));
+        dead += (static_cast<long long>(c) * 10000 < tot) ? 1 : 0;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {  // three independent butterflies, interleaved
+        lvar += __shfl_xor_sync(0xffffffffu, lvar, o);
+        cvar += __shfl_xor_sync(0xffffffffu, cvar, o);
+        ent += __shfl_xor_sync(0xffffffffu, ent, o);
+        dead += __shfl_xor_sync(0xffffffffu, dead, o);
+      }
+      if (lane == 0) {
+        // The closing formulas in fp32: their inputs are exact integers or double sums,
+        // and scalar FP64 divisions, square roots and exp are long dependent chains here.
+        if (tot > 0) {
+          const float Ef = static_cast<float>(E);
+          const float lstd = E > 1 ? sqrtf(static_cast<float>(lvar) / (Ef - 1.f)) : 0.f;
+          const float cstd = E > 1 ? sqrtf(static_cast<float>(cvar) / (Ef - 1.f)) : 0.f;
+          stats[0] = lstd * Ef;  // std(load) / mean(load), mean(load) = 1/E
+          stats[1] = static_cast<float>(dead) / Ef;
+          stats[2] = static_cast<float>(mx) / static_cast<float>(tot) * Ef;
+          stats[3] = static_cast<float>(ent);
+          stats[4] = expf(static_cast<float>(ent));
+          stats[5] = cstd / (static_cast<float>(cmean) + 1e-6f);
+        } else {
+          for (int q = 0; q < 6; ++q) stats[q] = 0.f;
+        }
       }
     }
   }
