@@ -74,10 +74,18 @@ TRAIN_METRIC = "MoE-layer fwd+bwd (training step) tokens/s at 1 B300; backward G
 D_AUX = 0.01
 
 # dram__bytes_read.sum + dram__bytes_write.sum of one moe_expert_ffn (the grouped GEMM
-# pair G1 + G2) from an ncu capture, with the hash (gemm_source_hash) of the GEMM sources
-# that capture ran.  A figure whose hash differs from the current sources' is stale and
-# reported as null.
-NCU_TRAFFIC_BYTES = {}
+# pair G1 + G2) from an ncu capture: (hash of the GEMM sources that capture ran, bytes,
+# how).  The 15 GB layers are captured on their reduced twins (same per-expert shapes,
+# 32 or 8 experts) and scaled by the algorithmic bytes.  A figure whose hash differs from
+# the current sources' (gemm_source_hash) is stale and reported as null.
+NCU_TRAFFIC_BYTES = {
+    "mixtral_prefill": ("edc4789208d4676b", 2718490000, "captured at full size"),
+    "switch_capacity": ("edc4789208d4676b", 155200000, "captured at full size"),
+    "deepseek_fine": ("edc4789208d4676b", 17503840000,
+                      "deepseek_fine_e32 capture (1.0029 x its algorithmic bytes), scaled"),
+    "decode": ("edc4789208d4676b", 4502890000,
+               "decode_e8 capture (1.0067 x its algorithmic bytes), scaled"),
+}
 GEMM_SOURCES = ("sparse_mixture_experts_61_b300/csrc/gemm_tc.cu",
                 "sparse_mixture_experts_61_b300/csrc/tc_pipe.cuh",
                 "sparse_mixture_experts_61_b300/csrc/common.cuh")
@@ -94,10 +102,11 @@ def gemm_source_hash() -> str:
 
 
 def ncu_traffic(name: str):
+    """(bytes, how) of the current GEMM sources' capture for a workload, or (None, None)."""
     entry = NCU_TRAFFIC_BYTES.get(name)
     if entry is None or entry[0] != gemm_source_hash():
-        return None
-    return entry[1]
+        return None, None
+    return entry[1], entry[2]
 
 
 def load_peaks():
@@ -337,7 +346,7 @@ def roofline(w, M, nonempty, t_ffn_s, peaks):
     flops, byts = ffn_algorithmic(w, M, nonempty)
     t_tensor = flops / (peaks["bf16_tflops"] * 1e12)
     t_hbm = byts / (peaks["hbm_gbs"] * 1e9)
-    traffic = ncu_traffic(w.name)
+    traffic, traffic_how = ncu_traffic(w.name)
     if t_tensor >= t_hbm:
         achieved = flops / t_ffn_s / 1e12
         r = dict(bound="tensor", achieved=round(achieved, 1), peak=peaks["bf16_tflops"],
@@ -348,7 +357,8 @@ def roofline(w, M, nonempty, t_ffn_s, peaks):
         achieved = byts / t_ffn_s / 1e9
         r = dict(bound="hbm", achieved=round(achieved, 1), peak=peaks["hbm_gbs"], unit="GB/s",
                  frac=round(achieved / peaks["hbm_gbs"], 4))
-    r.update(traffic=traffic, kernel="grouped expert GEMM pair G1+G2 (moe_expert_ffn)",
+    r.update(traffic=traffic, traffic_source=traffic_how,
+             kernel="grouped expert GEMM pair G1+G2 (moe_expert_ffn)",
              algorithmic_flops=flops, algorithmic_bytes=byts, peak_source=peaks["source"],
              ms=round(t_ffn_s * 1e3, 4))
     return r

@@ -55,3 +55,17 @@ def test_roofline_bound_and_fraction():
     r = bench.roofline(d, d.T * d.k, 24, 1e-3, peaks)
     assert r["bound"] == "hbm" and r["unit"] == "GB/s" and r["peak"] == 6500.0
     assert r["algorithmic_bytes"] >= 24 * 2 * d.d * d.h * 2
+
+
+def test_traffic_figure_is_dropped_when_the_gemm_sources_change(monkeypatch):
+    """roofline.traffic comes from a capture of specific GEMM sources: with any other
+    sources (a different hash) the figure is reported as null, not carried over."""
+    sys.path.insert(0, ROOT)
+    import bench
+
+    name = next(iter(bench.NCU_TRAFFIC_BYTES))
+    recorded = bench.NCU_TRAFFIC_BYTES[name][0]
+    monkeypatch.setattr(bench, "gemm_source_hash", lambda: recorded)
+    assert bench.ncu_traffic(name)[0] == bench.NCU_TRAFFIC_BYTES[name][1]
+    monkeypatch.setattr(bench, "gemm_source_hash", lambda: "0" * 16)
+    assert bench.ncu_traffic(name) == (None, None)
