@@ -381,10 +381,11 @@ __global__ void __launch_bounds__(kFinThreads)
   __syncthreads();
   if (e == 0) {
     if (psum && aux) {
-      double tot = 0.0;
+      // fp32: the warp partials in warp order, then one product and one quotient.
+      float tot = 0.f;
       for (int w = 0; w < kExpertWarps; ++w) tot += s_loss[w];
-      const double TT = static_cast<double>(T) * static_cast<double>(T);
-      aux[0] = T > 0 ? static_cast<float>(static_cast<double>(E) * tot / TT) : 0.f;
+      const float Tf = static_cast<float>(T);
+      aux[0] = T > 0 ? static_cast<float>(E) * tot / (Tf * Tf) : 0.f;
     }
     if (dropped) dropped[0] = s_drop;
   }
@@ -396,63 +397,63 @@ __global__ void __launch_bounds__(kFinThreads)
   }
 
   // Routing statistics of the pre-drop counts, in warp 0 once the counts are in shared
-  // memory (this GPU's FP64 rate is a small fraction of its FP32 rate, so block-wide
-  // double reductions over every warp cost more than the rest of the kernel):
-  // load_e = count_e / total; the total, the maximum and the dead test
-  // (load_e < 1e-4  <=>  10^4 * count_e < total) are exact integer arithmetic; the
-  // load mean is 1/E; loads and sums of squares are double (three FP64 operations per
-  // expert); each entropy term's logarithm is fp32 (logf), accumulated in double.
-  // Sample standard deviations (divisor E - 1).
+  // memory, without FP64 (this GPU's FP64 pipe is thin, and scalar double chains cost
+  // microseconds here).  With load_e = count_e / total and S2 = sum_e count_e^2, both
+  // sums of squared deviations follow from one exact integer,
+  //   N = E * S2 - total^2  (>= 0):   sum_e (load_e - 1/E)^2 = N / (E total^2),
+  //                                   sum_e (count_e - total/E)^2 = N / E,
+  // computed in 128-bit integer arithmetic (count_e < 2^31, total < 2^31), so only the
+  // closing fp32 formulas round.  The total, the maximum and the dead-expert test
+  // (load_e < 1e-4  <=>  10^4 * count_e < total) are exact; the entropy's terms
+  // -load_e ln(load_e + 1e-10) are non-negative (up to 1e-10 load_e) and summed in fp32.
+  // Sample standard deviations (divisor E - 1); mean load = 1/E.
   if (stats) {
     if (e < E) s_c[e] = cnt;
     __syncthreads();
     if (warp == 0) {
       long long tot = 0;
+      unsigned long long s2 = 0;
       int mx = 0;
       for (int i = lane; i < E; i += 32) {
-        tot += s_c[i];
-        mx = max(mx, s_c[i]);
+        const int c = s_c[i];
+        tot += c;
+        s2 += static_cast<unsigned long long>(c) * static_cast<unsigned long long>(c);
+        mx = max(mx, c);
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
         tot += __shfl_xor_sync(0xffffffffu, tot, o);
+        s2 += __shfl_xor_sync(0xffffffffu, s2, o);
         mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
       }
-      double lvar = 0.0, cvar = 0.0, ent = 0.0;
+      const float inv = tot > 0 ? 1.f / static_cast<float>(tot) : 0.f;
+      float ent = 0.f;
       int dead = 0;
-      const double total = static_cast<double>(tot);
-      const double inv = tot > 0 ? 1.0 / total : 0.0;
-      const double lmean = 1.0 / E, cmean = total * lmean;
       for (int i = lane; i < E; i += 32) {
         const int c = s_c[i];
-        const double load = static_cast<double>(c) * inv;
-        const double dl = load - lmean, dc = static_cast<double>(c) - cmean;
-        lvar = fma(dl, dl, lvar);
-        cvar = fma(dc, dc, cvar);
-        const float lf = static_cast<float>(load);
-        ent -= static_cast<double>(lf * logf(lf + 1e-10f));
+        const float load = static_cast<float>(c) * inv;
+        ent -= load * logf(load + 1e-10f);
         dead += (static_cast<long long>(c) * 10000 < tot) ? 1 : 0;
       }
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {  // three independent butterflies, interleaved
-        lvar += __shfl_xor_sync(0xffffffffu, lvar, o);
-        cvar += __shfl_xor_sync(0xffffffffu, cvar, o);
+      for (int o = 16; o > 0; o >>= 1) {
         ent += __shfl_xor_sync(0xffffffffu, ent, o);
         dead += __shfl_xor_sync(0xffffffffu, dead, o);
       }
       if (lane == 0) {
-        // The closing formulas in fp32: their inputs are exact integers or double sums,
-        // and scalar FP64 divisions, square roots and exp are long dependent chains here.
         if (tot > 0) {
-          const float Ef = static_cast<float>(E);
-          const float lstd = E > 1 ? sqrtf(static_cast<float>(lvar) / (Ef - 1.f)) : 0.f;
-          const float cstd = E > 1 ? sqrtf(static_cast<float>(cvar) / (Ef - 1.f)) : 0.f;
-          stats[0] = lstd * Ef;  // std(load) / mean(load), mean(load) = 1/E
+          const unsigned __int128 n128 =
+              static_cast<unsigned __int128>(E) * s2 -
+              static_cast<unsigned __int128>(tot) * static_cast<unsigned long long>(tot);
+          const float Ef = static_cast<float>(E), totf = static_cast<float>(tot);
+          // sqrt(N / (E (E - 1))) = the count standard deviation
+          const float cstd = E > 1 ? sqrtf(static_cast<float>(n128) / (Ef * (Ef - 1.f))) : 0.f;
+          stats[0] = cstd * Ef / totf;  // std(load) / mean(load)
           stats[1] = static_cast<float>(dead) / Ef;
-          stats[2] = static_cast<float>(mx) / static_cast<float>(tot) * Ef;
-          stats[3] = static_cast<float>(ent);
-          stats[4] = expf(static_cast<float>(ent));
-          stats[5] = cstd / (static_cast<float>(cmean) + 1e-6f);
+          stats[2] = static_cast<float>(mx) / totf * Ef;
+          stats[3] = ent;
+          stats[4] = expf(ent);
+          stats[5] = cstd / (totf / Ef + 1e-6f);
         } else {
           for (int q = 0; q < 6; ++q) stats[q] = 0.f;
         }
