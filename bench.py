@@ -79,12 +79,12 @@ D_AUX = 0.01
 # 32 or 8 experts) and scaled by the algorithmic bytes.  A figure whose hash differs from
 # the current sources' (gemm_source_hash) is stale and reported as null.
 NCU_TRAFFIC_BYTES = {
-    "mixtral_prefill": ("edc4789208d4676b", 2718490000, "captured at full size"),
-    "switch_capacity": ("edc4789208d4676b", 155200000, "captured at full size"),
-    "deepseek_fine": ("edc4789208d4676b", 17503840000,
-                      "deepseek_fine_e32 capture (1.0029 x its algorithmic bytes), scaled"),
-    "decode": ("edc4789208d4676b", 4502890000,
-               "decode_e8 capture (1.0067 x its algorithmic bytes), scaled"),
+    "mixtral_prefill": ("1774bad022eefabe", 2721147648, "captured at full size"),
+    "switch_capacity": ("1774bad022eefabe", 155240960, "captured at full size"),
+    "deepseek_fine": ("1774bad022eefabe", 17497714688,
+                      "deepseek_fine_e32 capture (1.0026 x its algorithmic bytes), scaled"),
+    "decode": ("1774bad022eefabe", 4507687178,
+               "decode_e8 capture (1.0078 x its algorithmic bytes), scaled"),
 }
 GEMM_SOURCES = ("sparse_mixture_experts_61_b300/csrc/gemm_tc.cu",
                 "sparse_mixture_experts_61_b300/csrc/tc_pipe.cuh",
@@ -499,7 +499,7 @@ def run_ours(args, world, rank, local):
     torch.cuda.set_device(dev)
     w = WORKLOADS[args.workload]
     inp = make_inputs(w, seed=rank, device=str(dev))
-    cfg = moe.config_from_workload(w)
+    cfg = moe.config_from_workload(w, fused_gather=int(args.fused_gather))
     i32 = dict(dtype=torch.int32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
@@ -633,6 +633,7 @@ def run_ours(args, world, rank, local):
                    "capacity_factor": w.capacity_factor, "kept_rows": M,
                    "nonempty_experts": nonempty, "inputs": input_recipe(w),
                    "l2": "flushed before every timed step (256 MB write outside the event pair)",
+                   "fused_gather": bool(args.fused_gather),
                    "parallelism": f"replicas x{world} (token-parallel, no collective)"},
         "roofline": roofline(w, M, nonempty, t_ffn, peaks),
         "e2e": {"value": round(replica_throughput(world, w.T, e2e_ms), 1), "unit": UNIT,
@@ -645,7 +646,9 @@ def run_ours(args, world, rank, local):
                 "serial_value": round(replica_throughput(world, w.T, ser_ms), 1),
                 "serial": "per step: x copied in, moe_forward, y copied out, no overlap "
                           "(L2 flushed before each step)"},
-        "gpu_launches": (KERNELS_PER_EC_FORWARD if ec else KERNELS_PER_FORWARD) * args.steps,
+        # with fused_gather the forward launches no row-copy kernel
+        "gpu_launches": (KERNELS_PER_EC_FORWARD if ec else
+                         KERNELS_PER_FORWARD - (1 if args.fused_gather else 0)) * args.steps,
         "clocks": clocks.summary(t0, t1) if clocks else None,
     }
     if world == 1 and not args.no_cpu_baseline:
@@ -866,6 +869,9 @@ def main():
                     help="forward (default) or train: forward + backward of the layer per step")
     ap.add_argument("--no-workloads", action="store_true",
                     help="skip the `workloads` map of the other layer configurations")
+    ap.add_argument("--fused-gather", action="store_true",
+                    help="time the forward with cfg.fused_gather (GEMM1 gathers its token rows "
+                         "from x; no expert-ordered copy in the workspace)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -891,7 +897,7 @@ def main():
             line = run_train(args, world, rank, local)
         else:
             line = run_ours(args, world, rank, local)
-            if args.workload == DEFAULT_WORKLOAD and not args.no_workloads:
+            if args.workload == DEFAULT_WORKLOAD and not args.no_workloads and not args.fused_gather:
                 line = run_family(args, world, rank, local, line)
         if world > 1:
             import torch.distributed as dist

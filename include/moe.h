@@ -138,6 +138,15 @@ typedef struct moe_config {
   double capacity_factor; /* > 0: capacity C = ceil(T * capacity_factor / E) kept assignments
                              per expert, later ones dropped; <= 0: no limit */
   int32_t noise;          /* moe_noise: routing noise applied before selection */
+  /* 0 (default): moe_forward copies each kept token row into expert order (x_perm) before
+     the expert GEMMs.  1: moe_forward's first expert GEMM reads the token rows straight
+     from x (tile::gather4 loads by the dispatch's row -> token map) and the workspace holds
+     no expert-ordered copy, T*k*d*2 bytes smaller (940 MB for T = 8192, k = 8,
+     d = 7168) -- for callers short of device memory.  Results are bitwise identical; it
+     is slower (the gathers issue more copies per k-block than the tiled loads).  bf16
+     top-k layers only (MOE_ERR_UNSUPPORTED otherwise); a forward that is given an x_perm
+     buffer fills it and uses it as with 0.  Stage calls are unaffected. */
+  int32_t fused_gather;
 } moe_config;
 
 /* Inputs and outputs of moe_forward.  Outputs marked "or NULL" are optional;

@@ -62,7 +62,7 @@ class MoeConfig(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int64), ("d", ctypes.c_int32), ("h", ctypes.c_int32),
                 ("E", ctypes.c_int32), ("k", ctypes.c_int32), ("dtype", ctypes.c_int32),
                 ("gate", ctypes.c_int32), ("capacity_factor", ctypes.c_double),
-                ("noise", ctypes.c_int32)]
+                ("noise", ctypes.c_int32), ("fused_gather", ctypes.c_int32)]
 
 
 class MoeForwardArgs(ctypes.Structure):
@@ -146,15 +146,17 @@ def status_str(status: int) -> str:
     return lib().moe_status_str(int(status)).decode()
 
 
-def config(T, d, h, E, k, dtype="bf16", gate=0, capacity_factor=0.0, noise=0) -> MoeConfig:
+def config(T, d, h, E, k, dtype="bf16", gate=0, capacity_factor=0.0, noise=0,
+           fused_gather=0) -> MoeConfig:
     dt = {"f32": MOE_F32, "bf16": MOE_BF16}[dtype] if isinstance(dtype, str) else int(dtype)
     return MoeConfig(int(T), int(d), int(h), int(E), int(k), dt, int(gate),
-                     float(capacity_factor or 0.0), int(noise))
+                     float(capacity_factor or 0.0), int(noise), int(fused_gather))
 
 
-def config_from_workload(w, noise=0) -> MoeConfig:
+def config_from_workload(w, noise=0, fused_gather=0) -> MoeConfig:
     """Config for an object with T, d, h, E, k, dtype, gate, capacity_factor attributes."""
-    return config(w.T, w.d, w.h, w.E, w.k, w.dtype, w.gate, w.capacity_factor, noise)
+    return config(w.T, w.d, w.h, w.E, w.k, w.dtype, w.gate, w.capacity_factor, noise,
+                  fused_gather)
 
 
 def _p(t) -> Optional[int]:

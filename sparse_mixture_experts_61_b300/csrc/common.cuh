@@ -161,6 +161,19 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, uint
       : "memory");
 }
 
+// Four rows of a 2-D tensor (row indices y0..y3, columns from x) written to four
+// consecutive 128-byte rows at dst: a tile::gather4 load.  The tensor map's box is one
+// row high and 64 bf16 (128 bytes) wide; with 128-byte swizzling each row lands where a
+// tiled load of the same rows would put it.  Completes 512 bytes on `bar`.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const void* tmap, uint32_t bar, int x,
+                                            int y0, int y1, int y2, int y3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3)
+      : "memory");
+}
+
 // 3-D tiled store of a shared-memory box (bulk-group completion); rows and columns
 // outside the tensor are not written.
 __device__ __forceinline__ void tma_store_3d(const void* tmap, uint32_t src, int x, int y, int z) {

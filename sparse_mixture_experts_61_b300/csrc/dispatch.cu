@@ -184,7 +184,7 @@ cudaError_t launch_dispatch_place(int dtype, const int32_t* topk_idx, int64_t T,
   launch_pdl(dispatch_place_kernel, static_cast<unsigned>(nchunks), kThreads, 0, stream, 
       topk_idx, T, E, k, C, chunk_base, offsets, slot_row, row_token, flags);
   cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  if (e != cudaSuccess || x_perm == nullptr) return e;
   // Xp by scatter from the tokens (each x row read once).
   const int nvec = d * (dtype == MOE_F32 ? 4 : 2) / 16;
   const int64_t units = T * ((nvec + kScatterVecs - 1) / kScatterVecs);

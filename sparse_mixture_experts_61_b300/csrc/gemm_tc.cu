@@ -77,7 +77,7 @@ struct SplitK {
   __device__ __forceinline__ bool busy(int c) const { return begin(c) < begin(c + 1); }
 };
 
-template <int TB, int STAGES, int EPI>
+template <int TB, int STAGES, int EPI, bool GATHER>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     tc_ffn_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                   const GemmArgs p) {
@@ -88,8 +88,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   constexpr uint32_t kWeightBytes = TILE_M * TC_BK * 2;
   constexpr uint32_t kBoxBytes = TOK_BOX * TC_BK * 2;
   constexpr int64_t kPartFloats = int64_t{TILE_M} * TB;  // one parked piece
+  constexpr uint32_t kRowBytes = TC_BK * 2;              // one token row of a k-block
   using Smem = PipeSmem<TILE_M * TC_BK * 2, TB * TC_BK * 2, STAGES>;
   Smem& S = smem_aligned<Smem>();
+  // Gathered token rows: the current piece's token ids, after the pipeline state in the
+  // dynamic shared memory (allocated only for a gathering launch, so that the default
+  // launch's footprint is unchanged).
+  int* s_tok = reinterpret_cast<int*>(
+      (reinterpret_cast<uintptr_t>(&S) + sizeof(Smem) + 15) & ~static_cast<uintptr_t>(15));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.G;
   pipe_prologue<Smem, STAGES>(S, kTmemCols, p, G, TB, &tmW, &tmX);
@@ -150,12 +156,37 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     c.row_end = c.row0 + bsz < end ? c.row0 + bsz : end;
     c.ntok = static_cast<int>((c.row_end - c.row0 + 15) & ~int64_t{15});
     c.nbox = (c.ntok + TOK_BOX - 1) / TOK_BOX;
-    c.bytes = kWeightBytes + static_cast<uint32_t>(c.nbox) * kBoxBytes;
+    c.bytes = kWeightBytes + (GATHER ? static_cast<uint32_t>(c.ntok) * kRowBytes
+                                     : static_cast<uint32_t>(c.nbox) * kBoxBytes);
     return c;
   };
 
   if (warp == 0) {
-    if (lane == 0)
+    if constexpr (GATHER) {
+      // Token rows straight from x: the piece's token ids are fetched by the whole warp
+      // (the block's padding rows repeat its last token; an id outside [0, rows) is
+      // flagged and read as token 0), then four rows of x per gather.
+      run_producer_warp<STAGES>(
+          S, 0, 1, npieces, decode,
+          [&](const Coord& c, int ln) {
+            for (int i = ln; i < c.ntok; i += 32) {
+              const int64_t r = c.row0 + i < c.row_end ? c.row0 + i : c.row_end - 1;
+              int t = p.gather_rows[r];
+              if (t < 0 || t >= p.gather_src_rows) {
+                raise_flag(p.flags, MOE_DEVERR_BAD_ROW);
+                t = 0;
+              }
+              s_tok[i] = t;
+            }
+          },
+          [&](const Coord& c, int kb, uint32_t sa, uint32_t sb, uint32_t bar) {
+            tma_load_3d(sa, &tmW, bar, kb * TC_BK, c.n0, c.g);
+            for (int j = 0; j < c.ntok; j += 4)
+              tma_gather4(sb + j * kRowBytes, &tmX, bar, kb * TC_BK, s_tok[j], s_tok[j + 1],
+                          s_tok[j + 2], s_tok[j + 3]);
+          },
+          abort, p.flags);
+    } else if (lane == 0) {
       run_producer<STAGES>(
           S, 0, 1, npieces, decode,
           [&](const Coord& c, int kb, uint32_t sa, uint32_t sb, uint32_t bar) {
@@ -165,6 +196,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                           static_cast<int>(c.row0) + j * TOK_BOX);
           },
           abort, p.flags);
+    }
   } else if (warp == 1) {
     if (lane == 0)
       run_mma<STAGES, TB>(S, 0, 1, npieces, S.tmem_base, decode,
@@ -304,7 +336,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 // writes it with one TMA store: whole 128-byte lines instead of 16-byte pieces of 32
 // rows per store instruction (1.2-1.4% faster on the prefill and 256-expert layers).
 // When the pre-activation is also requested, every warp stores directly.
-template <int BN, int STAGES, int EPI>
+template <int BN, int STAGES, int EPI, bool GATHER>
 __global__ void __launch_bounds__(ROWS_THREADS, 1)
     tc_rows_ffn_kernel(const __grid_constant__ CUtensorMap tmX,
                        const __grid_constant__ CUtensorMap tmW,
@@ -316,6 +348,13 @@ __global__ void __launch_bounds__(ROWS_THREADS, 1)
   constexpr uint32_t kStageBytes = (TILE_M + BN) * TC_BK * 2;
   using Smem = PipeSmem<TILE_M * TC_BK * 2, BN * TC_BK * 2, STAGES>;
   Smem& S = smem_aligned<Smem>();
+  // Gathered token rows: the current tile's token ids, in the padding between the
+  // pipeline state and the 1 KB-aligned epilogue staging boxes (the dynamic shared memory
+  // is already at the per-block maximum, so there is no room for a static array).
+  static_assert(((sizeof(Smem) + 1023) & ~size_t{1023}) - sizeof(Smem) >= TILE_M * sizeof(int) + 16,
+                "room for the token ids before the staging boxes");
+  int* s_tok = reinterpret_cast<int*>(
+      (reinterpret_cast<uintptr_t>(&S) + sizeof(Smem) + 15) & ~static_cast<uintptr_t>(15));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.G;
   pipe_prologue<Smem, STAGES>(S, kTmemCols, p, G, TILE_M, &tmX, &tmW, 32 * ROWS_EPI_WARPS);
@@ -345,7 +384,31 @@ __global__ void __launch_bounds__(ROWS_THREADS, 1)
   };
 
   if (warp == 0) {
-    if (lane == 0)
+    if constexpr (GATHER) {
+      // Token rows straight from x: the tile's token ids are fetched by the whole warp
+      // (rows past the group's end repeat its last token; an id outside [0, rows) is
+      // flagged and read as token 0), then the 128-row token tile as 32 gathers of four.
+      run_producer_warp<STAGES>(
+          S, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), total, decode,
+          [&](const Coord& c, int ln) {
+            for (int i = ln; i < TILE_M; i += 32) {
+              const int64_t r = c.row0 + i < c.row_end ? c.row0 + i : c.row_end - 1;
+              int t = p.gather_rows[r];
+              if (t < 0 || t >= p.gather_src_rows) {
+                raise_flag(p.flags, MOE_DEVERR_BAD_ROW);
+                t = 0;
+              }
+              s_tok[i] = t;
+            }
+          },
+          [&](const Coord& c, int kb, uint32_t sa, uint32_t sb, uint32_t bar) {
+            for (int j = 0; j < TILE_M; j += 4)
+              tma_gather4(sa + j * TC_BK * 2, &tmX, bar, kb * TC_BK, s_tok[j], s_tok[j + 1],
+                          s_tok[j + 2], s_tok[j + 3]);
+            tma_load_3d(sb, &tmW, bar, kb * TC_BK, c.n0, c.g);
+          },
+          abort, p.flags);
+    } else if (lane == 0) {
       run_producer<STAGES>(
           S, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), total, decode,
           [&](const Coord& c, int kb, uint32_t sa, uint32_t sb, uint32_t bar) {
@@ -353,6 +416,7 @@ __global__ void __launch_bounds__(ROWS_THREADS, 1)
             tma_load_3d(sb, &tmW, bar, kb * TC_BK, c.n0, c.g);
           },
           abort, p.flags);
+    }
   } else if (warp == 1) {
     if (lane == 0)
       run_mma<STAGES, BN>(S, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), total,
@@ -603,21 +667,30 @@ template <int TB, int STAGES, int EPI>
 cudaError_t launch_ffn(const GemmArgs& a, int sm_count, cudaStream_t stream) {
   if (!a.sk_ctr || !a.sk_part) return cudaErrorInvalidValue;
   CUtensorMap tmW, tmX;
-  if (!stacked_map(&tmW, a.B, a.G, a.N, a.K, TILE_M) ||
-      !rows_map(&tmX, a.A, a.rows_alloc, a.K, TOK_BOX))
-    return cudaErrorInvalidValue;
+  // Token rows: 32-row boxes of the expert-ordered rows, or one-row boxes of x to gather.
+  const bool ok_x = a.gather_rows ? rows_map(&tmX, a.gather_src, a.gather_src_rows, a.K, 1)
+                                  : rows_map(&tmX, a.A, a.rows_alloc, a.K, TOK_BOX);
+  if (!stacked_map(&tmW, a.B, a.G, a.N, a.K, TILE_M) || !ok_x) return cudaErrorInvalidValue;
   using Smem = PipeSmem<TILE_M * TC_BK * 2, TB * TC_BK * 2, STAGES>;
   // One CTA per SM; the parked pieces and counters are sized for kMaxSmsForSizing.
   const int grid = std::min(sm_count, kMaxSmsForSizing);
-  return launch_pipe(tc_ffn_kernel<TB, STAGES, EPI>, sizeof(Smem) + 1024, grid, tmW, tmX, a,
-                     stream);
+  if constexpr (EPI == EPI_BIAS_SILU) {
+    if (a.gather_rows)
+      return launch_pipe(tc_ffn_kernel<TB, STAGES, EPI, true>,
+                         sizeof(Smem) + 1024 + TB * sizeof(int) + 16, grid, tmW, tmX, a, stream);
+  }
+  if (a.gather_rows) return cudaErrorInvalidValue;
+  return launch_pipe(tc_ffn_kernel<TB, STAGES, EPI, false>, sizeof(Smem) + 1024, grid, tmW, tmX,
+                     a, stream);
 }
 
 template <int BN, int STAGES, int EPI>
 cudaError_t launch_rows_ffn(const GemmArgs& a, int sm_count, cudaStream_t stream) {
   CUtensorMap tmX, tmW;
-  if (!rows_map(&tmX, a.A, a.rows_alloc, a.K, TILE_M) || !stacked_map(&tmW, a.B, a.G, a.N, a.K, BN))
-    return cudaErrorInvalidValue;
+  // Token rows: 128-row boxes of the expert-ordered rows, or one-row boxes of x to gather.
+  const bool ok_x = a.gather_rows ? rows_map(&tmX, a.gather_src, a.gather_src_rows, a.K, 1)
+                                  : rows_map(&tmX, a.A, a.rows_alloc, a.K, TILE_M);
+  if (!ok_x || !stacked_map(&tmW, a.B, a.G, a.N, a.K, BN)) return cudaErrorInvalidValue;
   // Upper bound on tiles: sum_g ceil(rows_g / 128) <= rows_alloc / 128 + G.
   const int64_t bound = ((a.rows_alloc + TILE_M - 1) / TILE_M + a.G) * ((a.N + BN - 1) / BN);
   const int grid = static_cast<int>(std::min<int64_t>(bound, sm_count));
@@ -625,13 +698,19 @@ cudaError_t launch_rows_ffn(const GemmArgs& a, int sm_count, cudaStream_t stream
   CUtensorMap tmO;
   if (!rows_map(&tmO, a.out, a.rows_alloc, a.N, 32)) return cudaErrorInvalidValue;
   const size_t smem = ((sizeof(Smem) + 1023) & ~size_t{1023}) + 8 * 4096 + 1024;
-  auto kern = tc_rows_ffn_kernel<BN, STAGES, EPI>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
-  if (e != cudaSuccess) return e;
-  if (grid <= 0) return cudaSuccess;
-  launch_pdl(kern, grid, ROWS_THREADS, smem, stream, tmX, tmW, tmO, a);
-  return cudaGetLastError();
+  auto go = [&](auto kern) -> cudaError_t {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    if (grid <= 0) return cudaSuccess;
+    launch_pdl(kern, grid, ROWS_THREADS, smem, stream, tmX, tmW, tmO, a);
+    return cudaGetLastError();
+  };
+  if constexpr (EPI == EPI_BIAS_SILU) {
+    if (a.gather_rows) return go(tc_rows_ffn_kernel<BN, STAGES, EPI, true>);
+  }
+  if (a.gather_rows) return cudaErrorInvalidValue;
+  return go(tc_rows_ffn_kernel<BN, STAGES, EPI, false>);
 }
 
 template <int BN, int STAGES>
@@ -676,6 +755,9 @@ int router_splits(int64_t T, int E, int d, int sms) {
 }
 
 cudaError_t launch_tc_gemm_bf16(const GemmArgs& a, int epi, int sm_count, cudaStream_t stream) {
+  // Gathered token rows exist for the first expert GEMM only.
+  if (a.gather_rows && (epi != EPI_BIAS_SILU || !a.gather_src || a.gather_src_rows < 1))
+    return cudaErrorInvalidValue;
   switch (epi) {
     case EPI_BIAS_SILU:
       return a.max_group > kSmallGroup ? launch_rows_ffn<256, 4, EPI_BIAS_SILU>(a, sm_count, stream)

@@ -33,7 +33,7 @@ cudaError_t launch_dispatch_hist(const int32_t* topk_idx, int64_t T, int E, int 
                                  int* flags, cudaStream_t stream);
 
 // D2 + D3: stable positions, capacity drop, slot_row / row_token and the expert-ordered
-// rows (copied token by token to each kept row).
+// rows (copied token by token to each kept row; not copied when x_perm is nullptr).
 cudaError_t launch_dispatch_place(int dtype, const int32_t* topk_idx, int64_t T, int E, int k,
                                   int64_t C, const int32_t* chunk_base, const int32_t* offsets,
                                   int32_t* slot_row, int32_t* row_token, const void* x,
@@ -93,6 +93,12 @@ struct GemmArgs {
   // split_part_floats(max_group) floats for the pieces of split tiles.
   int* sk_ctr;
   float* sk_part;
+  // Expert GEMM 1 only: when gather_rows is given, the token rows of row r are read
+  // straight from gather_src [gather_src_rows, K] at row gather_rows[r] (the dispatch's
+  // row -> token map) instead of from A, which is then not read.
+  const int32_t* gather_rows;
+  const void* gather_src;
+  int64_t gather_src_rows;
 };
 
 // K splits of the bf16 router contraction for T tokens, E experts, model width d on a

@@ -87,7 +87,7 @@ Layout make_layout(const moe_config& c) {
   L.slot_row = o; o = align_up(o + T * k * 4);
   L.row_token = o; o = align_up(o + T * k * 4);
   L.dropped = o; o = align_up(o + 4);
-  L.x_perm = o; o = align_up(o + T * k * c.d * s);
+  L.x_perm = o; if (!c.fused_gather) o = align_up(o + T * k * c.d * s);
   L.h_buf = o; o = align_up(o + T * k * c.h * s);
   L.y_perm = o; o = align_up(o + T * k * c.d * s);
   L.total = o;
@@ -107,6 +107,8 @@ moe_status check_config(const moe_config* c) {
   if (!std::isfinite(c->capacity_factor)) return MOE_ERR_INVALID_ARGUMENT;
   if (c->noise < MOE_NOISE_NONE || c->noise > MOE_NOISE_LOGIT_SOFTMAX)
     return MOE_ERR_INVALID_ARGUMENT;
+  if (c->fused_gather != 0 && c->fused_gather != 1) return MOE_ERR_INVALID_ARGUMENT;
+  if (c->fused_gather && c->dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
   if (c->T < 0 || c->k < 1 || c->k > kMaxK || c->E < c->k || c->E > kMaxExperts)
     return MOE_ERR_UNSUPPORTED;
   if (c->d < 8 || c->d % 8 != 0 || c->h < 8 || c->h % 8 != 0) return MOE_ERR_UNSUPPORTED;
@@ -211,7 +213,8 @@ moe_status run_expert_ffn_rows(const moe_config& c, int64_t rows_alloc, int64_t 
                                const void* x_perm, const int32_t* offsets, const void* w1,
                                const void* b1, const void* w2, const void* b2, void* h_buf,
                                void* y_perm, int* flags, int* sk_ctr, float* sk_part, int sms,
-                               cudaStream_t st, void* h_pre = nullptr) {
+                               cudaStream_t st, void* h_pre = nullptr,
+                               const int32_t* gather_rows = nullptr, const void* x = nullptr) {
   GemmArgs g1{};
   g1.A = x_perm;
   g1.pre_out = h_pre;
@@ -227,8 +230,13 @@ moe_status run_expert_ffn_rows(const moe_config& c, int64_t rows_alloc, int64_t 
   g1.flags = flags;
   g1.sk_ctr = sk_ctr;
   g1.sk_part = sk_part;
+  g1.gather_rows = gather_rows;
+  g1.gather_src = x;
+  g1.gather_src_rows = c.T;
   GemmArgs g2 = g1;
   g2.sk_ctr = sk_ctr + kSplitCounters;
+  g2.gather_rows = nullptr;
+  g2.gather_src = nullptr;
   g2.A = h_buf;
   g2.pre_out = nullptr;
   g2.B = w2;
@@ -251,10 +259,11 @@ moe_status run_expert_ffn_rows(const moe_config& c, int64_t rows_alloc, int64_t 
 moe_status run_expert_ffn(const moe_config& c, const Layout& L, void* ws, const void* x_perm,
                           const int32_t* offsets, const void* w1, const void* b1, const void* w2,
                           const void* b2, void* h_buf, void* y_perm, int* flags, int sms,
-                          cudaStream_t st, void* h_pre = nullptr) {
+                          cudaStream_t st, void* h_pre = nullptr,
+                          const int32_t* gather_rows = nullptr, const void* x = nullptr) {
   return run_expert_ffn_rows(c, c.T * c.k, max_group_of(c), x_perm, offsets, w1, b1, w2, b2, h_buf,
                              y_perm, flags, at<int>(ws, L.split_ctr), at<float>(ws, L.split_part),
-                             sms, st, h_pre);
+                             sms, st, h_pre, gather_rows, x);
 }
 
 // ---------------------------------------------------------------- expert choice
@@ -278,6 +287,8 @@ moe_status check_ec_config(const moe_config* c) {
   if (!std::isfinite(c->capacity_factor) || !(c->capacity_factor > 0.0))
     return MOE_ERR_INVALID_ARGUMENT;
   if (c->noise != MOE_NOISE_NONE) return MOE_ERR_INVALID_ARGUMENT;
+  if (c->fused_gather != 0 && c->fused_gather != 1) return MOE_ERR_INVALID_ARGUMENT;
+  if (c->fused_gather) return MOE_ERR_UNSUPPORTED;  // top-k layers only
   if (c->T < 0 || c->T >= (int64_t{1} << 31) || c->E < 1 || c->E > kMaxExperts)
     return MOE_ERR_UNSUPPORTED;
   if (c->d < 8 || c->d % 8 != 0 || c->h < 8 || c->h % 8 != 0) return MOE_ERR_UNSUPPORTED;
@@ -517,15 +528,19 @@ moe_status moe::forward_entry(const moe_config* cfg, const moe_forward_args* a, 
     MOE_CUDA(launch_route_finalize(hist, psum, static_cast<int>(L.nchunks), c.E, c.T, C, counts,
                                    aux, chunk_base, kept, offsets, dropped, a->routing_stats, st));
   }
+  // cfg->fused_gather: GEMM1 reads the token rows from x by row_token, and no expert-ordered
+  // copy exists (unless the caller asked for one in x_perm).
+  const bool gather = c.fused_gather && a->x_perm == nullptr;
   {
     MOE_TRACE("moe_forward: dispatch");
     MOE_CUDA(launch_dispatch_place(c.dtype, idx, c.T, c.E, c.k, C, chunk_base, offsets, slot_row,
-                                   row_token, a->x, x_perm, c.d, flags, st));
+                                   row_token, a->x, gather ? nullptr : x_perm, c.d, flags, st));
   }
   {
     MOE_TRACE("moe_forward: expert_ffn");
     if ((s = run_expert_ffn(c, L, ws, x_perm, offsets, a->w1, a->b1, a->w2, a->b2, h_buf, y_perm,
-                            flags, sms, st, a->h_pre)) != MOE_OK)
+                            flags, sms, st, a->h_pre, gather ? row_token : nullptr,
+                            gather ? a->x : nullptr)) != MOE_OK)
       return s;
   }
   {

@@ -180,6 +180,50 @@ __device__ __forceinline__ void run_producer(Smem& S, int first, int step, int t
   }
 }
 
+// run_producer for the whole warp 0: before each tile's first k-block every lane calls
+// prepare(coords, lane) (work spread over the warp, such as fetching a tile's row
+// indices into shared memory, finished before lane 0 issues that tile's copies); the
+// ring waits and load(coords, kb, smem_a, smem_b, bar) are lane 0's.
+template <int STAGES, class Smem, class Decode, class Prepare, class Load>
+__device__ __forceinline__ void run_producer_warp(Smem& S, int first, int step, int total,
+                                                  Decode decode, Prepare prepare, Load load,
+                                                  volatile int* abort, int* flags) {
+  const int lane = threadIdx.x & 31;
+  int s = 0;
+  uint32_t ph = 0, issued = 0, issued_par = 0;
+  bool ok = true;
+  for (int tile = first; ok && tile < total; tile += step) {
+    const auto c = decode(tile);
+    __syncwarp();  // lane 0 has issued the previous tile's copies
+    prepare(c, lane);
+    __syncwarp();
+    for (int kb = c.kb0; kb < c.kb1; ++kb) {
+      bool got = true;
+      if (lane == 0) got = mbar_wait_bounded(smem_u32(&S.empty[s]), ph ^ 1u, abort, flags);
+      if (!__shfl_sync(0xffffffffu, got ? 1 : 0, 0)) {
+        ok = false;
+        break;
+      }
+      if (lane == 0) {
+        const uint32_t fb = smem_u32(&S.full[s]);
+        mbar_arrive_expect_tx(fb, c.bytes);
+        load(c, kb, smem_u32(S.a[s]), smem_u32(S.b[s]), fb);
+        issued |= 1u << s;
+        issued_par = (issued_par & ~(1u << s)) | (ph << s);
+      }
+      if (++s == STAGES) {
+        s = 0;
+        ph ^= 1u;
+      }
+    }
+  }
+  if (!ok && lane == 0) {
+    // Unwinding: let this CTA's copies in flight land before it exits.
+    for (int q = 0; q < STAGES; ++q)
+      if ((issued >> q) & 1u) mbar_wait_unwind(smem_u32(&S.full[q]), (issued_par >> q) & 1u);
+  }
+}
+
 // Warp 1, lane 0.  decode(tile) -> coordinates with the k-block range [.kb0, .kb1);
 // idesc_of(coords) -> instruction descriptor of the tile's MMAs.  B_MN: the B stage
 // holds MN-major boxes of [64 K rows x 64 N] (8 KB apart) instead of one K-major box.

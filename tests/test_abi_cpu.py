@@ -83,12 +83,15 @@ def test_status_strings(L):
     (dict(capacity_factor=float("nan")), moe.MOE_ERR_INVALID_ARGUMENT),
     (dict(noise=4), moe.MOE_ERR_INVALID_ARGUMENT),
     (dict(noise=-1), moe.MOE_ERR_INVALID_ARGUMENT),
+    (dict(fused_gather=2), moe.MOE_ERR_INVALID_ARGUMENT),
+    (dict(fused_gather=1, dtype=0), moe.MOE_ERR_UNSUPPORTED),
 ])
 def test_config_validation(L, kw, status):
-    base = dict(T=64, d=64, h=128, E=8, k=2, dtype=1, gate=0, capacity_factor=0.0, noise=0)
+    base = dict(T=64, d=64, h=128, E=8, k=2, dtype=1, gate=0, capacity_factor=0.0, noise=0,
+                fused_gather=0)
     base.update(kw)
     cfg = moe.MoeConfig(base["T"], base["d"], base["h"], base["E"], base["k"], base["dtype"],
-                        base["gate"], base["capacity_factor"], base["noise"])
+                        base["gate"], base["capacity_factor"], base["noise"], base["fused_gather"])
     n = ctypes.c_size_t()
     assert L.moe_workspace_size(ctypes.byref(cfg), ctypes.byref(n)) == status
     assert L.moe_route(ctypes.byref(cfg), FAKE, FAKE, None, None, None, FAKE, FAKE, None, None, None, FAKE, 1 << 40, None) == status
@@ -115,6 +118,21 @@ def test_workspace_sizes_cover_buffers(L):
     assert full % 256 == 0 and stage % 256 == 0
     c32 = moe.config(4096, 4096, 14336, 8, 2, "f32")
     assert moe.moe_workspace_size(c32) > full
+
+
+def test_fused_gather_drops_the_row_copy_from_the_workspace(L):
+    """With fused_gather the forward's workspace holds no expert-ordered copy of the token
+    rows: exactly T*k*d*2 bytes less (rounded to the 256-byte region alignment); the stage
+    workspace is unchanged, and expert-choice routing refuses the flag."""
+    T, d, h, E, k = 8192, 7168, 2048, 256, 8
+    plain = moe.config(T, d, h, E, k, "bf16", gate=1)
+    fused = moe.config(T, d, h, E, k, "bf16", gate=1, fused_gather=1)
+    assert moe.moe_workspace_size(plain) - moe.moe_workspace_size(fused) == T * k * d * 2
+    assert moe.moe_stage_workspace_size(plain) == moe.moe_stage_workspace_size(fused)
+    ec = moe.config(T, d, h, E, k, "bf16", gate=1, capacity_factor=8.0, fused_gather=1)
+    n = ctypes.c_size_t()
+    assert L.moe_expert_choice_workspace_size(ctypes.byref(ec), ctypes.byref(n)) == \
+        moe.MOE_ERR_UNSUPPORTED
 
 
 def test_required_pointers_and_alignment(L):

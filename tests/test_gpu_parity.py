@@ -239,6 +239,65 @@ def test_split_tiles_deterministic(w):
         np.testing.assert_array_equal(y.float().cpu().numpy(), a["y"])
 
 
+FUSED = [w for w in list(PARITY_WORKLOADS.values()) + EDGE if w.dtype == "bf16"]
+
+
+@pytest.mark.parametrize("w", FUSED, ids=[w.name for w in FUSED])
+def test_fused_gather_is_bitwise_the_forward(w):
+    """cfg.fused_gather: GEMM1 reads the token rows from x through the row -> token map
+    (both expert GEMM kernels, split tiles, ragged tails, one-token batches): every output
+    is bitwise the default forward's, on a workspace without the row copy."""
+    dev = tl.to_device(make_inputs(w, seed=9))
+    a = tl.host(tl.run_forward(w, dev)["outs"])
+    cfg = moe.config_from_workload(w, fused_gather=1)
+    r = tl.run_forward(w, dev, cfg=cfg)
+    assert r["flags"] == 0
+    assert r["ws"].numel() < moe.moe_workspace_size(moe.config_from_workload(w))
+    b = tl.host(r["outs"])
+    for key in a:
+        np.testing.assert_array_equal(b[key], a[key], err_msg=key)
+
+
+def test_fused_gather_with_x_perm_output():
+    """A fused_gather forward that is given an x_perm buffer fills it (the rows in expert
+    order, as the default forward writes them) and returns the same outputs."""
+    w = PARITY_WORKLOADS["switch_capacity"]  # capacity drops: fewer rows than T*k
+    dev = tl.to_device(make_inputs(w, seed=4))
+    outs = tl.alloc_outputs(w, "cuda")
+    outs["x_perm"] = torch.full((w.T * w.k, w.d), float("nan"), dtype=w.torch_dtype,
+                                device="cuda")
+    a = tl.host(tl.run_forward(w, dev, outs=outs)["outs"])
+    outs2 = {k: torch.full_like(v, -7 if v.dtype == torch.int32 else float("nan"))
+             for k, v in outs.items()}
+    r = tl.run_forward(w, dev, outs=outs2, cfg=moe.config_from_workload(w, fused_gather=1))
+    assert r["flags"] == 0
+    b = tl.host(r["outs"])
+    M = int(a["offsets"][-1])
+    np.testing.assert_array_equal(b["x_perm"][:M], a["x_perm"][:M])
+    for key in a:
+        if key != "x_perm":
+            np.testing.assert_array_equal(b[key], a[key], err_msg=key)
+
+
+@pytest.mark.parametrize("name", ["mixtral_prefill", "switch_capacity", "decode"])
+def test_fused_gather_full_size(name):
+    """The same at the benchmark's sizes: row tiles (prefill) and weights-as-M tiles with
+    and without split tiles (Switch, decode)."""
+    w = WORKLOADS[name]
+    inp = make_inputs(w, seed=0, device="cuda")
+    outs = dict(y=torch.empty((w.T, w.d), dtype=w.torch_dtype, device="cuda"))
+    ws = torch.empty(moe.moe_workspace_size(moe.config_from_workload(w)), dtype=torch.uint8,
+                     device="cuda")
+    moe.moe_forward(moe.config_from_workload(w), inp, outs, ws)
+    assert moe.moe_device_error(ws) == 0
+    y0 = outs["y"].clone()
+    cfg = moe.config_from_workload(w, fused_gather=1)
+    ws = torch.empty(moe.moe_workspace_size(cfg), dtype=torch.uint8, device="cuda")
+    moe.moe_forward(cfg, inp, outs, ws)
+    assert moe.moe_device_error(ws) == 0
+    assert torch.equal(outs["y"], y0)
+
+
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_all_ties_and_drop_storm(dtype):
     """W_g = 0: every logit ties, so every token picks experts 0..k-1; with capacity 1.25
