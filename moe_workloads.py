@@ -117,6 +117,9 @@ EC_PARITY_WORKLOADS = {
     "deepseek_fine_ec": WORKLOADS["deepseek_fine_ec"].scaled(T=389, d=512, h=256),
     "decode_ec": WORKLOADS["decode"].scaled(name="decode_ec", routing="expert_choice", d=512,
                                             h=768, capacity_factor=1.0),
+    # C = 544 rows per expert: the 256-row tile kernel (two full tiles and a half tile).
+    "wide_ec": WORKLOADS["mixtral_prefill_ec"].scaled(name="wide_ec", T=1088, E=4, d=256,
+                                                       h=512),
 }
 
 

@@ -323,6 +323,141 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   pipe_teardown(S, kTmemCols);
 }
 
+// Bias (and SiLU) of 32 accumulator columns of one row, packed to bf16: v holds the fp32
+// accumulators, bias (or null) the 32 columns' biases; pre receives the packed
+// pre-activation when the epilogue is SiLU.
+template <int EPI>
+__device__ __forceinline__ void bias_act_32(const float (&v)[32], const uint4 (&bias)[4],
+                                           bool has_bias, uint4 (&packed)[4], uint4 (&pre)[4]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    float b[8];
+    if (has_bias) {
+      const __nv_bfloat162* bh = reinterpret_cast<const __nv_bfloat162*>(&bias[q]);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(bh[i]);
+        b[2 * i] = f.x;
+        b[2 * i + 1] = f.y;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) b[i] = 0.f;
+    }
+    __nv_bfloat162* ph = reinterpret_cast<__nv_bfloat162*>(&packed[q]);
+    __nv_bfloat162* pp = reinterpret_cast<__nv_bfloat162*>(&pre[q]);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float x0 = v[8 * q + 2 * i] + b[2 * i];
+      float x1 = v[8 * q + 2 * i + 1] + b[2 * i + 1];
+      if (EPI == EPI_BIAS_SILU) {
+        pp[i] = __floats2bfloat162_rn(x0, x1);
+        x0 = silu(x0);
+        x1 = silu(x1);
+      }
+      ph[i] = __floats2bfloat162_rn(x0, x1);
+    }
+  }
+}
+
+// One epilogue warp's share of a 128-row accumulator: its 32 TMEM lanes starting at t_row
+// (output rows store_row ... store_row + 31; this lane's row is `row`), accumulator
+// columns [col_lo, col_lo + COLS) of the tile that starts at output column n0, 64 at a
+// time.  Adds the bias, applies the activation and writes bf16: through the warp's 4 KB
+// staging box and one TMA store per 64 columns when use_tma (all 32 rows in the group,
+// the columns in range, no pre-activation output), else with 16-byte stores per row,
+// skipping a row past the group's end (valid false) and columns past N.  The 64 columns
+// and their biases are loaded and converted before the warp waits for its previous
+// store to have read the staging box, so that read overlaps the arithmetic.
+template <int EPI, int COLS>
+__device__ __forceinline__ void rows_epilogue_slab(uint32_t t_row, int col_lo, bool use_tma,
+                                                   int64_t row, bool valid, int n0, int N,
+                                                   const __nv_bfloat16* bias,
+                                                   __nv_bfloat16* out, void* pre_out,
+                                                   uint8_t* stg, const CUtensorMap* tmO,
+                                                   int store_row, int lane) {
+  static_assert(COLS % 64 == 0, "64-column pieces");
+#pragma unroll 1
+  for (int col = col_lo; col < col_lo + COLS; col += 64) {
+    float v0[32], v1[32];
+    if (use_tma) {
+      // use_tma: every column of the piece is in range.
+      uint4 bv[2][4];
+      if (bias) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          bv[i / 4][i % 4] = __ldg(reinterpret_cast<const uint4*>(bias + col + 8 * i));
+      }
+      uint4 packed[2][4], pre[4];
+      tmem_ld_32cols(t_row + col, v0);
+      tmem_ld_32cols(t_row + col + 32, v1);
+      tc_wait_ld();
+      bias_act_32<EPI>(v0, bv[0], bias != nullptr, packed[0], pre);
+      bias_act_32<EPI>(v1, bv[1], bias != nullptr, packed[1], pre);
+      if (lane == 0) bulk_wait_group_read0();
+      __syncwarp();
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int chunk = i ^ (lane & 7);
+        *reinterpret_cast<uint4*>(stg + lane * 128 + chunk * 16) = packed[i / 4][i % 4];
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_2d(tmO, smem_u32(stg), n0 + col, store_row);
+        bulk_commit_group();
+      }
+      continue;
+    }
+    // Rows or columns at an edge (or a pre-activation output): 16-byte stores per row.
+    auto direct = [&](const float (&v)[32], int c0) {
+      if (!valid || n0 + c0 >= N) return;
+      const bool full32 = n0 + c0 + 32 <= N;
+      uint4 b32[4];
+      if (bias && full32) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) b32[q] = __ldg(reinterpret_cast<const uint4*>(bias + c0 + 8 * q));
+      } else {
+        // Columns past N: biases of the columns in range, zeros beyond.
+        __nv_bfloat16* bh = reinterpret_cast<__nv_bfloat16*>(b32);
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          bh[i] = (bias && n0 + c0 + i < N) ? bias[c0 + i] : __float2bfloat16(0.f);
+      }
+      uint4 packed[4], pre[4];
+      bias_act_32<EPI>(v, b32, bias != nullptr, packed, pre);
+      __nv_bfloat16* o = out + row * N + n0 + c0;
+      __nv_bfloat16* op = (EPI == EPI_BIAS_SILU && pre_out)
+                              ? static_cast<__nv_bfloat16*>(pre_out) + (o - out)
+                              : nullptr;
+      if (full32) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          *reinterpret_cast<uint4*>(o + 8 * q) = packed[q];
+          if (op) *reinterpret_cast<uint4*>(op + 8 * q) = pre[q];
+        }
+      } else {
+        const __nv_bfloat16* pv = reinterpret_cast<const __nv_bfloat16*>(packed);
+        const __nv_bfloat16* pr = reinterpret_cast<const __nv_bfloat16*>(pre);
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (n0 + c0 + i < N) {
+            o[i] = pv[i];
+            if (op) op[i] = pr[i];
+          }
+      }
+    };
+    __syncwarp();  // the TMEM loads are warp-collective
+    tmem_ld_32cols(t_row + col, v0);
+    tc_wait_ld();
+    direct(v0, col);
+    __syncwarp();
+    tmem_ld_32cols(t_row + col + 32, v1);
+    tc_wait_ld();
+    direct(v1, col + 32);
+  }
+}
+
 // ------------------------------------------------------------- expert FFN, row tiles
 // A = token block [128 x 64] of the row buffer (2-D map); B = weight block [BN x 64]
 // of W[g] (3-D map over [G, N, K]); D[128 x BN] in TMEM, lane = token row, column =
@@ -445,110 +580,9 @@ __global__ void __launch_bounds__(ROWS_THREADS, 1)
                              static_cast<uint32_t>(acc * BN);
       const __nv_bfloat16* bias =
           bias_base ? bias_base + static_cast<int64_t>(c.g) * p.N + c.n0 : nullptr;
-#pragma unroll 1
-      for (int col = col_lo; col < col_lo + kColsPerWarp; col += 32) {
-        float v[32];
-        if (use_tma && (col % 64) == 0) {
-          if (lane == 0) bulk_wait_group_read0();
-          __syncwarp();
-        }
-        tmem_ld_32cols(t_row + col, v);
-        tc_wait_ld();
-        if (use_tma) {
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            float b[8];
-            if (bias) {
-              const uint4 bv = __ldg(reinterpret_cast<const uint4*>(bias + col + 8 * q));
-              const __nv_bfloat162* bh = reinterpret_cast<const __nv_bfloat162*>(&bv);
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                const float2 f = __bfloat1622float2(bh[i]);
-                b[2 * i] = f.x;
-                b[2 * i + 1] = f.y;
-              }
-            } else {
-#pragma unroll
-              for (int i = 0; i < 8; ++i) b[i] = 0.f;
-            }
-            uint4 packed;
-            __nv_bfloat162* ph = reinterpret_cast<__nv_bfloat162*>(&packed);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              float x0 = v[8 * q + 2 * i] + b[2 * i];
-              float x1 = v[8 * q + 2 * i + 1] + b[2 * i + 1];
-              if (EPI == EPI_BIAS_SILU) {
-                x0 = silu(x0);
-                x1 = silu(x1);
-              }
-              ph[i] = __floats2bfloat162_rn(x0, x1);
-            }
-            const int chunk = ((col % 64) / 8 + q) ^ (lane & 7);
-            *reinterpret_cast<uint4*>(stg + lane * 128 + chunk * 16) = packed;
-          }
-          if ((col % 64) == 32) {
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-              tma_store_2d(&tmO, smem_u32(stg), c.n0 + col - 32, static_cast<int>(c.row0) + quad * 32);
-              bulk_commit_group();
-            }
-          }
-          continue;
-        }
-        if (!valid || c.n0 + col >= p.N) continue;
-        __nv_bfloat16* o = out + row * p.N + c.n0 + col;
-        const bool whole = c.n0 + col + 32 <= p.N;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          float b[8];
-          if (bias && whole) {
-            const uint4 bv = __ldg(reinterpret_cast<const uint4*>(bias + col + 8 * q));
-            const __nv_bfloat162* bh = reinterpret_cast<const __nv_bfloat162*>(&bv);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const float2 f = __bfloat1622float2(bh[i]);
-              b[2 * i] = f.x;
-              b[2 * i + 1] = f.y;
-            }
-          } else {
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-              b[i] = (bias && c.n0 + col + 8 * q + i < p.N) ? __bfloat162float(bias[col + 8 * q + i])
-                                                              : 0.f;
-          }
-          uint4 packed, pre;
-          __nv_bfloat162* ph = reinterpret_cast<__nv_bfloat162*>(&packed);
-          __nv_bfloat162* pp = reinterpret_cast<__nv_bfloat162*>(&pre);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            float x0 = v[8 * q + 2 * i] + b[2 * i];
-            float x1 = v[8 * q + 2 * i + 1] + b[2 * i + 1];
-            if (EPI == EPI_BIAS_SILU) {
-              pp[i] = __floats2bfloat162_rn(x0, x1);
-              x0 = silu(x0);
-              x1 = silu(x1);
-            }
-            ph[i] = __floats2bfloat162_rn(x0, x1);
-          }
-          __nv_bfloat16* op = (EPI == EPI_BIAS_SILU && p.pre_out)
-                                  ? static_cast<__nv_bfloat16*>(p.pre_out) + (o - out)
-                                  : nullptr;
-          if (whole) {
-            *reinterpret_cast<uint4*>(o + 8 * q) = packed;
-            if (op) *reinterpret_cast<uint4*>(op + 8 * q) = pre;
-          } else {
-            const __nv_bfloat16* pv = reinterpret_cast<const __nv_bfloat16*>(&packed);
-            const __nv_bfloat16* pr = reinterpret_cast<const __nv_bfloat16*>(&pre);
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-              if (c.n0 + col + 8 * q + i < p.N) {
-                o[8 * q + i] = pv[i];
-                if (op) op[8 * q + i] = pr[i];
-              }
-          }
-        }
-      }
+      rows_epilogue_slab<EPI, kColsPerWarp>(t_row, col_lo, use_tma, row, valid, c.n0, p.N, bias,
+                                           out, p.pre_out, stg, &tmO,
+                                           static_cast<int>(c.row0) + quad * 32, lane);
       tc_fence_before();
       mbar_arrive(smem_u32(&S.tempty[acc]));
       acc ^= 1;
@@ -663,6 +697,171 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   pipe_teardown(S, kTmemCols);
 }
 
+// Expert GEMM on 256-row token tiles (groups larger than 128 rows).  A k-block stage holds
+// the tile's two 128-row token halves and one 256-row block of the weights, and the MMA
+// thread issues both halves against the shared weight block into two accumulators (TMEM
+// columns 0-255 and 256-511): 64 KB of operands per 2 x (128 x 256 x 64) MMAs, where two
+// 128-row tiles need 96 KB, so the same shared-memory ring (three 64 KB stages instead of
+// four of 48 KB) carries a third more MMA work per byte -- the main loop of the 128-row
+// kernel waits on operand delivery, not on the tensor core.  With all 512 columns in use
+// the accumulators are not double-buffered: the epilogue drains the first half and
+// releases it before the second, so the next tile's first-half MMAs start during the
+// second half's drain while the producer refills the ring.  A tile with at most 128 rows
+// left (a group's tail) loads and computes only its first half.
+template <int STAGES, int EPI, int EPI_WARPS, bool STAGED>
+__global__ void __launch_bounds__(64 + 32 * EPI_WARPS, 1)
+    tc_rows_wide_ffn_kernel(const __grid_constant__ CUtensorMap tmX,
+                            const __grid_constant__ CUtensorMap tmW,
+                            const __grid_constant__ CUtensorMap tmO, const GemmArgs p) {
+  static_assert(EPI == EPI_BIAS_SILU || EPI == EPI_BIAS, "expert epilogues only");
+  static_assert(EPI_WARPS % 4 == 0 && EPI_WARPS >= 4 && EPI_WARPS <= 16, "whole lane quadrants");
+  constexpr int BN = 256;
+  constexpr int TM = 2 * TILE_M;
+  constexpr uint32_t kTmemCols = 2 * BN;
+  constexpr uint32_t kIdesc = bf16_idesc(TILE_M, BN);
+  constexpr uint32_t kHalfBytes = TILE_M * TC_BK * 2;
+  constexpr uint32_t kWeightBytes = BN * TC_BK * 2;
+  using Smem = PipeSmem<2 * kHalfBytes, kWeightBytes, STAGES>;
+  Smem& S = smem_aligned<Smem>();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = p.G;
+  pipe_prologue<Smem, STAGES>(S, kTmemCols, p, G, TM, &tmX, &tmW, 32 * EPI_WARPS);
+
+  const int NB = (p.N + BN - 1) / BN;
+  const int total = S.pref[G] * NB;
+  const int KB = (p.K + TC_BK - 1) / TC_BK;
+  volatile int* abort = &S.abort;
+
+  struct Coord {
+    int g, n0, kb0, kb1;
+    bool two;  // the second 128-row half holds rows of the group
+    uint32_t bytes;
+    int64_t row0, row_end;
+  };
+  auto decode = [&](int tile) {
+    Coord c;
+    c.g = find_group(S.pref, G, NB, tile);
+    const int mt = S.pref[c.g + 1] - S.pref[c.g];
+    const int local = tile - S.pref[c.g] * NB;
+    c.n0 = (local / mt) * BN;
+    c.row0 = p.offsets[c.g] + static_cast<int64_t>(local % mt) * TM;
+    c.row_end = p.offsets[c.g + 1];
+    c.two = c.row_end - c.row0 > TILE_M;
+    c.bytes = kWeightBytes + (c.two ? 2u : 1u) * kHalfBytes;
+    c.kb0 = 0;
+    c.kb1 = KB;
+    return c;
+  };
+  const int first = static_cast<int>(blockIdx.x), step = static_cast<int>(gridDim.x);
+
+  if (warp == 0) {
+    if (lane == 0)
+      run_producer<STAGES>(
+          S, first, step, total, decode,
+          [&](const Coord& c, int kb, uint32_t sa, uint32_t sb, uint32_t bar) {
+            tma_load_2d(sa, &tmX, bar, kb * TC_BK, static_cast<int>(c.row0));
+            if (c.two)
+              tma_load_2d(sa + kHalfBytes, &tmX, bar, kb * TC_BK, static_cast<int>(c.row0) + TILE_M);
+            tma_load_3d(sb, &tmW, bar, kb * TC_BK, c.n0, c.g);
+          },
+          abort, p.flags);
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // tempty[h]: the epilogue has drained accumulator half h of the previous tile (it
+      // arrives on both once per tile, also for a one-half tile); tfull[0]: the tile's MMAs
+      // are complete.
+      int s = 0;
+      uint32_t ph = 0, aph = 0;
+      bool ok = true, issued_any = false;
+      for (int tile = first; ok && tile < total; tile += step) {
+        const Coord c = decode(tile);
+        if (!mbar_wait_bounded(smem_u32(&S.tempty[0]), aph ^ 1u, abort, p.flags)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        for (int kb = c.kb0; kb < c.kb1; ++kb) {
+          if (!mbar_wait_bounded(smem_u32(&S.full[s]), ph, abort, p.flags)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(S.a[s]), b0 = smem_u32(S.b[s]);
+#pragma unroll
+          for (int kk = 0; kk < TC_BK / 16; ++kk)
+            tc_mma_bf16(S.tmem_base, sw128_kmajor_desc(a0 + kk * 32),
+                        sw128_kmajor_desc(b0 + kk * 32), kIdesc,
+                        (kb != c.kb0 || kk != 0) ? 1u : 0u);
+          issued_any = true;
+          if (c.two) {
+            if (kb == c.kb0) {
+              if (!mbar_wait_bounded(smem_u32(&S.tempty[1]), aph ^ 1u, abort, p.flags)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+            }
+#pragma unroll
+            for (int kk = 0; kk < TC_BK / 16; ++kk)
+              tc_mma_bf16(S.tmem_base + BN, sw128_kmajor_desc(a0 + kHalfBytes + kk * 32),
+                          sw128_kmajor_desc(b0 + kk * 32), kIdesc,
+                          (kb != c.kb0 || kk != 0) ? 1u : 0u);
+          }
+          tc_commit(smem_u32(&S.empty[s]));
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit(smem_u32(&S.tfull[0]));
+        aph ^= 1u;
+      }
+      // Unwinding: every MMA issued by this thread completes before TMEM is released.
+      if (!ok && issued_any) {
+        tc_commit(smem_u32(&S.drain));
+        mbar_wait_unwind(smem_u32(&S.drain), 0);
+      }
+    }
+  } else {
+    const int quad = warp & 3;  // TMEM lanes this warp may read: 32*quad .. 32*quad+31
+    constexpr int kColsPerWarp = BN * 4 / EPI_WARPS;
+    const int col_lo = ((warp - 2) / 4) * kColsPerWarp;  // this warp's share of the columns
+    const __nv_bfloat16* bias_base = static_cast<const __nv_bfloat16*>(p.bias);
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
+    uint8_t* stg = reinterpret_cast<uint8_t*>(&S) + ((sizeof(Smem) + 1023) & ~size_t{1023}) +
+                   (warp - 2) * 4096;
+    uint32_t aph = 0;
+    for (int tile = first; tile < total; tile += step) {
+      const Coord c = decode(tile);
+      const bool got = mbar_wait_bounded(smem_u32(&S.tfull[0]), aph, abort, p.flags);
+      if (!__all_sync(0xffffffffu, got)) break;  // the warp-collective loads need every lane
+      tc_fence_after();
+      const __nv_bfloat16* bias =
+          bias_base ? bias_base + static_cast<int64_t>(c.g) * p.N + c.n0 : nullptr;
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h) {
+        if (h == 0 || c.two) {
+          const int64_t r0 = c.row0 + h * TILE_M + quad * 32;
+          const bool use_tma =
+              STAGED && p.pre_out == nullptr && r0 + 32 <= c.row_end &&
+              c.n0 + col_lo + kColsPerWarp <= p.N;
+          const uint32_t t_row =
+              S.tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(h * BN);
+          rows_epilogue_slab<EPI, kColsPerWarp>(t_row, col_lo, use_tma, r0 + lane,
+                                                r0 + lane < c.row_end, c.n0, p.N, bias, out,
+                                                p.pre_out, stg, &tmO, static_cast<int>(r0), lane);
+        }
+        tc_fence_before();
+        mbar_arrive(smem_u32(&S.tempty[h]));
+      }
+      aph ^= 1u;
+    }
+    if (lane == 0) bulk_wait_group0();
+  }
+  pipe_teardown(S, kTmemCols);
+}
+
 template <int TB, int STAGES, int EPI>
 cudaError_t launch_ffn(const GemmArgs& a, int sm_count, cudaStream_t stream) {
   if (!a.sk_ctr || !a.sk_part) return cudaErrorInvalidValue;
@@ -713,6 +912,28 @@ cudaError_t launch_rows_ffn(const GemmArgs& a, int sm_count, cudaStream_t stream
   return go(tc_rows_ffn_kernel<BN, STAGES, EPI, false>);
 }
 
+template <int STAGES, int EPI, int EPI_WARPS = ROWS_EPI_WARPS, bool STAGED = true>
+cudaError_t launch_rows_wide_ffn(const GemmArgs& a, int sm_count, cudaStream_t stream) {
+  constexpr int BN = 256, TM = 2 * TILE_M;
+  CUtensorMap tmX, tmW, tmO;
+  if (!rows_map(&tmX, a.A, a.rows_alloc, a.K, TILE_M) ||
+      !stacked_map(&tmW, a.B, a.G, a.N, a.K, BN) || !rows_map(&tmO, a.out, a.rows_alloc, a.N, 32))
+    return cudaErrorInvalidValue;
+  // Upper bound on tiles: sum_g ceil(rows_g / 256) <= rows_alloc / 256 + G.
+  const int64_t bound = ((a.rows_alloc + TM - 1) / TM + a.G) * ((a.N + BN - 1) / BN);
+  const int grid = static_cast<int>(std::min<int64_t>(bound, sm_count));
+  using Smem = PipeSmem<2 * TILE_M * TC_BK * 2, BN * TC_BK * 2, STAGES>;
+  const size_t smem =
+      ((sizeof(Smem) + 1023) & ~size_t{1023}) + (STAGED ? EPI_WARPS * 4096 : 0) + 1024;
+  auto kern = tc_rows_wide_ffn_kernel<STAGES, EPI, EPI_WARPS, STAGED>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  if (grid <= 0) return cudaSuccess;
+  launch_pdl(kern, grid, 64 + 32 * EPI_WARPS, smem, stream, tmX, tmW, tmO, a);
+  return cudaGetLastError();
+}
+
 template <int BN, int STAGES>
 cudaError_t launch_router(const GemmArgs& a, int sm_count, cudaStream_t stream) {
   CUtensorMap tmX, tmW;
@@ -754,16 +975,35 @@ int router_splits(int64_t T, int E, int d, int sms) {
   return static_cast<int>((kb + per - 1) / per);
 }
 
+// Groups larger than 128 rows.  256-row tiles carry a third more MMA work per operand
+// byte, which pays where each expert's weight blocks are reused by many row tiles (512 or
+// more rows per expert on average): there the tensor core bounds the main loop, and the
+// 256-row tiles run it about 1.4x faster per FLOP.  With fewer rows per expert the weight
+// stream from DRAM bounds both tile shapes, while the 256-row tiles pay for their
+// epilogue (their accumulators fill TMEM, so it does not overlap the next tile's MMAs) and
+// for half-empty last tiles.  Gathered token rows and a pre-activation output keep the
+// 128-row tiles (their epilogue stores row by row, which the wide tile would expose).
+constexpr int64_t kWideMinRowsPerGroup = 512;
+
+template <int EPI>
+cudaError_t launch_rows_for(const GemmArgs& a, int sm_count, cudaStream_t stream) {
+  const bool wide = a.gather_rows == nullptr && a.pre_out == nullptr &&
+                    a.rows_alloc >= kWideMinRowsPerGroup * a.G;
+  return wide ? launch_rows_wide_ffn<3, EPI>(a, sm_count, stream)
+              : launch_rows_ffn<256, 4, EPI>(a, sm_count, stream);
+}
+
+
 cudaError_t launch_tc_gemm_bf16(const GemmArgs& a, int epi, int sm_count, cudaStream_t stream) {
   // Gathered token rows exist for the first expert GEMM only.
   if (a.gather_rows && (epi != EPI_BIAS_SILU || !a.gather_src || a.gather_src_rows < 1))
     return cudaErrorInvalidValue;
   switch (epi) {
     case EPI_BIAS_SILU:
-      return a.max_group > kSmallGroup ? launch_rows_ffn<256, 4, EPI_BIAS_SILU>(a, sm_count, stream)
+      return a.max_group > kSmallGroup ? launch_rows_for<EPI_BIAS_SILU>(a, sm_count, stream)
                                        : launch_ffn_for<EPI_BIAS_SILU>(a, a.max_group, sm_count, stream);
     case EPI_BIAS:
-      return a.max_group > kSmallGroup ? launch_rows_ffn<256, 4, EPI_BIAS>(a, sm_count, stream)
+      return a.max_group > kSmallGroup ? launch_rows_for<EPI_BIAS>(a, sm_count, stream)
                                        : launch_ffn_for<EPI_BIAS>(a, a.max_group, sm_count, stream);
     default:
       switch (router_bn(a.N)) {

@@ -294,7 +294,10 @@ __device__ __forceinline__ Smem& smem_aligned() {
                                   ~static_cast<uintptr_t>(1023));
 }
 
-__device__ __forceinline__ float silu(float x) { return x / (1.f + __expf(-x)); }
+// SiLU(x) = x / (1 + e^-x) with the fast division intrinsic (within 2 ulp in fp32, far below
+// the bf16 rounding of the result; 0 when e^-x overflows, x when it underflows).  The
+// IEEE-rounded division took four times as long in the epilogue.
+__device__ __forceinline__ float silu(float x) { return __fdividef(x, 1.f + __expf(-x)); }
 
 // ------------------------------------------------------------------ host side
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {

@@ -194,6 +194,14 @@ EDGE = [
     Workload("tight_capacity_k2", T=300, d=128, h=128, E=8, k=2, dtype="bf16", gate=1,
              capacity_factor=0.5, logit_bias="normal1.5"),
     Workload("narrow_d8", T=77, d=8, h=16, E=32, k=2, dtype="bf16", gate=0, capacity_factor=0),
+    # 512 or more rows per expert on average: the 256-row tile kernel, with full tiles, a
+    # half-filled last tile, a ragged K tail (264 = 4 x 64 + 8) and a ragged last weight
+    # block (520 = 2 x 256 + 8 columns, stored row by row) ...
+    Workload("wide_tiles", T=1100, d=264, h=520, E=4, k=2, dtype="bf16", gate=1,
+             capacity_factor=0, bias_std=0.1),
+    # ... and with a capacity that drops rows (C = 564 of ~1024 per expert).
+    Workload("wide_tiles_capacity", T=1024, d=128, h=384, E=2, k=1, dtype="bf16", gate=0,
+             capacity_factor=1.1, bias_std=0.1, logit_bias="normal1.5"),
 ] + [
     # Shapes whose weights-as-M expert GEMMs split tiles between SMs (on a 148-SM B300):
     # GEMM1 here is 4 tiles of 150 k-blocks cut into ~19 pieces each (several load
