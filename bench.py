@@ -67,6 +67,15 @@ L2_FLUSH_BYTES = 256 << 20
 HEAD_START_CYCLES = 200_000
 KERNELS_PER_FORWARD = 8   # router GEMM, softmax/top-k, finalize/scan, place, row copy, GEMM1, GEMM2, combine
 KERNELS_PER_EC_FORWARD = 7  # router GEMM, softmax, per-expert select, gather, GEMM1, GEMM2, combine
+
+
+def forward_launches(w, fused_gather=False) -> int:
+    """Our kernel launches in one top-k moe_forward of workload w: a bf16 top-1 layer whose
+    expert groups fit the weights-as-M GEMMs (at most 128 rows) has no combine pass (the
+    expert GEMMs write y); with fused_gather there is no row copy."""
+    cap = math.ceil(w.T * w.capacity_factor / w.E) if w.capacity_factor > 0 else w.T
+    fused_combine = w.k == 1 and w.dtype == "bf16" and min(cap, w.T) <= 128
+    return KERNELS_PER_FORWARD - int(fused_combine) - int(bool(fused_gather))
 # moe_backward: combine and gate backward, dA / dXp / router-dx GEMMs, the dx sum, dW2 / dW1 /
 # dW_g GEMMs with two tail-packing kernels before each expert one, three two-kernel column sums
 KERNELS_PER_BACKWARD = 19
@@ -646,9 +655,8 @@ def run_ours(args, world, rank, local):
                 "serial_value": round(replica_throughput(world, w.T, ser_ms), 1),
                 "serial": "per step: x copied in, moe_forward, y copied out, no overlap "
                           "(L2 flushed before each step)"},
-        # with fused_gather the forward launches no row-copy kernel
         "gpu_launches": (KERNELS_PER_EC_FORWARD if ec else
-                         KERNELS_PER_FORWARD - (1 if args.fused_gather else 0)) * args.steps,
+                         forward_launches(w, args.fused_gather)) * args.steps,
         "clocks": clocks.summary(t0, t1) if clocks else None,
     }
     if world == 1 and not args.no_cpu_baseline:

@@ -176,7 +176,12 @@ typedef struct moe_forward_args {
      forward's copy inside the workspace; h_pre is only written when given): */
   void* x_perm;             /* [T*k,d] the gathered token rows Xp */
   void* h_act;              /* [T*k,h] H = SiLU(A), GEMM1's output */
-  void* y_perm;             /* [T*k,d] Yp, GEMM2's output */
+  void* y_perm;             /* [T*k,d] Yp, GEMM2's output.  A bf16 top-1 layer (k = 1)
+                               whose groups are at most 128 rows (T, or C under a
+                               capacity) folds the combine into the expert GEMMs when
+                               this is NULL -- GEMM2 writes each kept token's row of y,
+                               GEMM1 zeroes the dropped tokens' rows -- and then writes
+                               no Yp anywhere; y is bitwise the same either way. */
   void* h_pre;              /* [T*k,h] A = W1 x + b1, the pre-activation */
 } moe_forward_args;
 

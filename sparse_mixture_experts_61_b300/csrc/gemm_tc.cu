@@ -77,7 +77,7 @@ struct SplitK {
   __device__ __forceinline__ bool busy(int c) const { return begin(c) < begin(c + 1); }
 };
 
-template <int TB, int STAGES, int EPI, bool GATHER>
+template <int TB, int STAGES, int EPI, bool GATHER, bool TOP1>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     tc_ffn_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                   const GemmArgs p) {
@@ -204,6 +204,20 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                           p.flags);
   } else {
     const int quad = warp & 3;  // TMEM lanes this warp may read: 32*quad .. 32*quad+31
+    if constexpr (TOP1 && EPI == EPI_BIAS_SILU) {
+      // Top-1 combine, first part: zero the layer-output rows of the tokens whose slot was
+      // dropped (GEMM 2 writes every other token's row), one warp per token, while the
+      // first tiles' operands stream in.
+      const int nvec = p.comb_cols / 8;
+      uint4* y = static_cast<uint4*>(p.comb_out);
+      const int64_t nw = static_cast<int64_t>(grid) * (TC_THREADS / 32 - 2);
+      for (int64_t t = static_cast<int64_t>(cta) * (TC_THREADS / 32 - 2) + (warp - 2);
+           t < p.comb_rows; t += nw) {
+        if (p.comb_slot[t] >= 0) continue;
+        uint4* row = y + t * nvec;
+        for (int v = lane; v < nvec; v += 32) row[v] = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
     int acc = 0;
     uint32_t aph = 0;
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
@@ -222,6 +236,33 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       const int nrows = static_cast<int>(c.row_end - c.row0);
       // Bias, activation and bf16 store of feature n for token columns [col, col + 32).
       auto store = [&](int col, const float(&v)[32]) {
+        if constexpr (TOP1 && EPI == EPI_BIAS) {
+          // Top-1 combine: row i's output goes to its token's row of the layer output,
+          // scaled by the token's gate weight the way the combine scales one slot.  The
+          // 32 rows' tokens and weights are read one per lane and shared by shuffles.
+          int tk = -1;
+          float gw = 0.f;
+          if (col + lane < nrows) {
+            tk = p.comb_token[c.row0 + col + lane];
+            if (tk < 0 || tk >= p.comb_rows) {
+              raise_flag(p.flags, MOE_DEVERR_BAD_ROW);
+              tk = -1;
+            } else {
+              gw = p.comb_w[tk];
+            }
+          }
+          __nv_bfloat16* y = static_cast<__nv_bfloat16*>(p.comb_out);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int t = __shfl_sync(0xffffffffu, tk, i);
+            const float w = __shfl_sync(0xffffffffu, gw, i);
+            if (n_ok && t >= 0) {
+              const float yp = __bfloat162float(__float2bfloat16_rn(v[i] + b));
+              y[static_cast<int64_t>(t) * p.N + n] = __float2bfloat16_rn(fmaf(w, yp, 0.f));
+            }
+          }
+          return;
+        }
         if (!n_ok) return;
         __nv_bfloat16* o = out + (c.row0 + col) * p.N + n;
 #pragma unroll
@@ -873,14 +914,22 @@ cudaError_t launch_ffn(const GemmArgs& a, int sm_count, cudaStream_t stream) {
   using Smem = PipeSmem<TILE_M * TC_BK * 2, TB * TC_BK * 2, STAGES>;
   // One CTA per SM; the parked pieces and counters are sized for kMaxSmsForSizing.
   const int grid = std::min(sm_count, kMaxSmsForSizing);
+  const size_t smem = sizeof(Smem) + 1024;
+  const size_t smem_gather = smem + TB * sizeof(int) + 16;
   if constexpr (EPI == EPI_BIAS_SILU) {
+    if (a.gather_rows && a.comb_out)
+      return launch_pipe(tc_ffn_kernel<TB, STAGES, EPI, true, true>, smem_gather, grid, tmW, tmX,
+                         a, stream);
     if (a.gather_rows)
-      return launch_pipe(tc_ffn_kernel<TB, STAGES, EPI, true>,
-                         sizeof(Smem) + 1024 + TB * sizeof(int) + 16, grid, tmW, tmX, a, stream);
+      return launch_pipe(tc_ffn_kernel<TB, STAGES, EPI, true, false>, smem_gather, grid, tmW,
+                         tmX, a, stream);
   }
+  if (a.comb_out)
+    return launch_pipe(tc_ffn_kernel<TB, STAGES, EPI, false, true>, smem, grid, tmW, tmX, a,
+                       stream);
   if (a.gather_rows) return cudaErrorInvalidValue;
-  return launch_pipe(tc_ffn_kernel<TB, STAGES, EPI, false>, sizeof(Smem) + 1024, grid, tmW, tmX,
-                     a, stream);
+  return launch_pipe(tc_ffn_kernel<TB, STAGES, EPI, false, false>, sizeof(Smem) + 1024, grid,
+                     tmW, tmX, a, stream);
 }
 
 template <int BN, int STAGES, int EPI>
@@ -995,8 +1044,13 @@ cudaError_t launch_rows_for(const GemmArgs& a, int sm_count, cudaStream_t stream
 
 
 cudaError_t launch_tc_gemm_bf16(const GemmArgs& a, int epi, int sm_count, cudaStream_t stream) {
-  // Gathered token rows exist for the first expert GEMM only.
+  // Gathered token rows exist for the first expert GEMM only, the fused top-1 combine for
+  // the second on the weights-as-M kernel only.
   if (a.gather_rows && (epi != EPI_BIAS_SILU || !a.gather_src || a.gather_src_rows < 1))
+    return cudaErrorInvalidValue;
+  if (a.comb_out &&
+      (a.max_group > kSmallGroup || a.comb_rows < 1 || a.comb_cols < 8 || a.comb_cols % 8 ||
+       (epi == EPI_BIAS ? !a.comb_token || !a.comb_w : epi == EPI_BIAS_SILU ? !a.comb_slot : true)))
     return cudaErrorInvalidValue;
   switch (epi) {
     case EPI_BIAS_SILU:

@@ -99,6 +99,19 @@ struct GemmArgs {
   const int32_t* gather_rows;
   const void* gather_src;
   int64_t gather_src_rows;
+  // The combine of a top-1 layer folded into the weights-as-M expert GEMMs (comb_token
+  // given; comb_out is the layer output [comb_rows, comb_cols]).  GEMM 2: row r's output
+  // goes to comb_out at row comb_token[r] (the row -> token map), scaled by that token's
+  // gate weight comb_w[token] exactly as the combine scales its one slot (fma(w, output
+  // rounded to bf16, 0), rounded to bf16), instead of to out.  GEMM 1: its epilogue warps
+  // first set to zero the comb_out rows of the tokens whose slot comb_slot[token] was
+  // dropped (-1), while the first tiles' operands stream in.
+  const int32_t* comb_token;
+  const float* comb_w;
+  const int32_t* comb_slot;
+  void* comb_out;
+  int64_t comb_rows;
+  int comb_cols;
 };
 
 // K splits of the bf16 router contraction for T tokens, E experts, model width d on a

@@ -61,6 +61,20 @@ int64_t max_group_of(const moe_config& c) {
   return C >= 0 && C < c.T ? C : c.T;
 }
 
+// Top-1 bf16 layers whose expert groups fit the weights-as-M GEMMs get the combine folded
+// into the expert GEMMs in moe_forward (with k = 1 the combine only scales and moves rows):
+// GEMM 1 zeroes the output rows of dropped tokens, GEMM 2 writes the others.
+bool fused_top1_combine(const moe_config& c) {
+  return c.k == 1 && c.dtype == MOE_BF16 && max_group_of(c) <= kSmallGroup;
+}
+
+struct TopOneCombine {
+  const int32_t* row_token;  // [T*k] row -> token
+  const float* w;            // [T] gate weights
+  const int32_t* slot_row;   // [T] token -> row, -1 when dropped
+  void* y;                   // [T, d] layer output
+};
+
 Layout make_layout(const moe_config& c) {
   Layout L{};
   const int64_t T = c.T, E = c.E, k = c.k;
@@ -214,7 +228,8 @@ moe_status run_expert_ffn_rows(const moe_config& c, int64_t rows_alloc, int64_t 
                                const void* b1, const void* w2, const void* b2, void* h_buf,
                                void* y_perm, int* flags, int* sk_ctr, float* sk_part, int sms,
                                cudaStream_t st, void* h_pre = nullptr,
-                               const int32_t* gather_rows = nullptr, const void* x = nullptr) {
+                               const int32_t* gather_rows = nullptr, const void* x = nullptr,
+                               const TopOneCombine* top1 = nullptr) {
   GemmArgs g1{};
   g1.A = x_perm;
   g1.pre_out = h_pre;
@@ -233,6 +248,14 @@ moe_status run_expert_ffn_rows(const moe_config& c, int64_t rows_alloc, int64_t 
   g1.gather_rows = gather_rows;
   g1.gather_src = x;
   g1.gather_src_rows = c.T;
+  if (top1) {
+    g1.comb_token = top1->row_token;
+    g1.comb_w = top1->w;
+    g1.comb_slot = top1->slot_row;
+    g1.comb_out = top1->y;
+    g1.comb_rows = c.T;
+    g1.comb_cols = c.d;
+  }
   GemmArgs g2 = g1;
   g2.sk_ctr = sk_ctr + kSplitCounters;
   g2.gather_rows = nullptr;
@@ -260,10 +283,11 @@ moe_status run_expert_ffn(const moe_config& c, const Layout& L, void* ws, const 
                           const int32_t* offsets, const void* w1, const void* b1, const void* w2,
                           const void* b2, void* h_buf, void* y_perm, int* flags, int sms,
                           cudaStream_t st, void* h_pre = nullptr,
-                          const int32_t* gather_rows = nullptr, const void* x = nullptr) {
+                          const int32_t* gather_rows = nullptr, const void* x = nullptr,
+                          const TopOneCombine* top1 = nullptr) {
   return run_expert_ffn_rows(c, c.T * c.k, max_group_of(c), x_perm, offsets, w1, b1, w2, b2, h_buf,
                              y_perm, flags, at<int>(ws, L.split_ctr), at<float>(ws, L.split_part),
-                             sms, st, h_pre, gather_rows, x);
+                             sms, st, h_pre, gather_rows, x, top1);
 }
 
 // ---------------------------------------------------------------- expert choice
@@ -531,6 +555,10 @@ moe_status moe::forward_entry(const moe_config* cfg, const moe_forward_args* a, 
   // cfg->fused_gather: GEMM1 reads the token rows from x by row_token, and no expert-ordered
   // copy exists (unless the caller asked for one in x_perm).
   const bool gather = c.fused_gather && a->x_perm == nullptr;
+  // A bf16 top-1 layer on the weights-as-M GEMMs: GEMM2 writes each kept token's output row
+  // itself (the combine's one-slot arithmetic), GEMM1 zeroes the other tokens' rows, and
+  // there is no combine pass -- unless the caller asked for Yp in y_perm.
+  const bool fuse_combine = fused_top1_combine(c) && a->y_perm == nullptr;
   {
     MOE_TRACE("moe_forward: dispatch");
     MOE_CUDA(launch_dispatch_place(c.dtype, idx, c.T, c.E, c.k, C, chunk_base, offsets, slot_row,
@@ -538,12 +566,13 @@ moe_status moe::forward_entry(const moe_config* cfg, const moe_forward_args* a, 
   }
   {
     MOE_TRACE("moe_forward: expert_ffn");
+    const TopOneCombine top1{row_token, w, slot_row, a->y};
     if ((s = run_expert_ffn(c, L, ws, x_perm, offsets, a->w1, a->b1, a->w2, a->b2, h_buf, y_perm,
                             flags, sms, st, a->h_pre, gather ? row_token : nullptr,
-                            gather ? a->x : nullptr)) != MOE_OK)
+                            gather ? a->x : nullptr, fuse_combine ? &top1 : nullptr)) != MOE_OK)
       return s;
   }
-  {
+  if (!fuse_combine) {
     MOE_TRACE("moe_forward: combine");
     MOE_CUDA(launch_combine(c.dtype, y_perm, slot_row, w, c.T, c.d, c.k, a->y, flags, st));
   }

@@ -306,6 +306,45 @@ def test_fused_gather_full_size(name):
     assert torch.equal(outs["y"], y0)
 
 
+TOP1 = [w for w in list(PARITY_WORKLOADS.values()) + EDGE if w.k == 1 and w.dtype == "bf16"]
+
+
+@pytest.mark.parametrize("w", TOP1, ids=[w.name for w in TOP1])
+def test_top1_combine_in_gemm2_is_bitwise_the_combine(w):
+    """A bf16 top-1 forward writes y from GEMM2's epilogue and zeroes the rows of tokens
+    with no kept slot in the dispatch (split tiles included); a forward asked for y_perm
+    runs the separate combine pass instead.  Same bits everywhere, from an all-NaN y."""
+    dev = tl.to_device(make_inputs(w, seed=5))
+    a = tl.run_forward(w, dev)
+    assert a["flags"] == 0
+    outs = tl.alloc_outputs(w, "cuda")
+    outs["y_perm"] = torch.empty((w.T * w.k, w.d), dtype=w.torch_dtype, device="cuda")
+    b = tl.run_forward(w, dev, outs=outs)
+    assert b["flags"] == 0
+    ya, yb = tl.host(a["outs"])["y"], tl.host(b["outs"])["y"]
+    assert not np.isnan(ya).any()
+    np.testing.assert_array_equal(ya, yb)
+    dropped = (tl.host(a["outs"])["slot_row"] < 0).all(axis=1)
+    assert (ya[dropped] == 0).all()
+
+
+def test_top1_combine_in_gemm2_full_size():
+    """The same on the 128-expert Switch layer at the benchmark's size (most tokens
+    dropped by the capacity)."""
+    w = WORKLOADS["switch_capacity"]
+    inp = make_inputs(w, seed=0, device="cuda")
+    cfg = moe.config_from_workload(w)
+    ws = torch.empty(moe.moe_workspace_size(cfg), dtype=torch.uint8, device="cuda")
+    y0 = torch.full((w.T, w.d), float("nan"), dtype=w.torch_dtype, device="cuda")
+    moe.moe_forward(cfg, inp, dict(y=y0), ws)
+    assert moe.moe_device_error(ws) == 0
+    y1 = torch.full_like(y0, float("nan"))
+    yp = torch.empty((w.T * w.k, w.d), dtype=w.torch_dtype, device="cuda")
+    moe.moe_forward(cfg, inp, dict(y=y1, y_perm=yp), ws)
+    assert moe.moe_device_error(ws) == 0
+    assert torch.equal(y0, y1)
+
+
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_all_ties_and_drop_storm(dtype):
     """W_g = 0: every logit ties, so every token picks experts 0..k-1; with capacity 1.25
