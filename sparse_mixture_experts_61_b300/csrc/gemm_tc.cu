@@ -208,14 +208,21 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       // Top-1 combine, first part: zero the layer-output rows of the tokens whose slot was
       // dropped (GEMM 2 writes every other token's row), one warp per token, while the
       // first tiles' operands stream in.
+      // A warp takes 32 consecutive tokens at a time: their slots are read one per lane in
+      // a single round trip, then the dropped tokens' rows are written.
       const int nvec = p.comb_cols / 8;
       uint4* y = static_cast<uint4*>(p.comb_out);
-      const int64_t nw = static_cast<int64_t>(grid) * (TC_THREADS / 32 - 2);
-      for (int64_t t = static_cast<int64_t>(cta) * (TC_THREADS / 32 - 2) + (warp - 2);
-           t < p.comb_rows; t += nw) {
-        if (p.comb_slot[t] >= 0) continue;
-        uint4* row = y + t * nvec;
-        for (int v = lane; v < nvec; v += 32) row[v] = make_uint4(0u, 0u, 0u, 0u);
+      const int64_t nw = static_cast<int64_t>(grid) * (TC_THREADS / 32 - 2) * 32;
+      for (int64_t t0 = (static_cast<int64_t>(cta) * (TC_THREADS / 32 - 2) + (warp - 2)) * 32;
+           t0 < p.comb_rows; t0 += nw) {
+        const int64_t t = t0 + lane;
+        unsigned drop = __ballot_sync(0xffffffffu, t < p.comb_rows && p.comb_slot[t] < 0);
+        while (drop) {
+          const int i = __ffs(drop) - 1;
+          drop &= drop - 1;
+          uint4* row = y + (t0 + i) * nvec;
+          for (int v = lane; v < nvec; v += 32) row[v] = make_uint4(0u, 0u, 0u, 0u);
+        }
       }
     }
     int acc = 0;
@@ -228,6 +235,25 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       const bool n_ok = n < p.N;
       const float b = (bias && n_ok) ? __bfloat162float(bias[static_cast<int64_t>(c.g) * p.N + n])
                                      : 0.f;
+      // Top-1 combine: the tokens and gate weights of the tile's rows, one per lane for each
+      // 32-row chunk, read before the accumulator is ready.
+      int tok[TB / 32];
+      float gate[TB / 32];
+      if constexpr (TOP1 && EPI == EPI_BIAS) {
+#pragma unroll
+        for (int j = 0; j < TB / 32; ++j) {
+          const int64_t r = c.row0 + 32 * j + lane;
+          tok[j] = r < c.row_end ? p.comb_token[r] : -1;
+        }
+#pragma unroll
+        for (int j = 0; j < TB / 32; ++j) {
+          if (tok[j] >= p.comb_rows || (tok[j] < 0 && c.row0 + 32 * j + lane < c.row_end)) {
+            raise_flag(p.flags, MOE_DEVERR_BAD_ROW);
+            tok[j] = -1;
+          }
+          gate[j] = tok[j] >= 0 ? p.comb_w[tok[j]] : 0.f;
+        }
+      }
       const bool got = mbar_wait_bounded(smem_u32(&S.tfull[acc]), aph, abort, p.flags);
       if (!__all_sync(0xffffffffu, got)) break;  // the warp-collective loads need every lane
       tc_fence_after();
@@ -239,18 +265,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         if constexpr (TOP1 && EPI == EPI_BIAS) {
           // Top-1 combine: row i's output goes to its token's row of the layer output,
           // scaled by the token's gate weight the way the combine scales one slot.  The
-          // 32 rows' tokens and weights are read one per lane and shared by shuffles.
+          // 32 rows' tokens and weights (read ahead, one per lane) are shared by shuffles.
           int tk = -1;
           float gw = 0.f;
-          if (col + lane < nrows) {
-            tk = p.comb_token[c.row0 + col + lane];
-            if (tk < 0 || tk >= p.comb_rows) {
-              raise_flag(p.flags, MOE_DEVERR_BAD_ROW);
-              tk = -1;
-            } else {
-              gw = p.comb_w[tk];
+#pragma unroll
+          for (int j = 0; j < TB / 32; ++j)
+            if (col == 32 * j) {
+              tk = tok[j];
+              gw = gate[j];
             }
-          }
           __nv_bfloat16* y = static_cast<__nv_bfloat16*>(p.comb_out);
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
