@@ -275,13 +275,23 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
               gw = gate[j];
             }
           __nv_bfloat16* y = static_cast<__nv_bfloat16*>(p.comb_out);
+          // Eight rows' tokens and weights are shuffled out together, then stored, so the
+          // shuffles' latency is not paid row by row.
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int t = __shfl_sync(0xffffffffu, tk, i);
-            const float w = __shfl_sync(0xffffffffu, gw, i);
-            if (n_ok && t >= 0) {
-              const float yp = __bfloat162float(__float2bfloat16_rn(v[i] + b));
-              y[static_cast<int64_t>(t) * p.N + n] = __float2bfloat16_rn(fmaf(w, yp, 0.f));
+          for (int i0 = 0; i0 < 32; i0 += 8) {
+            int t8[8];
+            float w8[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              t8[u] = __shfl_sync(0xffffffffu, tk, i0 + u);
+              w8[u] = __shfl_sync(0xffffffffu, gw, i0 + u);
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              if (n_ok && t8[u] >= 0) {
+                const float yp = __bfloat162float(__float2bfloat16_rn(v[i0 + u] + b));
+                y[static_cast<int64_t>(t8[u]) * p.N + n] = __float2bfloat16_rn(fmaf(w8[u], yp, 0.f));
+              }
             }
           }
           return;
