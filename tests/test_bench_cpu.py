@@ -69,3 +69,26 @@ def test_traffic_figure_is_dropped_when_the_gemm_sources_change(monkeypatch):
     assert bench.ncu_traffic(name)[0] == bench.NCU_TRAFFIC_BYTES[name][1]
     monkeypatch.setattr(bench, "gemm_source_hash", lambda: "0" * 16)
     assert bench.ncu_traffic(name) == (None, None)
+
+
+def test_forward_launch_count():
+    """gpu_launches counts the forward's own kernels: eight, one fewer on a bf16 top-1 layer
+    whose groups fit the weights-as-M GEMMs (the combine is folded into them), and one fewer
+    again with fused_gather (no row copy)."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from moe_workloads import WORKLOADS, Workload
+
+    assert bench.forward_launches(WORKLOADS["mixtral_prefill"]) == 8
+    assert bench.forward_launches(WORKLOADS["decode"]) == 8
+    assert bench.forward_launches(WORKLOADS["switch_capacity"]) == 7  # C = 80 rows
+    assert bench.forward_launches(WORKLOADS["switch_capacity"], fused_gather=True) == 6
+    assert bench.forward_launches(WORKLOADS["mixtral_prefill"], fused_gather=True) == 7
+    # top-1 with groups above 128 rows, and top-1 in fp32 (groups of at most 64 rows), keep
+    # the combine pass
+    big = Workload("top1_big", T=4096, d=256, h=512, E=8, k=1, dtype="bf16", gate=1,
+                   capacity_factor=0.0)
+    assert bench.forward_launches(big) == 8
+    f32 = Workload("top1_f32", T=64, d=64, h=128, E=8, k=1, dtype="f32", gate=1,
+                   capacity_factor=0.0)
+    assert bench.forward_launches(f32) == 8
