@@ -88,13 +88,13 @@ D_AUX = 0.01
 # 32 or 8 experts) and scaled by the algorithmic bytes.  A figure whose hash differs from
 # the current sources' (gemm_source_hash) is stale and reported as null.
 NCU_TRAFFIC_BYTES = {
-    "mixtral_prefill": ("53b1224660659a3c", 2998012672, "captured at full size"),
-    "switch_capacity": ("53b1224660659a3c", 158926080,
+    "mixtral_prefill": ("cbf75181ceb343bf", 2965290752, "captured at full size"),
+    "switch_capacity": ("cbf75181ceb343bf", 159500288,
                         "captured at full size (the forward's GEMMs, combine folded in)"),
-    "deepseek_fine": ("53b1224660659a3c", 17520529408,
-                      "deepseek_fine_e32 capture (1.0039 x its algorithmic bytes), scaled"),
-    "decode": ("53b1224660659a3c", 4506690190,
-               "decode_e8 capture (1.0076 x its algorithmic bytes), scaled"),
+    "deepseek_fine": ("cbf75181ceb343bf", 17516703744,
+                      "deepseek_fine_e32 capture (1.0036 x its algorithmic bytes), scaled"),
+    "decode": ("cbf75181ceb343bf", 4500414010,
+               "decode_e8 capture (1.0062 x its algorithmic bytes), scaled"),
 }
 GEMM_SOURCES = ("sparse_mixture_experts_61_b300/csrc/gemm_tc.cu",
                 "sparse_mixture_experts_61_b300/csrc/tc_pipe.cuh",
