@@ -202,6 +202,10 @@ EDGE = [
     # ... and with a capacity that drops rows (C = 564 of ~1024 per expert).
     Workload("wide_tiles_capacity", T=1024, d=128, h=384, E=2, k=1, dtype="bf16", gate=0,
              capacity_factor=1.1, bias_std=0.1, logit_bias="normal1.5"),
+    # Weights-as-M groups of 65-128 rows (C = 100): token tiles of two 64-row boxes, the
+    # second partly past the group; top-1, so the combine is folded into the GEMMs.
+    Workload("two_token_boxes", T=400, d=192, h=320, E=4, k=1, dtype="bf16", gate=1,
+             capacity_factor=1.0, bias_std=0.1),
 ] + [
     # Shapes whose weights-as-M expert GEMMs split tiles between SMs (on a 148-SM B300):
     # GEMM1 here is 4 tiles of 150 k-blocks cut into ~19 pieces each (several load
